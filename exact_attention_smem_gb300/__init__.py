@@ -1,0 +1,51 @@
+"""Exact scaled-dot-product attention for GB300 (sm_103a), behind a small C ABI.
+
+``fa_fwd`` / ``fa_bwd`` and friends mirror include/fa.h one to one (see
+``_lib``). ``forward`` and ``backward`` are conveniences that allocate outputs
+and workspace with torch and call them; torch is used for device memory and
+streams only.
+"""
+from __future__ import annotations
+
+import math
+
+from ._lib import (FAError, fa_bwd, fa_bwd_workspace_bytes, fa_debug_set,  # noqa: F401
+                   fa_exp2_poly_host, fa_fwd, fa_get_device_error, fa_sched_list, fa_test_exp2,
+                   fa_test_mma, fa_test_wait_timeout, load)
+
+
+def _dims(q, k, cu_seqlens):
+    if cu_seqlens is not None:
+        T, Hq, d = q.shape
+        return cu_seqlens.numel() - 1, Hq, k.shape[1], T, k.shape[0], d
+    B, Sq, Hq, d = q.shape
+    return B, Hq, k.shape[2], Sq, k.shape[1], d
+
+
+def forward(q, k, v, causal=False, scale=None, cu_seqlens=None, out=None, lse=None, stream=None):
+    """O, LSE for bf16 q/k/v ([B,S,H,d] dense or [T,H,d] packed with int32 cu_seqlens)."""
+    import torch
+    B, Hq, Hkv, Sq, Sk, d = _dims(q, k, cu_seqlens)
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        shape = (Hq, Sq) if cu_seqlens is not None else (B, Hq, Sq)
+        lse = torch.empty(shape, dtype=torch.float32, device=q.device)
+    fa_fwd(q, k, v, out, lse, B, Hq, Hkv, Sq, Sk, d, causal, scale, cu_seqlens, stream)
+    return out, lse
+
+
+def backward(q, k, v, o, lse, dout, causal=False, scale=None, cu_seqlens=None, workspace=None,
+             stream=None):
+    """dQ, dK, dV (bf16) for the forward above."""
+    import torch
+    B, Hq, Hkv, Sq, Sk, d = _dims(q, k, cu_seqlens)
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    nbytes = fa_bwd_workspace_bytes(B, Hq, Sq, d, Sq if cu_seqlens is not None else 0)
+    if workspace is None or workspace.numel() < nbytes:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, Sq, Sk, d, causal, scale, cu_seqlens,
+           workspace, nbytes, stream)
+    return dq, dk, dv

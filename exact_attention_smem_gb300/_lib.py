@@ -1,0 +1,152 @@
+"""ctypes binding of the C ABI in include/fa.h (argument marshalling only).
+
+Every function keeps the C name and argument order; tensors are passed as
+torch tensors (their device pointers are handed to the library) and `stream`
+as a torch.cuda.Stream or None (the current stream). No computation happens
+here: the attention path runs entirely in the library's CUDA kernels, and the
+library must be present — there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libfa_gb300.so")
+
+_lib = None
+
+FA_OK = 0
+FA_ERR_INVALID_ARG = 1
+FA_ERR_UNSUPPORTED = 2
+FA_ERR_ARCH = 3
+FA_ERR_CUDA = 4
+FA_ERR_WORKSPACE = 5
+FA_ERR_TIMEOUT = 6
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_F = ctypes.c_float
+
+_SIGS = {
+    "fa_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P]),
+    "fa_bwd_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I, _I]),
+    "fa_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P,
+                    ctypes.c_size_t, _P]),
+    "fa_status_string": (ctypes.c_char_p, [_I]),
+    "fa_last_error": (ctypes.c_char_p, []),
+    "fa_get_device_error": (_I, [ctypes.POINTER(_I), _I]),
+    "fa_debug_set": (_I, [ctypes.c_char_p, ctypes.c_double]),
+    "fa_test_exp2": (_I, [_P, _P, _I, _I, _P]),
+    "fa_exp2_poly_host": (_F, [_F]),
+    "fa_test_mma": (_I, [_P, _P, _P, _I, _I, _P]),
+    "fa_test_wait_timeout": (_I, [_P, ctypes.c_double, _P]),
+    "fa_sched_list": (_I, [_I, _I, _P, _I, _I, _I, _I, _I, _I, _P, _I]),
+}
+
+
+class FAError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        lib = load()
+        msg = lib.fa_status_string(status).decode()
+        detail = lib.fa_last_error().decode()
+        super().__init__(f"{where}: {msg} ({status}){': ' + detail if detail else ''}")
+        self.status = status
+
+
+def load():
+    """Load the library (built by exact_attention_smem_gb300.build); raise if missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(
+            f"{LIB_PATH} is missing: build it with `python -m exact_attention_smem_gb300.build` "
+            "(the attention path has no fallback)")
+    lib = ctypes.CDLL(LIB_PATH)
+    for name, (res, args) in _SIGS.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def exported_symbols():
+    return list(_SIGS)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(status, where):
+    if status != FA_OK:
+        raise FAError(status, where)
+
+
+def fa_fwd(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, d, causal, scale, cu_seqlens=None, stream=None):
+    _check(load().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Sq, Sk, d,
+                         int(causal), float(scale), _ptr(cu_seqlens), _stream(stream)), "fa_fwd")
+
+
+def fa_bwd_workspace_bytes(B, Hq, Sq, d, total_q=0):
+    return int(load().fa_bwd_workspace_bytes(B, Hq, Sq, d, total_q))
+
+
+def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, Sq, Sk, d, causal, scale,
+           cu_seqlens, workspace, workspace_bytes, stream=None):
+    _check(load().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq),
+                         _ptr(dk), _ptr(dv), B, Hq, Hkv, Sq, Sk, d, int(causal), float(scale),
+                         _ptr(cu_seqlens), _ptr(workspace), int(workspace_bytes),
+                         _stream(stream)), "fa_bwd")
+
+
+def fa_get_device_error(clear=True):
+    code = ctypes.c_int(0)
+    _check(load().fa_get_device_error(ctypes.byref(code), int(clear)), "fa_get_device_error")
+    return code.value
+
+
+def fa_debug_set(key, value):
+    _check(load().fa_debug_set(key.encode(), float(value)), "fa_debug_set")
+
+
+def fa_test_exp2(x, y, mode, stream=None):
+    _check(load().fa_test_exp2(_ptr(x), _ptr(y), x.numel(), mode, _stream(stream)), "fa_test_exp2")
+
+
+def fa_exp2_poly_host(x: float) -> float:
+    return float(load().fa_exp2_poly_host(x))
+
+
+def fa_test_mma(A, B, C, mode, N, stream=None):
+    _check(load().fa_test_mma(_ptr(A), _ptr(B), _ptr(C), mode, N, _stream(stream)), "fa_test_mma")
+
+
+def fa_test_wait_timeout(status_dev, timeout_ms, stream=None):
+    _check(load().fa_test_wait_timeout(_ptr(status_dev), float(timeout_ms), _stream(stream)),
+           "fa_test_wait_timeout")
+
+
+def fa_sched_list(kind, B, cu_seqlens_host, Sq, Sk, heads, causal, grid, cta):
+    """Return the (seq, row block, head, cost) units of one CTA, in order."""
+    lib = load()
+    cu = None
+    if cu_seqlens_host is not None:
+        arr = (ctypes.c_int * len(cu_seqlens_host))(*[int(x) for x in cu_seqlens_host])
+        cu = ctypes.cast(arr, ctypes.c_void_p)
+    n = lib.fa_sched_list(kind, B, cu, Sq, Sk, heads, int(causal), grid, cta, None, 0)
+    if n < 0:
+        raise ValueError("fa_sched_list: bad arguments")
+    out = (ctypes.c_int * (4 * max(n, 1)))()
+    lib.fa_sched_list(kind, B, cu, Sq, Sk, heads, int(causal), grid, cta,
+                      ctypes.cast(out, ctypes.c_void_p), n)
+    return [tuple(out[4 * i:4 * i + 4]) for i in range(n)]

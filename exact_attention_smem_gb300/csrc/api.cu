@@ -1,0 +1,392 @@
+// C ABI (include/fa.h): argument validation, TMA descriptor encoding, device
+// property caching and kernel launches. Nothing here allocates device memory.
+#include "../../include/fa.h"
+#include "exp2_poly.cuh"
+#include "internal.h"
+#include "sched.cuh"
+
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+namespace fa {
+
+cudaError_t launch_exp2_probe(const float* x, float* y, int n, int mode, cudaStream_t st);
+cudaError_t launch_mma_probe(const __nv_bfloat16* A, const __nv_bfloat16* B, float* C, int mode,
+                             int N, cudaStream_t st);
+cudaError_t launch_wait_timeout_probe(int* status, unsigned long long timeout_ns,
+                                      cudaStream_t st);
+
+__device__ int g_error_word;  // first expired bounded wait (site code), per device
+
+namespace {
+
+thread_local std::string t_last_error;
+
+int fail(int status, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  t_last_error = buf;
+  return status;
+}
+
+std::mutex g_mu;
+Knobs g_knobs;
+
+struct DevInfo {
+  bool init = false;
+  int sms = 0, major = 0, minor = 0;
+  int* err_word = nullptr;
+};
+DevInfo g_dev[64];
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int device_info(DevInfo** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(FA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= 64) return fail(FA_ERR_CUDA, "device index %d out of range", dev);
+  std::lock_guard<std::mutex> lk(g_mu);
+  DevInfo& di = g_dev[dev];
+  if (!di.init) {
+    cudaDeviceProp prop;
+    e = cudaGetDeviceProperties(&prop, dev);
+    if (e != cudaSuccess)
+      return fail(FA_ERR_CUDA, "cudaGetDeviceProperties: %s", cudaGetErrorString(e));
+    di.sms = prop.multiProcessorCount;
+    di.major = prop.major;
+    di.minor = prop.minor;
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_error_word);
+    if (e != cudaSuccess)
+      return fail(FA_ERR_CUDA, "cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+    di.err_word = static_cast<int*>(p);
+    if (!g_encode) {
+      cudaDriverEntryPointQueryResult q;
+      void* fn = nullptr;
+      e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                           &q);
+      if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+        return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    di.init = true;
+  }
+  if (di.major != 10 || di.minor != 3)
+    return fail(FA_ERR_ARCH, "device compute capability %d.%d; this library is built for 10.3 "
+                "(sm_103a)", di.major, di.minor);
+  *out = &di;
+  return FA_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// [rows, heads, d] bf16 view, boxes of 64 columns x 1 head x 128 rows, 128B swizzle.
+int encode_rows(CUtensorMap* tm, const void* ptr, long long rows, int heads, int d) {
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)rows};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)heads * d * 2};
+  cuuint32_t box[3] = {64, 1, 128};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return FA_OK;
+}
+
+struct Shape {
+  long long Tq, Tk;  // rows of the flattened q / k tensors
+  bool packed;
+};
+
+int validate_common(const void* const* ptrs, int nptrs, int B, int Hq, int Hkv, int Sq, int Sk,
+                    int d, float scale, const int* cu, Shape* sh) {
+  for (int i = 0; i < nptrs; ++i) {
+    if (!ptrs[i]) return fail(FA_ERR_INVALID_ARG, "tensor pointer %d is NULL", i);
+    if (!aligned16(ptrs[i]))
+      return fail(FA_ERR_INVALID_ARG, "tensor pointer %d is not 16-byte aligned", i);
+  }
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || Sq < 0 || Sk < 0)
+    return fail(FA_ERR_INVALID_ARG, "bad sizes B=%d Hq=%d Hkv=%d Sq=%d Sk=%d", B, Hq, Hkv, Sq, Sk);
+  if (Hq % Hkv != 0) return fail(FA_ERR_INVALID_ARG, "Hq (%d) %% Hkv (%d) != 0", Hq, Hkv);
+  if (d != 64 && d != 128) return fail(FA_ERR_UNSUPPORTED, "head dim %d (supported: 64, 128)", d);
+  if (!std::isfinite(scale) || !(scale > 0.f))
+    return fail(FA_ERR_INVALID_ARG, "scale must be finite and > 0");
+  if (cu) {
+    if (Sq != Sk)
+      return fail(FA_ERR_INVALID_ARG, "packed layout: Sq and Sk must both equal the packed "
+                  "row count T (got %d, %d)", Sq, Sk);
+    sh->Tq = sh->Tk = Sq;
+    sh->packed = true;
+  } else {
+    sh->Tq = (long long)B * Sq;
+    sh->Tk = (long long)B * Sk;
+    sh->packed = false;
+  }
+  if (sh->Tq > (1ll << 31) - 512 || sh->Tk > (1ll << 31) - 512)
+    return fail(FA_ERR_INVALID_ARG, "too many rows");
+  return FA_OK;
+}
+
+}  // namespace
+
+Knobs knobs_snapshot() {
+  std::lock_guard<std::mutex> lk(g_mu);
+  return g_knobs;
+}
+
+int num_sms() {
+  DevInfo* di = nullptr;
+  return device_info(&di) == FA_OK ? di->sms : 0;
+}
+
+int* device_error_word() {
+  DevInfo* di = nullptr;
+  return device_info(&di) == FA_OK ? di->err_word : nullptr;
+}
+
+}  // namespace fa
+
+using namespace fa;
+
+extern "C" int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                      int Hq, int Hkv, int Sq, int Sk, int d, int causal, float scale,
+                      const int* cu_seqlens, void* stream) {
+  t_last_error.clear();
+  const void* ptrs[5] = {q, k, v, o, lse};
+  Shape sh;
+  int st = validate_common(ptrs, 5, B, Hq, Hkv, Sq, Sk, d, scale, cu_seqlens, &sh);
+  if (st != FA_OK) return st;
+  if (B == 0 || sh.Tq == 0) return FA_OK;
+  DevInfo* di = nullptr;
+  if ((st = device_info(&di)) != FA_OK) return st;
+  const Knobs kn = knobs_snapshot();
+
+  FwdParams p;
+  memset(&p, 0, sizeof(p));
+  if ((st = encode_rows(&p.tm_q, q, sh.Tq, Hq, d)) != FA_OK) return st;
+  if (sh.Tk > 0) {
+    if ((st = encode_rows(&p.tm_k, k, sh.Tk, Hkv, d)) != FA_OK) return st;
+    if ((st = encode_rows(&p.tm_v, v, sh.Tk, Hkv, d)) != FA_OK) return st;
+  } else {
+    // no keys at all: every row is fully masked; maps are never used by the TMA
+    if ((st = encode_rows(&p.tm_k, q, sh.Tq, Hq, d)) != FA_OK) return st;
+    if ((st = encode_rows(&p.tm_v, q, sh.Tq, Hq, d)) != FA_OK) return st;
+  }
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.lse = lse;
+  p.cu = cu_seqlens;
+  p.nseq = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.Sq = Sq;
+  p.Sk = Sk;
+  p.total_q = (int)sh.Tq;
+  p.causal = causal ? 1 : 0;
+  p.lse_hstride = sh.packed ? (int)sh.Tq : Sq;
+  p.lse_seqstride = sh.packed ? 0 : (long long)Hq * Sq;
+  p.scale_log2 = (float)((double)scale * 1.4426950408889634);
+  p.tau = kn.tau_log2;
+  p.err = di->err_word;
+  p.timeout_ns = (unsigned long long)kn.timeout_ns;
+
+  // persistent grid: one CTA per SM, capped by an upper bound on the unit count
+  long long units;
+  if (sh.packed)
+    units = (long long)Hq * ((sh.Tq + 255) / 256 + B);
+  else
+    units = (long long)Hq * B * ((Sq + 255) / 256);
+  int grid = kn.grid_override > 0 ? kn.grid_override : di->sms;
+  if (units < grid) grid = (int)units;
+  if (grid < 1) grid = 1;
+  cudaError_t e = launch_fwd(p, d, grid, static_cast<cudaStream_t>(stream), kn.poly8);
+  if (e != cudaSuccess) return fail(FA_ERR_CUDA, "forward launch: %s", cudaGetErrorString(e));
+  return FA_OK;
+}
+
+extern "C" size_t fa_bwd_workspace_bytes(int B, int Hq, int Sq, int d, int total_q) {
+  if (B < 0 || Hq <= 0 || Sq < 0 || d <= 0 || total_q < 0) return 0;
+  const size_t T = total_q > 0 ? (size_t)total_q : (size_t)B * (size_t)Sq;
+  auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+  return up(T * Hq * d * sizeof(float)) + 2 * up(T * Hq * sizeof(float));
+}
+
+extern "C" int fa_bwd(const void* q, const void* k, const void* v, const void* o,
+                      const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
+                      int Hq, int Hkv, int Sq, int Sk, int d, int causal, float scale,
+                      const int* cu_seqlens, void* workspace, size_t workspace_bytes,
+                      void* stream) {
+  t_last_error.clear();
+  const void* ptrs[9] = {q, k, v, o, lse, dout, dq, dk, dv};
+  Shape sh;
+  int st = validate_common(ptrs, 9, B, Hq, Hkv, Sq, Sk, d, scale, cu_seqlens, &sh);
+  if (st != FA_OK) return st;
+  if (B == 0 || (sh.Tq == 0 && sh.Tk == 0)) return FA_OK;
+  const size_t need = fa_bwd_workspace_bytes(B, Hq, Sq, d, sh.packed ? (int)sh.Tq : 0);
+  if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return fail(FA_ERR_WORKSPACE, "workspace must be >= %zu bytes and 256-byte aligned", need);
+  DevInfo* di = nullptr;
+  if ((st = device_info(&di)) != FA_OK) return st;
+  const Knobs kn = knobs_snapshot();
+
+  BwdParams p;
+  memset(&p, 0, sizeof(p));
+  const long long Tq = sh.Tq > 0 ? sh.Tq : 1, Tk = sh.Tk > 0 ? sh.Tk : 1;
+  if ((st = encode_rows(&p.tm_q, q, Tq, Hq, d)) != FA_OK) return st;
+  if ((st = encode_rows(&p.tm_do, dout, Tq, Hq, d)) != FA_OK) return st;
+  if ((st = encode_rows(&p.tm_k, k, Tk, Hkv, d)) != FA_OK) return st;
+  if ((st = encode_rows(&p.tm_v, v, Tk, Hkv, d)) != FA_OK) return st;
+  auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+  char* ws = static_cast<char*>(workspace);
+  const size_t T = (size_t)sh.Tq;
+  p.dq_acc = reinterpret_cast<float*>(ws);
+  p.lse_log2 = reinterpret_cast<float*>(ws + up(T * Hq * d * sizeof(float)));
+  p.delta = reinterpret_cast<float*>(ws + up(T * Hq * d * sizeof(float)) +
+                                     up(T * Hq * sizeof(float)));
+  p.dk = static_cast<__nv_bfloat16*>(dk);
+  p.dv = static_cast<__nv_bfloat16*>(dv);
+  p.cu = cu_seqlens;
+  p.nseq = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.Sq = Sq;
+  p.Sk = Sk;
+  p.total_q = (int)sh.Tq;
+  p.total_k = (int)sh.Tk;
+  p.causal = causal ? 1 : 0;
+  p.scale_log2 = (float)((double)scale * 1.4426950408889634);
+  p.scale = scale;
+  p.err = di->err_word;
+  p.timeout_ns = (unsigned long long)kn.timeout_ns;
+  int grid = kn.grid_override > 0 ? kn.grid_override : di->sms;
+  cudaError_t e = launch_bwd(p, d, grid, static_cast<cudaStream_t>(stream), kn.bwd_poly8,
+                             static_cast<const __nv_bfloat16*>(o),
+                             static_cast<const __nv_bfloat16*>(dout), lse,
+                             static_cast<__nv_bfloat16*>(dq), sh.packed ? (int)sh.Tq : Sq,
+                             sh.packed ? 0 : (long long)Hq * Sq);
+  if (e == cudaErrorNotSupported) return fail(FA_ERR_UNSUPPORTED, "backward not available");
+  if (e != cudaSuccess) return fail(FA_ERR_CUDA, "backward launch: %s", cudaGetErrorString(e));
+  return FA_OK;
+}
+
+extern "C" const char* fa_status_string(int status) {
+  switch (status) {
+    case FA_OK: return "ok";
+    case FA_ERR_INVALID_ARG: return "invalid argument";
+    case FA_ERR_UNSUPPORTED: return "unsupported";
+    case FA_ERR_ARCH: return "wrong GPU architecture (need sm_103a)";
+    case FA_ERR_CUDA: return "CUDA error";
+    case FA_ERR_WORKSPACE: return "workspace missing or too small";
+    case FA_ERR_TIMEOUT: return "device wait timed out";
+    default: return "unknown status";
+  }
+}
+
+extern "C" const char* fa_last_error(void) { return t_last_error.c_str(); }
+
+extern "C" int fa_get_device_error(int* code, int clear) {
+  if (!code) return fail(FA_ERR_INVALID_ARG, "code is NULL");
+  DevInfo* di = nullptr;
+  int st = device_info(&di);
+  if (st != FA_OK) return st;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = cudaMemcpyFromSymbol(code, g_error_word, sizeof(int));
+  if (e == cudaSuccess && clear) {
+    int zero = 0;
+    e = cudaMemcpyToSymbol(g_error_word, &zero, sizeof(int));
+  }
+  if (e != cudaSuccess) return fail(FA_ERR_CUDA, "error word read: %s", cudaGetErrorString(e));
+  return FA_OK;
+}
+
+extern "C" int fa_debug_set(const char* key, double value) {
+  if (!key) return fail(FA_ERR_INVALID_ARG, "key is NULL");
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!strcmp(key, "tau")) {
+    if (!(value >= 0.0 && value <= 16.0)) return fail(FA_ERR_INVALID_ARG, "tau in [0, 16]");
+    g_knobs.tau_log2 = (float)value;
+  } else if (!strcmp(key, "poly8") || !strcmp(key, "bwd_poly8")) {
+    const int v = (int)value;
+    if (v != 0 && v != 2 && v != 4) return fail(FA_ERR_INVALID_ARG, "poly8 in {0, 2, 4}");
+    (key[0] == 'p' ? g_knobs.poly8 : g_knobs.bwd_poly8) = v;
+  } else if (!strcmp(key, "timeout_ms")) {
+    if (!(value >= 1.0 && value <= 60000.0)) return fail(FA_ERR_INVALID_ARG, "timeout_ms");
+    g_knobs.timeout_ns = (long long)(value * 1e6);
+  } else if (!strcmp(key, "grid")) {
+    if (!(value >= 0.0 && value <= 100000.0)) return fail(FA_ERR_INVALID_ARG, "grid");
+    g_knobs.grid_override = (int)value;
+  } else {
+    return fail(FA_ERR_INVALID_ARG, "unknown key '%s'", key);
+  }
+  return FA_OK;
+}
+
+extern "C" int fa_test_exp2(const float* x, float* y, int n, int mode, void* stream) {
+  if (!x || !y || n < 0 || (mode != 0 && mode != 1))
+    return fail(FA_ERR_INVALID_ARG, "fa_test_exp2 arguments");
+  DevInfo* di = nullptr;
+  int st = device_info(&di);
+  if (st != FA_OK) return st;
+  cudaError_t e = launch_exp2_probe(x, y, n, mode, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : fail(FA_ERR_CUDA, "%s", cudaGetErrorString(e));
+}
+
+extern "C" float fa_exp2_poly_host(float x) { return fa::exp2_poly(x); }
+
+extern "C" int fa_test_mma(const void* A, const void* B, float* C, int mode, int N,
+                           void* stream) {
+  if (!A || !B || !C || mode < 0 || mode > 2 || (N != 64 && N != 128))
+    return fail(FA_ERR_INVALID_ARG, "fa_test_mma arguments");
+  DevInfo* di = nullptr;
+  int st = device_info(&di);
+  if (st != FA_OK) return st;
+  cudaError_t e = launch_mma_probe(static_cast<const __nv_bfloat16*>(A),
+                                   static_cast<const __nv_bfloat16*>(B), C, mode, N,
+                                   static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : fail(FA_ERR_CUDA, "%s", cudaGetErrorString(e));
+}
+
+extern "C" int fa_test_wait_timeout(int* status_dev, double timeout_ms, void* stream) {
+  if (!status_dev || !(timeout_ms > 0 && timeout_ms <= 10000))
+    return fail(FA_ERR_INVALID_ARG, "fa_test_wait_timeout arguments");
+  DevInfo* di = nullptr;
+  int st = device_info(&di);
+  if (st != FA_OK) return st;
+  cudaError_t e = launch_wait_timeout_probe(status_dev, (unsigned long long)(timeout_ms * 1e6),
+                                            static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : fail(FA_ERR_CUDA, "%s", cudaGetErrorString(e));
+}
+
+extern "C" int fa_sched_list(int kind, int B, const int* cu_seqlens_host, int Sq, int Sk,
+                             int heads, int causal, int grid, int cta, int* out, int max_units) {
+  if ((kind != 0 && kind != 1) || B < 0 || Sq < 0 || Sk < 0 || heads <= 0 || grid <= 0 ||
+      cta < 0 || cta >= grid || max_units < 0 || (max_units > 0 && !out))
+    return -1;
+  SchedSpec s{cu_seqlens_host, B, Sq, Sk, heads, causal ? 1 : 0, kind == 0 ? 256 : 128,
+              kind == 0 ? 128 : 64, kind};
+  Walker w;
+  w.init(s);
+  int count = 0;
+  for (int k = 0;; ++k) {
+    Unit u;
+    if (!w.seek(snake_index(k, grid, cta), u)) break;
+    if (count < max_units) {
+      out[4 * count + 0] = u.seq;
+      out[4 * count + 1] = u.m;
+      out[4 * count + 2] = u.head;
+      out[4 * count + 3] = u.cost;
+    }
+    ++count;
+  }
+  return count;
+}

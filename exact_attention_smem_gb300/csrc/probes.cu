@@ -1,0 +1,168 @@
+// Test hooks exported through the C ABI for the GPU tests (not used by the
+// attention path):
+//   * the device exponentials (software polynomial and MUFU ex2) over an array;
+//   * a one-tile tcgen05 MMA probe that checks the shared-memory/instruction
+//     descriptors, the TMEM load/store layout and the TMEM-A operand form
+//     against a plain product computed by the test;
+//   * a bounded-wait probe whose wait can never complete, which must end with
+//     the timeout status instead of hanging.
+#include "exp2_poly.cuh"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace fa {
+using namespace ptx;
+
+__global__ void exp2_probe_kernel(const float* x, float* y, int n, int mode) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) y[i] = mode == 0 ? exp2_poly(x[i]) : ex2_mufu(x[i]);
+}
+
+cudaError_t launch_exp2_probe(const float* x, float* y, int n, int mode, cudaStream_t st) {
+  if (n <= 0) return cudaSuccess;
+  exp2_probe_kernel<<<(n + 255) / 256, 256, 0, st>>>(x, y, n, mode);
+  return cudaGetLastError();
+}
+
+// Byte offset of element (r, c) of a rows x cols bf16 matrix stored as
+// 128-byte-swizzled column chunks of 64 elements (the TMA SWIZZLE_128B image).
+__device__ __forceinline__ uint32_t sw128_offset(int r, int c, int rows) {
+  const int chunk = c >> 6;
+  const int byte = (c & 63) * 2;
+  const int unit = (byte >> 4) ^ (r & 7);
+  return chunk * rows * 128 + r * 128 + unit * 16 + (byte & 15);
+}
+
+// mode 0: C[128][N] = A[128][128] * B[N][128]^T    (A, B K-major in shared memory)
+// mode 1: C[128][N] = A[128][128] * B[128][N]      (A from TMEM, B MN-major)
+// mode 2: C[128][N] = At[128][128]^T * B[128][N]   (A MN-major, B MN-major)
+// A/At/B are row-major bf16 in global memory; C is fp32 row-major.
+__global__ void __launch_bounds__(128, 1)
+    mma_probe_kernel(const __nv_bfloat16* A, const __nv_bfloat16* B, float* C, int mode, int N,
+                     int* err) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (base - raw);
+  const uint32_t a_s = base, b_s = base + 32768;
+  const uint32_t bar = base + 65536;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + 65536 + 64);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 65536 + 72);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tid = threadIdx.x;
+
+  // stage A (128 x 128) and B into swizzled shared memory with plain stores
+  for (int i = tid; i < 128 * 128; i += 128) {
+    const int r = i >> 7, c = i & 127;
+    *reinterpret_cast<__nv_bfloat16*>(smem + sw128_offset(r, c, 128)) = A[i];
+  }
+  const int b_rows = mode == 0 ? N : 128, b_cols = mode == 0 ? 128 : N;
+  for (int i = tid; i < b_rows * b_cols; i += 128) {
+    const int r = i / b_cols, c = i % b_cols;
+    *reinterpret_cast<__nv_bfloat16*>(smem + 32768 + sw128_offset(r, c, b_rows)) = B[i];
+  }
+  if (tid == 0) {
+    mbar_init(bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+  if (mode == 1) {
+    // thread r writes row r of A (bf16 pairs) into TMEM columns [0, 64)
+    const int r = tid;
+    uint32_t pk[32];
+    for (int half = 0; half < 2; ++half) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const int c = half * 64 + 2 * j;
+        const float lo = __bfloat162float(A[r * 128 + c]);
+        const float hi = __bfloat162float(A[r * 128 + c + 1]);
+        pk[j] = pack_bf16x2(lo, hi);
+      }
+      tmem_st32(tmem + lane_off + half * 32, pk);
+    }
+    tmem_st_wait();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t d_tm = tmem + 256;
+  if (tid == 0) {
+    for (int kk = 0; kk < 8; ++kk) {
+      if (mode == 0) {
+        const uint32_t off = (kk >> 2) * (128 * 128) + (kk & 3) * 32;
+        const uint32_t boff = (kk >> 2) * (N * 128) + (kk & 3) * 32;
+        mma_ss(d_tm, sdesc_sw128(a_s + off, 128 * 128, 1024),
+               sdesc_sw128(b_s + boff, N * 128, 1024), idesc_bf16(128, N, false, false),
+               kk > 0);
+      } else if (mode == 1) {
+        mma_ts(d_tm, tmem + kk * 8, sdesc_sw128(b_s + kk * 2048, 128 * 128, 1024),
+               idesc_bf16(128, N, false, true), kk > 0);
+      } else {
+        mma_ss(d_tm, sdesc_sw128(a_s + kk * 2048, 128 * 128, 1024),
+               sdesc_sw128(b_s + kk * 2048, 128 * 128, 1024), idesc_bf16(128, N, true, true),
+               kk > 0);
+      }
+    }
+    tc_commit(bar);
+  }
+  const WaitCtl wc{err, abort_flag, 1000000000ull};
+  const bool ok = mbar_wait(bar, 0, wc, SITE_TEST);
+  tc_fence_after();
+  if (ok) {
+    for (int c = 0; c < N; c += 32) {
+      uint32_t v[32];
+      tmem_ld32(tmem + lane_off + 256 + c, v);
+      for (int i = 0; i < 32; ++i) C[tid * N + c + i] = __uint_as_float(v[i]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+cudaError_t launch_mma_probe(const __nv_bfloat16* A, const __nv_bfloat16* B, float* C, int mode,
+                             int N, cudaStream_t st) {
+  const int smem = 65536 + 128 + 1024 + 65536;  // slack keeps any mis-decoded offset in bounds
+  cudaError_t e = cudaFuncSetAttribute(mma_probe_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  mma_probe_kernel<<<1, 128, smem, st>>>(A, B, C, mode, N, device_error_word());
+  return cudaGetLastError();
+}
+
+// A wait on a barrier that nothing ever arrives on: must return through the
+// timeout path, recording SITE_TEST in the error word and `status[0] = 1`.
+__global__ void wait_timeout_probe_kernel(int* status, int* err, unsigned long long timeout_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const WaitCtl wc{err, &abort_flag, timeout_ns};
+  const bool ok = mbar_wait(smem_u32(&bar), 0, wc, SITE_TEST);
+  if (threadIdx.x == 0) status[0] = ok ? 0 : 1;
+}
+
+cudaError_t launch_wait_timeout_probe(int* status, unsigned long long timeout_ns,
+                                      cudaStream_t st) {
+  wait_timeout_probe_kernel<<<1, 32, 0, st>>>(status, device_error_word(), timeout_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace fa

@@ -1,0 +1,164 @@
+/*
+ * fa.h — C ABI of the GB300 (sm_103a) exact-attention library.
+ *
+ * Operation (all entry points): exact scaled-dot-product attention,
+ *     O = softmax(scale * Q K^T + M) V,    LSE_i = ln sum_j exp(scale * (Q K^T)_ij + M_ij)
+ * where M is 0, or -inf above the bottom-right-aligned diagonal when causal
+ * (key j is visible to query i iff j <= i + (Sk - Sq)). The result is the exact
+ * one: the kernels tile the computation with an online softmax and never write
+ * the score matrix to memory ("FlashAttention-4 Conquers Asymmetric GPU
+ * Hardware Scaling", episode description, lineage paragraph; the method's
+ * kernel design is the one summarised in "FlashAttention-4: Algorithm and Kernel
+ * Pipelining Co-Design for Asymmetric Hardware Scaling", abstract and Summary).
+ * Query heads share key/value heads in groups of Hq / Hkv (grouped-query
+ * attention); query head h uses KV head h / (Hq / Hkv).
+ *
+ * Conventions shared by every entry point
+ *   - All tensor pointers are DEVICE pointers to contiguous memory on the
+ *     current CUDA device; base addresses must be 16-byte aligned.
+ *   - bf16 = IEEE bfloat16 (2 bytes); fp32 = IEEE binary32.
+ *   - Dense layout: q, o, dout, dq are [B][Sq][Hq][d]; k, v, dk, dv are
+ *     [B][Sk][Hkv][d]; lse is fp32 [B][Hq][Sq].
+ *   - Packed variable-length layout (cu_seqlens != NULL): B is the number of
+ *     sequences, cu_seqlens is a DEVICE int32 array of B+1 non-decreasing
+ *     offsets with cu_seqlens[0] = 0, and Sq == Sk == cu_seqlens[B] = T, the
+ *     number of packed rows. q, o, dout, dq are [T][Hq][d]; k, v, dk, dv are
+ *     [T][Hkv][d]; lse is fp32 [Hq][T]. Sequence i owns rows
+ *     [cu_seqlens[i], cu_seqlens[i+1]) of every tensor (self-attention: one
+ *     boundary list for queries and keys).
+ *   - d (head dimension) is 64 or 128; scale must be finite and > 0.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream). FA_OK means "validated and enqueued". The library allocates no
+ *     memory on any call and keeps no per-call state; the caller owns all
+ *     buffers and must keep them alive until the stream work completes.
+ *   - Rows with no visible key (possible only when causal with Sq > Sk) get
+ *     O = 0 and LSE = +inf, which makes their backward contribution zero.
+ *   - Errors are returned as fa_status codes; nothing is thrown across the ABI.
+ *     fa_last_error() returns a thread-local message for the last failure.
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#include <stddef.h>
+
+#if defined(__GNUC__)
+#define FA_API __attribute__((visibility("default")))
+#else
+#define FA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1,  /* bad pointer, size, alignment or layout */
+  FA_ERR_UNSUPPORTED = 2,  /* valid but not supported (e.g. d not in {64,128}) */
+  FA_ERR_ARCH = 3,         /* current device is not compute capability 10.3 */
+  FA_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed; see fa_last_error() */
+  FA_ERR_WORKSPACE = 5,    /* backward workspace missing or too small */
+  FA_ERR_TIMEOUT = 6       /* a kernel's bounded wait expired (see fa_get_device_error) */
+} fa_status;
+
+/*
+ * Forward: O (bf16) and LSE (fp32, natural log of the scaled scores).
+ *   q [.., Hq, d], k/v [.., Hkv, d] bf16 inputs (read only); o bf16 output,
+ *   lse fp32 output (layouts above). Hq % Hkv == 0. Sq, Sk >= 0 (0 = nothing
+ *   to do). The kernel is one persistent launch ordering its work
+ *   longest-first (LPT) for causal and packed batches.
+ */
+FA_API int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+           int Hkv, int Sq, int Sk, int d, int causal, float scale, const int* cu_seqlens,
+           void* stream);
+
+/*
+ * Bytes of device workspace fa_bwd needs: fp32 dQ accumulator [T][Hq][d], the
+ * fp32 row terms D_i = sum_c dO_ic O_ic and LSE*log2(e) ([Hq][T] each), with
+ * T = B*Sq (dense) or total_q (packed, pass the packed row count; 0 = dense).
+ */
+FA_API size_t fa_bwd_workspace_bytes(int B, int Hq, int Sq, int d, int total_q);
+
+/*
+ * Backward: dq, dk, dv (bf16) from q, k, v, o, lse (as written by fa_fwd) and
+ * dout. dk/dv of a KV head are summed over the query heads of its group.
+ * Runs three kernels on `stream`: a preprocess (D, LSE*log2e, zeroed dQ
+ * accumulator), the main kernel (dK, dV and fp32 dQ partial sums added
+ * atomically), and a convert pass dQ = bf16(scale * accumulator). `workspace`
+ * (device, 256-byte aligned, >= fa_bwd_workspace_bytes) is scratch owned by
+ * the caller; its contents on entry do not matter. dQ accumulation order is
+ * not fixed, so dq may differ in the last bits between runs.
+ */
+FA_API int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+           const void* dout, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Sq,
+           int Sk, int d, int causal, float scale, const int* cu_seqlens, void* workspace,
+           size_t workspace_bytes, void* stream);
+
+/* Static text for a status code. */
+FA_API const char* fa_status_string(int status);
+
+/* Thread-local detail of the last failing call on this thread ("" if none). */
+FA_API const char* fa_last_error(void);
+
+/*
+ * Reads (and optionally clears) the current device's error word, which a
+ * kernel sets when one of its bounded waits expires (the kernel then returns
+ * early instead of hanging; its outputs are invalid). Synchronises the device.
+ * *code receives 0 if no wait expired, else the site of the first expiry.
+ * Returns FA_OK, or FA_ERR_CUDA if the read failed.
+ */
+FA_API int fa_get_device_error(int* code, int clear);
+
+/*
+ * Test and tuning knobs (not part of the numerical contract). Keys:
+ *   "tau"        conditional-rescale threshold, base-2 units (default 0)
+ *   "poly8"      forward: eighths of the exponentials computed by the FMA-pipe
+ *                polynomial instead of MUFU ex2 (0, 2 or 4)
+ *   "bwd_poly8"  the same for the backward
+ *   "timeout_ms" bounded-wait deadline in milliseconds (default 2000)
+ *   "grid"       persistent grid size override (0 = one CTA per SM)
+ * Returns FA_OK or FA_ERR_INVALID_ARG. Process-wide; not thread-safe with
+ * concurrent launches.
+ */
+FA_API int fa_debug_set(const char* key, double value);
+
+/* ---- test hooks (exercise single device primitives; not the attention path) ---- */
+
+/* y[i] = 2^x[i] on the device: mode 0 software polynomial, mode 1 MUFU ex2. */
+FA_API int fa_test_exp2(const float* x, float* y, int n, int mode, void* stream);
+
+/* Host twin of the device polynomial exp2 (identical operation sequence). */
+FA_API float fa_exp2_poly_host(float x);
+
+/*
+ * One-tile tcgen05 MMA probe (one CTA), fp32 result C[128][N], N in {64,128}:
+ *   mode 0: C = A[128][128] * B[N][128]^T   mode 1: C = A * B[128][N] (A via TMEM)
+ *   mode 2: C = A^T * B[128][N]   (A is read as [K=128][M=128])
+ * A, B bf16 row-major device buffers.
+ */
+FA_API int fa_test_mma(const void* A, const void* B, float* C, int mode, int N, void* stream);
+
+/*
+ * Runs a kernel whose bounded wait can never complete; *status_dev (device
+ * int) becomes 1 when the wait timed out as designed. Leaves the site code in
+ * the device error word (clear it with fa_get_device_error(&c, 1)).
+ */
+FA_API int fa_test_wait_timeout(int* status_dev, double timeout_ms, void* stream);
+
+/*
+ * Host run of the work scheduler: writes, for CTA `cta` of a persistent grid
+ * of `grid` CTAs, its units in execution order as 4 ints each
+ * (sequence, row block, head, cost) into out (room for max_units units).
+ * kind 0 = forward (units of 256 query rows, cost = KV blocks of 128), kind 1
+ * = backward (units of 128 keys, cost = query blocks of 64). cu_seqlens_host
+ * is a HOST array (or NULL for dense B x Sq/Sk). Returns the number of units
+ * (may exceed max_units; only max_units are written), or -1 on bad arguments.
+ */
+FA_API int fa_sched_list(int kind, int B, const int* cu_seqlens_host, int Sq, int Sk, int heads,
+                  int causal, int grid, int cta, int* out, int max_units);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H */

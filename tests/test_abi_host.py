@@ -1,0 +1,84 @@
+"""Host-side checks of the C-ABI library (no GPU): symbols, validation, knobs."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from exact_attention_smem_gb300 import build as b
+    b.build()
+    from exact_attention_smem_gb300 import _lib
+    return _lib.load()
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "fa.h")).read()
+    return re.findall(r"FA_API[^;]*?\b(fa_\w+)\s*\(", src)
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared()
+    assert len(names) >= 12
+    for n in names:
+        assert hasattr(lib, n), n
+    from exact_attention_smem_gb300 import _lib
+    assert set(_lib.exported_symbols()) == set(names)
+
+
+def test_status_strings(lib):
+    for s in range(7):
+        assert lib.fa_status_string(s)
+    assert lib.fa_status_string(99) == b"unknown status"
+
+
+FAKE = 0x7f0000000000  # never dereferenced: validation rejects before any CUDA call
+
+
+def _fwd(lib, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, B=1, Hq=2, Hkv=2, Sq=16, Sk=16, d=128,
+             causal=0, scale=0.1, cu=None)
+    a.update(kw)
+    return lib.fa_fwd(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["Hq"], a["Hkv"], a["Sq"],
+                      a["Sk"], a["d"], a["causal"], a["scale"], a["cu"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(q=None), 1), (dict(lse=None), 1), (dict(v=FAKE + 8), 1), (dict(d=96), 2),
+    (dict(d=256), 2), (dict(Hq=3, Hkv=2), 1), (dict(Hkv=0), 1), (dict(scale=float("nan")), 1),
+    (dict(scale=-1.0), 1), (dict(scale=float("inf")), 1), (dict(Sq=-1), 1),
+    (dict(cu=FAKE, Sq=16, Sk=8), 1),
+])
+def test_forward_validation(lib, kw, status):
+    assert _fwd(lib, **kw) == status
+    assert lib.fa_last_error()
+
+
+def test_forward_empty_is_noop(lib):
+    assert _fwd(lib, B=0) == 0
+    assert _fwd(lib, Sq=0, Sk=0) == 0
+
+
+def test_backward_validation_and_workspace(lib):
+    need = lib.fa_bwd_workspace_bytes(2, 4, 100, 128, 0)
+    assert need == 2 * 100 * 4 * 128 * 4 + 2 * ((2 * 100 * 4 * 4 + 255) // 256 * 256)
+    assert lib.fa_bwd_workspace_bytes(1, 4, 300, 64, 512) == 512 * 4 * 64 * 4 + 2 * 512 * 4 * 4
+    args = [FAKE] * 9 + [2, 4, 4, 100, 100, 128, 1, 0.1, None]
+    assert lib.fa_bwd(*args, FAKE, need - 1, None) == 5
+    assert lib.fa_bwd(*args, FAKE + 16, need, None) == 5      # workspace must be 256-aligned
+    assert lib.fa_bwd(*args, None, need, None) == 5
+    bad = [FAKE] * 8 + [None] + [2, 4, 4, 100, 100, 128, 1, 0.1, None]
+    assert lib.fa_bwd(*bad, FAKE, need, None) == 1
+
+
+def test_debug_knobs(lib):
+    assert lib.fa_debug_set(b"tau", 2.0) == 0
+    assert lib.fa_debug_set(b"tau", 0.0) == 0
+    assert lib.fa_debug_set(b"tau", -1.0) == 1
+    assert lib.fa_debug_set(b"poly8", 3.0) == 1
+    assert lib.fa_debug_set(b"nope", 1.0) == 1
+    assert lib.fa_debug_set(None, 1.0) == 1

@@ -1,0 +1,69 @@
+"""Device primitives through the C ABI: exp2 variants, a one-tile tcgen05 MMA
+probe for each operand form the kernels use, and the bounded-wait timeout path."""
+import numpy as np
+import pytest
+import torch
+
+import exact_attention_smem_gb300 as fa
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _dev():
+    fa.load()
+    torch.cuda.set_device(0)
+    fa.fa_get_device_error(clear=True)
+    yield
+    assert fa.fa_get_device_error(clear=True) == 0
+
+
+def _exp2_dev(x, mode):
+    xd = torch.tensor(x, dtype=torch.float32, device="cuda")
+    y = torch.empty_like(xd)
+    fa.fa_test_exp2(xd, y, mode)
+    torch.cuda.synchronize()
+    return y.cpu().numpy()
+
+
+def test_poly_exp2_device_matches_host_twin_bitwise():
+    xs = np.concatenate([np.linspace(-130, 8, 100001, dtype=np.float32),
+                         (np.arange(0x8000, 0x10000, dtype=np.uint32) << 16).view(np.float32)])
+    xs = xs[~np.isnan(xs)]
+    dev = _exp2_dev(xs, 0)
+    host = np.array([fa.fa_exp2_poly_host(float(x)) for x in xs], dtype=np.float32)
+    assert np.array_equal(dev.view(np.uint32), host.view(np.uint32))
+    sel = xs >= -125
+    rel = np.abs(dev[sel] / oracle.exp2_exact(xs[sel].astype(np.float64)) - 1)
+    assert rel.max() <= 2.0 ** -13
+
+
+def test_mufu_exp2_accuracy():
+    xs = np.linspace(-125, 8, 200001, dtype=np.float32)
+    dev = _exp2_dev(xs, 1)
+    rel = np.abs(dev / oracle.exp2_exact(xs.astype(np.float64)) - 1)
+    assert rel.max() <= 2.0 ** -20
+
+
+@pytest.mark.parametrize("N", [64, 128])
+@pytest.mark.parametrize("mode", [0, 1, 2])
+def test_mma_probe(mode, N):
+    g = torch.Generator().manual_seed(100 + mode * 7 + N)
+    A = torch.randn(128, 128, generator=g).to(torch.bfloat16)
+    B = torch.randn(*((N, 128) if mode == 0 else (128, N)), generator=g).to(torch.bfloat16)
+    C = torch.full((128, N), float("nan"), device="cuda")
+    fa.fa_test_mma(A.cuda(), B.cuda(), C, mode, N)
+    torch.cuda.synchronize()
+    a, b = A.double().numpy(), B.double().numpy()
+    want = a @ b.T if mode == 0 else (a @ b if mode == 1 else a.T @ b)
+    got = C.cpu().double().numpy()
+    assert np.abs(got - want).max() <= 1e-3 * max(1.0, np.abs(want).max())
+
+
+def test_bounded_wait_times_out_instead_of_hanging():
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    fa.fa_test_wait_timeout(status, 50.0)
+    torch.cuda.synchronize()
+    assert status.item() == 1
+    assert fa.fa_get_device_error(clear=True) == 901

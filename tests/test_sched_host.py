@@ -1,0 +1,97 @@
+"""The LPT work scheduler, run on the host through the C ABI (no GPU).
+
+Costs are recomputed here by brute force from the masking rule (count the inner
+blocks that hold at least one key visible to at least one row of the unit), so
+the test does not share the scheduler's closed forms.
+"""
+import itertools
+
+import pytest
+
+from exact_attention_smem_gb300 import fa_sched_list
+
+
+def _seqs(B, cu, Sq, Sk):
+    if cu is None:
+        return [(Sq, Sk)] * B
+    return [(cu[i + 1] - cu[i],) * 2 for i in range(len(cu) - 1)]
+
+
+def _visible(i, j, ql, kl, causal):
+    return j < kl and i < ql and (not causal or j <= i + kl - ql)
+
+
+def _brute_units(kind, B, cu, Sq, Sk, heads, causal):
+    units = {}
+    for s, (ql, kl) in enumerate(_seqs(B, cu, Sq, Sk)):
+        if kind == 0:
+            for m in range((ql + 255) // 256):
+                rows = range(m * 256, min(ql, m * 256 + 256))
+                # KV blocks walked: from block 0 up to the last block with a visible key
+                last = -1
+                for jb in range((kl + 127) // 128):
+                    if any(_visible(i, j, ql, kl, causal) for i in (rows[-1],)
+                           for j in range(jb * 128, min(kl, jb * 128 + 128))):
+                        last = jb
+                for h in range(heads):
+                    units[(s, m, h)] = last + 1
+        else:
+            for n in range((kl + 127) // 128):
+                keys = range(n * 128, min(kl, n * 128 + 128))
+                first = None
+                for ib in range((ql + 63) // 64):
+                    if any(_visible(i, keys[0], ql, kl, causal) for i in range(ib * 64, min(ql, ib * 64 + 64))):
+                        first = ib
+                        break
+                c = 0 if first is None else (ql + 63) // 64 - first
+                for h in range(heads):
+                    units[(s, n, h)] = c
+    return units
+
+
+CASES = [
+    (0, 2, None, 600, 600, 3, True), (0, 2, None, 600, 600, 3, False), (0, 3, None, 1, 1, 2, True),
+    (0, 1, None, 300, 1000, 2, True), (0, 1, None, 1000, 300, 2, True),
+    (0, 4, [0, 1, 1, 700, 3000], 3000, 3000, 2, True), (0, 3, [0, 129, 385, 1000], 1000, 1000, 4, False),
+    (1, 2, None, 600, 600, 3, True), (1, 2, None, 600, 600, 3, False), (1, 1, None, 300, 1000, 2, True),
+    (1, 1, None, 1000, 300, 2, True), (1, 4, [0, 1, 1, 700, 3000], 3000, 3000, 2, True),
+]
+
+
+@pytest.mark.parametrize("grid", [1, 5, 152])
+@pytest.mark.parametrize("case", CASES)
+def test_every_unit_once_with_its_cost(case, grid):
+    kind, B, cu, Sq, Sk, heads, causal = case
+    want = _brute_units(kind, B, cu, Sq, Sk, heads, causal)
+    got = {}
+    for cta in range(grid):
+        for (s, m, h, c) in fa_sched_list(kind, B, cu, Sq, Sk, heads, causal, grid, cta):
+            assert (s, m, h) not in got
+            got[(s, m, h)] = c
+    assert got == want
+
+
+@pytest.mark.parametrize("case", CASES)
+def test_list_order_is_longest_first(case):
+    """Interleaving the CTAs' lists back into list order gives non-increasing cost."""
+    kind, B, cu, Sq, Sk, heads, causal = case
+    G = 7
+    per = [fa_sched_list(kind, B, cu, Sq, Sk, heads, causal, G, b) for b in range(G)]
+    order = []
+    for k in itertools.count():
+        row = [per[b][k] if k < len(per[b]) else None for b in range(G)]
+        if all(x is None for x in row):
+            break
+        if k % 2:
+            row = row[::-1]
+        order += [x for x in row if x is not None]
+    costs = [u[3] for u in order]
+    assert costs == sorted(costs, reverse=True)
+
+
+def test_causal_balance_near_lpt_bound():
+    """Long causal batch: per-CTA total cost within a few percent of the mean."""
+    G = 152
+    loads = [sum(u[3] for u in fa_sched_list(0, 1, None, 32768, 32768, 32, True, G, b)) for b in range(G)]
+    mean = sum(loads) / G
+    assert max(loads) <= 1.03 * mean
