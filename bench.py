@@ -1,0 +1,325 @@
+"""Benchmark: attention forward + backward BF16 TFLOP/s on one GB300.
+
+One step = one forward (O, LSE) and one backward (dQ, dK, dV) of the
+long-context causal workload (B=1, Hq=Hkv=32, S=32768, d=128) through the
+library's C ABI. Inputs (268 MB per tensor) are larger than the 129 MB L2, so
+no flush is needed between steps. FLOPs: forward 4*B*Hq*Sq*Sk*d, halved for
+causal; backward 2.5x forward.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0). N > 1 (torchrun) runs one independent replica
+per GPU (the path has no exchange step) and reports the whole-job aggregate.
+``--impl reference`` times the fp64 CPU oracle on the host cores on a bounded
+sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd/bwd BF16 TFLOPs/s on 1 GB300; % of dense BF16 tensor peak"
+WORKLOAD = "long_s32768_causal"
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d.get("bf16_tflops"), d.get("bf16_tflops_sustained"), "measured"
+    return 1900.0, 1700.0, "fallback"
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class Clocks:
+    """Samples nvidia-smi SM clocks and throttle reasons during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = max(float(r[2]) for r in rows if r[2].replace(".", "").isdigit())
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def flops(w, lengths=None):
+    from attn_inputs import flops_forward
+    f = flops_forward(w, lengths)
+    return f, 2.5 * f
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import exact_attention_smem_gb300 as fa
+    from attn_inputs import WORKLOADS, make_inputs
+
+    ws, rank, local = _dist()
+    torch.cuda.set_device(local)
+    if ws > 1:
+        dist.init_process_group("nccl")
+    fa.load()
+    w = WORKLOADS[WORKLOAD]
+    x = make_inputs(w, "cuda")
+    B, Hq, Hkv, S, d = w.B, w.Hq, w.Hkv, w.Sq, w.d
+    scale = w.scale
+    o = torch.empty_like(x.q)
+    lse = torch.empty(B, Hq, S, dtype=torch.float32, device="cuda")
+    dq, dk, dv = torch.empty_like(x.q), torch.empty_like(x.k), torch.empty_like(x.v)
+    nbytes = fa.fa_bwd_workspace_bytes(B, Hq, S, d, 0)
+    wsbuf = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    f_fwd, f_bwd = flops(w)
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        if ev is not None:
+            fa.fa_debug_set_events(0, ev[0], ev[1])
+        fa.fa_fwd(x.q, x.k, x.v, o, lse, B, Hq, Hkv, S, S, d, True, scale, None, stream)
+        if ev is not None:
+            fa.fa_debug_set_events(1, ev[2], ev[3])
+        fa.fa_bwd(x.q, x.k, x.v, o, lse, x.do, dq, dk, dv, B, Hq, Hkv, S, S, d, True, scale, None,
+                  wsbuf, nbytes, stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_error() == 0
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with Clocks(local) as clk:
+        t0.record(stream)
+        for i in range(args.steps):
+            step(evs[i])
+        t1.record(stream)
+        torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    assert fa.fa_get_device_error() == 0
+    ms = t0.elapsed_time(t1)
+    fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    bwd_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
+    if ws > 1:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # end-to-end through the public API with host buffers (pinned), copies timed
+    e2e = run_e2e(fa, w, x, args, stream) if rank == 0 else None
+
+    if rank != 0:
+        if ws > 1:
+            dist.destroy_process_group()
+        return
+    peak_b, peak_s, kind = _peaks()
+    per_step = (f_fwd + f_bwd)
+    value = per_step * args.steps * ws / (ms * 1e-3) / 1e12
+    bwd_tf = f_bwd / (bwd_ms * 1e-3) / 1e12
+    fwd_tf = f_fwd / (fwd_ms * 1e-3) / 1e12
+    cpu = cpu_baseline(args) if not args.no_cpu else None
+    out = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16)",
+        "config": {"workload": WORKLOAD, "B": B, "Hq": Hq, "Hkv": Hkv, "S": S, "d": d,
+                   "causal": True, "step": "fwd+bwd", "l2": "inputs (268 MB each) exceed L2",
+                   "parallelism": f"replicas x{ws}"},
+        "fwd_tflops": round(fwd_tf, 1), "bwd_tflops": round(bwd_tf, 1),
+        "fwd_frac_of_peak": round(fwd_tf / peak_s, 4), "bwd_frac_of_peak": round(bwd_tf / peak_s, 4),
+        "frac_of_peak": round(value / ws / peak_s, 4),
+        "roofline": {"bound": "tensor", "kernel": "bwd main (tcgen05)", "achieved": round(bwd_tf, 1),
+                     "peak": peak_s, "unit": "TFLOP/s", "frac": round(bwd_tf / peak_s, 4),
+                     "peak_kind": f"{kind} sustained bf16", "traffic": None,
+                     "fwd": {"achieved": round(fwd_tf, 1), "frac": round(fwd_tf / peak_s, 4)}},
+        "e2e": e2e,
+        "gpu_launches": 5 * args.steps,
+        "clocks": clk.summary(),
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(out))
+    if ws > 1:
+        dist.destroy_process_group()
+
+
+def run_e2e(fa, w, x, args, stream):
+    """Same step with inputs in pinned host memory: H2D copies, fwd, bwd, D2H of results."""
+    import torch
+    hq, hk, hv, hdo = (t.cpu().pin_memory() for t in (x.q, x.k, x.v, x.do))
+    B, Hq, Hkv, S, d = w.B, w.Hq, w.Hkv, w.Sq, w.d
+    dq_, dk_, dv_ = (torch.empty_like(t) for t in (x.q, x.k, x.v))
+    q_, k_, v_, do_ = (torch.empty_like(t) for t in (x.q, x.k, x.v, x.do))
+    o_ = torch.empty_like(x.q)
+    lse_ = torch.empty(B, Hq, S, dtype=torch.float32, device="cuda")
+    ho, hlse = torch.empty_like(hq).pin_memory(), torch.empty(B, Hq, S).pin_memory()
+    hdq, hdk, hdv = (torch.empty_like(t).pin_memory() for t in (hq, hk, hv))
+    nbytes = fa.fa_bwd_workspace_bytes(B, Hq, S, d, 0)
+    wsbuf = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+
+    def step():
+        for dst, src in ((q_, hq), (k_, hk), (v_, hv), (do_, hdo)):
+            dst.copy_(src, non_blocking=True)
+        fa.fa_fwd(q_, k_, v_, o_, lse_, B, Hq, Hkv, S, S, d, True, w.scale, None, stream)
+        fa.fa_bwd(q_, k_, v_, o_, lse_, do_, dq_, dk_, dv_, B, Hq, Hkv, S, S, d, True, w.scale,
+                  None, wsbuf, nbytes, stream)
+        for dst, src in ((ho, o_), (hlse, lse_), (hdq, dq_), (hdk, dk_), (hdv, dv_)):
+            dst.copy_(src, non_blocking=True)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n = max(1, min(args.steps, 5))
+    t0.record(stream)
+    for _ in range(n):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / n
+    f_fwd, f_bwd = flops(w)
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
+    d2h = sum(t.numel() * t.element_size() for t in (ho, hlse, hdq, hdk, hdv))
+    return {"value": round((f_fwd + f_bwd) / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+            "ms_per_step": round(ms, 3), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def _oracle_sample(w, x_cpu):
+    """fp64 oracle forward + backward of query head 0 (one of Hq heads) of the workload."""
+    import oracle
+    q = x_cpu.q[0, :, 0]
+    k = x_cpu.k[0, :, 0]
+    v = x_cpu.v[0, :, 0]
+    do = x_cpu.do[0, :, 0]
+    oracle.attend_head_backward(q, k, v, do, w.scale, w.causal)   # runs the forward inside
+
+
+def cpu_baseline(args, reps=1):
+    """Time the oracle (as it stands) on a bounded sample: one head of the workload."""
+    from attn_inputs import WORKLOADS, make_inputs
+    w = WORKLOADS[WORKLOAD]
+    x = make_inputs(w, "cpu")
+    f_fwd, f_bwd = flops(w)
+    sample_flops = (f_fwd + f_bwd) / w.Hq
+    t = time.perf_counter()
+    for _ in range(reps):
+        _oracle_sample(w, x)
+    dt = (time.perf_counter() - t) / reps
+    try:
+        import numpy as np
+        threads = np.__config__.show  # noqa: F841  (BLAS uses all cores by default)
+    except Exception:
+        pass
+    return {"value": round(sample_flops / dt / 1e12, 6), "unit": "TFLOP/s",
+            "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"query head 0 of {WORKLOAD} (1/{w.Hq} of the step's FLOPs), fp64 numpy "
+                      f"fwd+bwd, {dt:.1f} s"}
+
+
+def run_reference(args):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return
+    from attn_inputs import WORKLOADS, make_inputs
+    w = WORKLOADS[WORKLOAD]
+    x = make_inputs(w, "cpu")
+    f_fwd, f_bwd = flops(w)
+    sample_flops = (f_fwd + f_bwd) / w.Hq
+    for _ in range(args.warmup and 1):
+        pass
+    times = []
+    for _ in range(args.steps):
+        t = time.perf_counter()
+        _oracle_sample(w, x)
+        times.append(time.perf_counter() - t)
+    dt = statistics.mean(times)
+    value = sample_flops / dt / 1e12
+    out = {"metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": ws,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 1),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic (seeded N(0,1) bf16, upcast to fp64)", "impl": "reference",
+           "config": {"workload": WORKLOAD, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "S": w.Sq,
+                      "d": w.d, "causal": True, "step": "fwd+bwd (one head per step)"},
+           "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": os.cpu_count(),
+                            "kind": "oracle",
+                            "sample": f"query head 0 of {WORKLOAD} per step (1/{w.Hq} of the "
+                                      "workload's FLOPs), fp64 numpy fwd+bwd"},
+           "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline leg")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -37,6 +37,7 @@ _SIGS = {
     "fa_last_error": (ctypes.c_char_p, []),
     "fa_get_device_error": (_I, [ctypes.POINTER(_I), _I]),
     "fa_debug_set": (_I, [ctypes.c_char_p, ctypes.c_double]),
+    "fa_debug_set_events": (_I, [_I, _P, _P]),
     "fa_test_exp2": (_I, [_P, _P, _I, _I, _P]),
     "fa_exp2_poly_host": (_F, [_F]),
     "fa_test_mma": (_I, [_P, _P, _P, _I, _I, _P]),
@@ -117,6 +118,18 @@ def fa_get_device_error(clear=True):
 
 def fa_debug_set(key, value):
     _check(load().fa_debug_set(key.encode(), float(value)), "fa_debug_set")
+
+
+def fa_debug_set_events(which, start=None, stop=None):
+    """Arm one-shot timing events (torch.cuda.Event) around the next fwd/bwd main kernel."""
+    def h(ev):
+        if ev is None:
+            return None
+        if not ev.cuda_event:
+            ev.record()          # torch creates the CUDA event lazily
+            ev.synchronize()
+        return ctypes.c_void_p(ev.cuda_event)
+    _check(load().fa_debug_set_events(which, h(start), h(stop)), "fa_debug_set_events")
 
 
 def fa_test_exp2(x, y, mode, stream=None):

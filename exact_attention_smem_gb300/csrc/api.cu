@@ -90,11 +90,12 @@ int device_info(DevInfo** out) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// [rows, heads, d] bf16 view, boxes of 64 columns x 1 head x 128 rows, 128B swizzle.
-int encode_rows(CUtensorMap* tm, const void* ptr, long long rows, int heads, int d) {
+// [rows, heads, d] bf16 view, boxes of 64 columns x 1 head x box_rows rows, 128B swizzle.
+int encode_rows(CUtensorMap* tm, const void* ptr, long long rows, int heads, int d,
+                int box_rows = 128) {
   cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)rows};
   cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)heads * d * 2};
-  cuuint32_t box[3] = {64, 1, 128};
+  cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = g_encode(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims,
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -143,6 +144,13 @@ int validate_common(const void* const* ptrs, int nptrs, int B, int Hq, int Hkv, 
 Knobs knobs_snapshot() {
   std::lock_guard<std::mutex> lk(g_mu);
   return g_knobs;
+}
+
+void take_events(int which, cudaEvent_t* start, cudaEvent_t* stop) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  *start = g_knobs.ev[which][0];
+  *stop = g_knobs.ev[which][1];
+  g_knobs.ev[which][0] = g_knobs.ev[which][1] = nullptr;
 }
 
 int num_sms() {
@@ -209,7 +217,11 @@ extern "C" int fa_fwd(const void* q, const void* k, const void* v, void* o, floa
   int grid = kn.grid_override > 0 ? kn.grid_override : di->sms;
   if (units < grid) grid = (int)units;
   if (grid < 1) grid = 1;
+  cudaEvent_t ev0, ev1;
+  take_events(0, &ev0, &ev1);
+  if (ev0) cudaEventRecord(ev0, static_cast<cudaStream_t>(stream));
   cudaError_t e = launch_fwd(p, d, grid, static_cast<cudaStream_t>(stream), kn.poly8);
+  if (ev1) cudaEventRecord(ev1, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(FA_ERR_CUDA, "forward launch: %s", cudaGetErrorString(e));
   return FA_OK;
 }
@@ -218,7 +230,8 @@ extern "C" size_t fa_bwd_workspace_bytes(int B, int Hq, int Sq, int d, int total
   if (B < 0 || Hq <= 0 || Sq < 0 || d <= 0 || total_q < 0) return 0;
   const size_t T = total_q > 0 ? (size_t)total_q : (size_t)B * (size_t)Sq;
   auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
-  return up(T * Hq * d * sizeof(float)) + 2 * up(T * Hq * sizeof(float));
+  const size_t P = (size_t)pad_hstride((long long)T, B);
+  return up(T * Hq * d * sizeof(float)) + 2 * up(P * Hq * sizeof(float));
 }
 
 extern "C" int fa_bwd(const void* q, const void* k, const void* v, const void* o,
@@ -242,17 +255,26 @@ extern "C" int fa_bwd(const void* q, const void* k, const void* v, const void* o
   BwdParams p;
   memset(&p, 0, sizeof(p));
   const long long Tq = sh.Tq > 0 ? sh.Tq : 1, Tk = sh.Tk > 0 ? sh.Tk : 1;
-  if ((st = encode_rows(&p.tm_q, q, Tq, Hq, d)) != FA_OK) return st;
-  if ((st = encode_rows(&p.tm_do, dout, Tq, Hq, d)) != FA_OK) return st;
-  if ((st = encode_rows(&p.tm_k, k, Tk, Hkv, d)) != FA_OK) return st;
-  if ((st = encode_rows(&p.tm_v, v, Tk, Hkv, d)) != FA_OK) return st;
+  if ((st = encode_rows(&p.tm_q, sh.Tq > 0 ? q : k, sh.Tq > 0 ? Tq : Tk, sh.Tq > 0 ? Hq : Hkv,
+                        d, 64)) != FA_OK)
+    return st;
+  if ((st = encode_rows(&p.tm_do, sh.Tq > 0 ? dout : k, sh.Tq > 0 ? Tq : Tk,
+                        sh.Tq > 0 ? Hq : Hkv, d, 64)) != FA_OK)
+    return st;
+  if ((st = encode_rows(&p.tm_k, sh.Tk > 0 ? k : q, sh.Tk > 0 ? Tk : Tq, sh.Tk > 0 ? Hkv : Hq,
+                        d)) != FA_OK)
+    return st;
+  if ((st = encode_rows(&p.tm_v, sh.Tk > 0 ? v : q, sh.Tk > 0 ? Tk : Tq, sh.Tk > 0 ? Hkv : Hq,
+                        d)) != FA_OK)
+    return st;
   auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
   char* ws = static_cast<char*>(workspace);
   const size_t T = (size_t)sh.Tq;
+  const size_t P = (size_t)pad_hstride((long long)T, B);
   p.dq_acc = reinterpret_cast<float*>(ws);
-  p.lse_log2 = reinterpret_cast<float*>(ws + up(T * Hq * d * sizeof(float)));
-  p.delta = reinterpret_cast<float*>(ws + up(T * Hq * d * sizeof(float)) +
-                                     up(T * Hq * sizeof(float)));
+  p.lse2 = reinterpret_cast<float*>(ws + up(T * Hq * d * sizeof(float)));
+  p.delta = reinterpret_cast<float*>(ws + up(T * Hq * d * sizeof(float)) + up(P * Hq * sizeof(float)));
+  p.pad_hstride = (long long)P;
   p.dk = static_cast<__nv_bfloat16*>(dk);
   p.dv = static_cast<__nv_bfloat16*>(dv);
   p.cu = cu_seqlens;
@@ -268,13 +290,17 @@ extern "C" int fa_bwd(const void* q, const void* k, const void* v, const void* o
   p.scale = scale;
   p.err = di->err_word;
   p.timeout_ns = (unsigned long long)kn.timeout_ns;
+  BwdAux aux;
+  aux.o = static_cast<const __nv_bfloat16*>(o);
+  aux.dout = static_cast<const __nv_bfloat16*>(dout);
+  aux.lse = lse;
+  aux.lse_hstride = sh.packed ? (int)sh.Tq : Sq;
+  aux.lse_seqstride = sh.packed ? 0 : (long long)Hq * Sq;
+  aux.dq = static_cast<__nv_bfloat16*>(dq);
   int grid = kn.grid_override > 0 ? kn.grid_override : di->sms;
-  cudaError_t e = launch_bwd(p, d, grid, static_cast<cudaStream_t>(stream), kn.bwd_poly8,
-                             static_cast<const __nv_bfloat16*>(o),
-                             static_cast<const __nv_bfloat16*>(dout), lse,
-                             static_cast<__nv_bfloat16*>(dq), sh.packed ? (int)sh.Tq : Sq,
-                             sh.packed ? 0 : (long long)Hq * Sq);
-  if (e == cudaErrorNotSupported) return fail(FA_ERR_UNSUPPORTED, "backward not available");
+  cudaError_t e = launch_bwd(p, aux, d, grid, static_cast<cudaStream_t>(stream), kn.bwd_poly8);
+  if (e == cudaErrorNotSupported)
+    return fail(FA_ERR_UNSUPPORTED, "backward supports head dim 128 only");
   if (e != cudaSuccess) return fail(FA_ERR_CUDA, "backward launch: %s", cudaGetErrorString(e));
   return FA_OK;
 }
@@ -328,6 +354,14 @@ extern "C" int fa_debug_set(const char* key, double value) {
   } else {
     return fail(FA_ERR_INVALID_ARG, "unknown key '%s'", key);
   }
+  return FA_OK;
+}
+
+extern "C" int fa_debug_set_events(int which, void* start, void* stop) {
+  if (which != 0 && which != 1) return fail(FA_ERR_INVALID_ARG, "which must be 0 or 1");
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_knobs.ev[which][0] = static_cast<cudaEvent_t>(start);
+  g_knobs.ev[which][1] = static_cast<cudaEvent_t>(stop);
   return FA_OK;
 }
 

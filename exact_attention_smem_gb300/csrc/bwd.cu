@@ -1,9 +1,656 @@
-// Backward kernels (placeholder until the backward lands).
+// Backward attention for sm_103a: dQ, dK, dV from Q, K, V, O, dO and LSE.
+//
+// Three kernels on one stream:
+//   1. preprocess: D_i = sum_c dO_ic O_ic and LSE_i * log2(e) into padded row
+//      arrays (each sequence starts on a 64-row boundary so one 64-row block is
+//      one aligned 256-byte bulk copy), padding rows get LSE = +inf and D = 0,
+//      and the fp32 dQ accumulator is zeroed;
+//   2. main: one persistent CTA per SM walks (sequence, 128-key block, KV head)
+//      units longest-first. For each query head of the KV group and each block
+//      of 64 query rows that sees the keys it computes, with tcgen05 MMAs
+//      accumulating in TMEM:
+//         S^T  = K Q^T            P^T  = exp2(S^T * scale*log2e - LSE*log2e)
+//         dP^T = V dO^T           dS^T = P^T o (dP^T - D)
+//         dV  += P^T dO           dK  += dS^T Q        dQ^T = K^T dS^T
+//      and adds dQ^T into the fp32 accumulator with atomic adds. dK and dV stay
+//      in TMEM for the whole unit (summed over the GQA group) and are written
+//      once, dK scaled by the softmax scale;
+//   3. convert: dQ = bf16(scale * accumulator).
+// The pages' backward keeps accumulators and the P/dS operands in tensor
+// memory to cut shared-memory traffic ("FlashAttention-4: Algorithm and Kernel
+// Pipelining Co-Design for Asymmetric Hardware Scaling", abstract item (3) and
+// the Summary); here P^T and dS^T live in TMEM as the A operands of the dV/dK
+// MMAs, and dS^T is also staged once in shared memory as the B operand of dQ^T.
+//
+// Warps: 0-3 P/dS (one thread per key row = TMEM lane), 4-7 dQ drain (one
+// thread per head-dim row of dQ^T), 8 MMA issue + TMEM allocation, 9 TMA.
+// TMEM columns: dV [0,d) dK [d,2d) S^T/P^T [2d,2d+64) dP^T/dS^T [2d+64,2d+128)
+// dQ^T [2d+128,2d+192).
+#include "exp2_poly.cuh"
 #include "internal.h"
+#include "ptx.cuh"
+#include "sched.cuh"
+
+#include <cmath>
 
 namespace fa {
-cudaError_t launch_bwd(const BwdParams&, int, int, cudaStream_t, int, const __nv_bfloat16*,
-                       const __nv_bfloat16*, const float*, __nv_bfloat16*, int, long long) {
-  return cudaErrorNotSupported;
+using namespace ptx;
+
+namespace bwdk {
+
+constexpr int BN = 128;   // keys per unit
+constexpr int BMQ = 64;   // query rows per step
+constexpr int NUM_THREADS = 320;
+constexpr int MMA_WARP = 8;
+constexpr int TMA_WARP = 9;
+constexpr int NSTAGE = 3;
+constexpr int MAX_SEQ_SMEM = 1024;
+
+template <int D>
+struct Cfg {
+  static constexpr int CHUNKS = D / 64;
+  static constexpr int KV_CHUNK = 128 * 128;
+  static constexpr int KV_TILE = CHUNKS * KV_CHUNK;
+  static constexpr int Q_CHUNK = 64 * 128;
+  static constexpr int Q_TILE = CHUNKS * Q_CHUNK;
+  static constexpr int ST_LSE = 2 * Q_TILE;            // offsets inside a stage
+  static constexpr int ST_D = ST_LSE + 256;
+  static constexpr int STAGE_TX = 2 * Q_TILE + 512;
+  static constexpr int STAGE_BYTES = (STAGE_TX + 1023) & ~1023;
+  static constexpr int DS_BYTES = 128 * 128;            // dS^T [128 keys][64 q] bf16
+  static constexpr int K_OFF = 0;
+  static constexpr int V_OFF = KV_TILE;
+  static constexpr int ST_OFF = 2 * KV_TILE;
+  static constexpr int DS_OFF = ST_OFF + NSTAGE * STAGE_BYTES;
+  static constexpr int BAR_OFF = DS_OFF + 2 * DS_BYTES;
+  static constexpr int B_KVFULL = 0, B_KVEMPTY = 1, B_QDFULL = 2, B_QDEMPTY = 2 + NSTAGE,
+                       B_SFULL = 2 + 2 * NSTAGE, B_DPFULL = B_SFULL + 1, B_PREADY = B_SFULL + 2,
+                       B_DSREADY = B_SFULL + 3, B_DQFULL = B_SFULL + 4, B_DQEMPTY = B_SFULL + 5,
+                       B_DSBEMPTY = B_SFULL + 6, B_ACCFULL = B_DSBEMPTY + 2,
+                       B_ACCEMPTY = B_ACCFULL + 1, B_DRAIN = B_ACCFULL + 2, NBAR = B_DRAIN + 1;
+  static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
+  static constexpr int CU_OFF = MISC_OFF + 16;
+  static constexpr int SMEM_BYTES = CU_OFF + (MAX_SEQ_SMEM + 1) * 4 + 1024;
+  static constexpr uint32_t TM_DV = 0, TM_DK = D, TM_S = 2 * D, TM_DP = 2 * D + 64,
+                            TM_DQ = 2 * D + 128;
+  static constexpr uint32_t IDESC_SDP = idesc_bf16(128, 64, false, false);  // S^T, dP^T
+  static constexpr uint32_t IDESC_ACC = idesc_bf16(128, D, false, true);    // dV, dK (A in TMEM)
+  static constexpr uint32_t IDESC_DQ = idesc_bf16(D, 64, true, true);       // dQ^T
+};
+
+__device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
+
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > limit_ns) return;
+  }
 }
+
+// X^T (TMEM, 128 keys x 64 q) = Kt (128 x D, K-major) * Qb (64 x D, K-major)^T
+template <int D>
+__device__ __forceinline__ void issue_kq(uint32_t tm, uint32_t kt, uint32_t qb) {
+  using C = Cfg<D>;
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    mma_ss(tm, sdesc_sw128(kt + (kk >> 2) * C::KV_CHUNK + (kk & 3) * 32, C::KV_CHUNK, 1024),
+           sdesc_sw128(qb + (kk >> 2) * C::Q_CHUNK + (kk & 3) * 32, C::Q_CHUNK, 1024),
+           C::IDESC_SDP, kk > 0 ? 1u : 0u);
+  }
+}
+
+// Acc (TMEM, 128 keys x D) (+)= A^T (TMEM, 128 keys x 64 q, bf16) * Xb (64 q x D, MN-major)
+template <int D>
+__device__ __forceinline__ void issue_acc(uint32_t tm_acc, uint32_t tm_a, uint32_t xb, bool acc) {
+  using C = Cfg<D>;
+#pragma unroll
+  for (int kk = 0; kk < BMQ / 16; ++kk) {
+    mma_ts(tm_acc, tm_a + kk * 8, sdesc_sw128(xb + kk * 2048, C::Q_CHUNK, 1024), C::IDESC_ACC,
+           (acc || kk > 0) ? 1u : 0u);
+  }
+}
+
+// dQ^T (TMEM, D x 64 q) = Kt^T (D x 128 keys, MN-major A) * dS^T (128 keys x 64 q, MN-major B)
+template <int D>
+__device__ __forceinline__ void issue_dq(uint32_t tm, uint32_t kt, uint32_t dsb) {
+  using C = Cfg<D>;
+#pragma unroll
+  for (int kk = 0; kk < BN / 16; ++kk) {
+    mma_ss(tm, sdesc_sw128(kt + kk * 2048, C::KV_CHUNK, 1024),
+           sdesc_sw128(dsb + kk * 2048, C::DS_BYTES, 1024), C::IDESC_DQ, kk > 0 ? 1u : 0u);
+  }
+}
+
+struct StepInfo {
+  int h, m;
+};
+
+__device__ __forceinline__ StepInfo step_of(int i, int cost, int m_first, int g, int group) {
+  StepInfo s;
+  const int hh = i / cost;
+  s.h = g * group + hh;
+  s.m = m_first + (i - hh * cost);
+  return s;
+}
+
+__device__ __forceinline__ int first_qblock(const Unit& u, int causal) {
+  if (!causal) return 0;
+  int r0 = u.m * BN - (u.k_len - u.q_len);
+  r0 = r0 > 0 ? r0 : 0;
+  return r0 / BMQ;
+}
+
+template <int D, int POLY8>
+__global__ void __launch_bounds__(NUM_THREADS, 1) bwd_kernel(const __grid_constant__ BwdParams p) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (base - raw);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t bars = base + C::BAR_OFF;
+#define BAR(i) (bars + 8u * (uint32_t)(i))
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::MISC_OFF);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
+  int* cu_s = reinterpret_cast<int*>(smem + C::CU_OFF);
+
+  if (threadIdx.x == 0) {
+    mbar_init(BAR(C::B_KVFULL), 1);
+    mbar_init(BAR(C::B_KVEMPTY), 1);
+    for (int s = 0; s < NSTAGE; ++s) {
+      mbar_init(BAR(C::B_QDFULL + s), 1);
+      mbar_init(BAR(C::B_QDEMPTY + s), 1);
+    }
+    mbar_init(BAR(C::B_SFULL), 1);
+    mbar_init(BAR(C::B_DPFULL), 1);
+    mbar_init(BAR(C::B_PREADY), 128);
+    mbar_init(BAR(C::B_DSREADY), 128);
+    mbar_init(BAR(C::B_DQFULL), 1);
+    mbar_init(BAR(C::B_DQEMPTY), 128);
+    mbar_init(BAR(C::B_DSBEMPTY + 0), 1);
+    mbar_init(BAR(C::B_DSBEMPTY + 1), 1);
+    mbar_init(BAR(C::B_ACCFULL), 1);
+    mbar_init(BAR(C::B_ACCEMPTY), 128);
+    mbar_init(BAR(C::B_DRAIN), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == TMA_WARP && lane == 0) {
+    tma_prefetch_desc(&p.tm_q);
+    tma_prefetch_desc(&p.tm_do);
+    tma_prefetch_desc(&p.tm_k);
+    tma_prefetch_desc(&p.tm_v);
+  }
+  if (warp == MMA_WARP) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  const bool cu_in_smem = p.cu != nullptr && p.nseq <= MAX_SEQ_SMEM;
+  if (cu_in_smem)
+    for (int i = threadIdx.x; i <= p.nseq; i += NUM_THREADS) cu_s[i] = p.cu[i];
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  const SchedSpec spec{cu_in_smem ? cu_s : p.cu, p.nseq, p.Sq, p.Sk, p.Hkv, p.causal, BN, BMQ, 1};
+  const WaitCtl wc{p.err, abort_flag, p.timeout_ns};
+  const int G = gridDim.x;
+  const int cta = blockIdx.x;
+  const int group = p.Hq / p.Hkv;
+
+  if (warp == TMA_WARP) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      Walker w;
+      w.init(spec);
+      uint32_t it = 0;
+      int u_it = 0;
+      bool ok = true;
+      for (int k = 0; ok; ++k) {
+        Unit u;
+        if (!w.seek(snake_index(k, G, cta), u)) break;
+        if (u.cost == 0) continue;
+        const int g = u.head;
+        const int n = u.cost * group;
+        const int m_first = first_qblock(u, p.causal);
+        const long long pbase = pad_start(u.seq, u.q_start);
+        if (u_it > 0) {
+          ok = mbar_wait(BAR(C::B_KVEMPTY), (u_it - 1) & 1, wc, SITE_BWD_KV_EMPTY);
+          if (!ok) break;
+        }
+        mbar_arrive_expect_tx(BAR(C::B_KVFULL), 2 * C::KV_TILE);
+        for (int c = 0; c < C::CHUNKS; ++c) {
+          tma_load_3d(base + C::K_OFF + c * C::KV_CHUNK, &p.tm_k, BAR(C::B_KVFULL), c * 64, g,
+                      u.k_start + u.m * BN);
+          tma_load_3d(base + C::V_OFF + c * C::KV_CHUNK, &p.tm_v, BAR(C::B_KVFULL), c * 64, g,
+                      u.k_start + u.m * BN);
+        }
+        ++u_it;
+        for (int i = 0; i < n; ++i) {
+          const StepInfo st = step_of(i, u.cost, m_first, g, group);
+          const int s = it % NSTAGE;
+          if (it >= (uint32_t)NSTAGE) {
+            ok = mbar_wait(BAR(C::B_QDEMPTY + s), ((it / NSTAGE) - 1) & 1, wc, SITE_BWD_QD_EMPTY);
+            if (!ok) break;
+          }
+          const uint32_t sb = base + C::ST_OFF + s * C::STAGE_BYTES;
+          const uint32_t full = BAR(C::B_QDFULL + s);
+          mbar_arrive_expect_tx(full, C::STAGE_TX);
+          const int row = u.q_start + st.m * BMQ;
+          for (int c = 0; c < C::CHUNKS; ++c) {
+            tma_load_3d(sb + c * C::Q_CHUNK, &p.tm_q, full, c * 64, st.h, row);
+            tma_load_3d(sb + C::Q_TILE + c * C::Q_CHUNK, &p.tm_do, full, c * 64, st.h, row);
+          }
+          const long long off = (long long)st.h * p.pad_hstride + pbase + (long long)st.m * BMQ;
+          bulk_load(sb + C::ST_LSE, p.lse2 + off, 256, full);
+          bulk_load(sb + C::ST_D, p.delta + off, 256, full);
+          ++it;
+        }
+      }
+      if (!ok) {
+        for (uint32_t i = it > (uint32_t)NSTAGE ? it - NSTAGE : 0; i < it; ++i)
+          drain_wait(BAR(C::B_QDFULL + i % NSTAGE), (i / NSTAGE) & 1, 100000000ull);
+        if (u_it > 0) drain_wait(BAR(C::B_KVFULL), (u_it - 1) & 1, 100000000ull);
+      }
+    }
+  } else if (warp == MMA_WARP) {
+    // ------------------------------------------------------------ MMA issue
+    if (lane == 0) {
+      Walker w;
+      w.init(spec);
+      uint32_t it = 0;
+      int u_it = 0;
+      bool ok = true;
+      const uint32_t kt = base + C::K_OFF, vt = base + C::V_OFF;
+      for (int k = 0; ok; ++k) {
+        Unit u;
+        if (!w.seek(snake_index(k, G, cta), u)) break;
+        if (u.cost == 0) continue;
+        const int n = u.cost * group;
+        ok = mbar_wait(BAR(C::B_KVFULL), u_it & 1, wc, SITE_BWD_KV_FULL);
+        if (!ok) break;
+        tc_fence_after();
+        // prologue: S^T(0), dP^T(0)
+        {
+          const int s = it % NSTAGE;
+          ok = mbar_wait(BAR(C::B_QDFULL + s), (it / NSTAGE) & 1, wc, SITE_BWD_QD_FULL);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t sb = base + C::ST_OFF + s * C::STAGE_BYTES;
+          issue_kq<D>(tmem + C::TM_S, kt, sb);
+          tc_commit(BAR(C::B_SFULL));
+          issue_kq<D>(tmem + C::TM_DP, vt, sb + C::Q_TILE);
+          tc_commit(BAR(C::B_DPFULL));
+        }
+        for (int i = 0; i < n; ++i, ++it) {
+          const int s = it % NSTAGE;
+          const uint32_t sb = base + C::ST_OFF + s * C::STAGE_BYTES;
+          ok = mbar_wait(BAR(C::B_PREADY), it & 1, wc, SITE_BWD_P_READY);
+          if (!ok) break;
+          if (i == 0 && u_it > 0) {
+            ok = mbar_wait(BAR(C::B_ACCEMPTY), (u_it - 1) & 1, wc, SITE_BWD_ACC_FULL);
+            if (!ok) break;
+          }
+          tc_fence_after();
+          issue_acc<D>(tmem + C::TM_DV, tmem + C::TM_S, sb + C::Q_TILE, i > 0);   // dV += P^T dO
+          uint32_t sb2 = 0;
+          if (i + 1 < n) {
+            const int s2 = (it + 1) % NSTAGE;
+            ok = mbar_wait(BAR(C::B_QDFULL + s2), ((it + 1) / NSTAGE) & 1, wc, SITE_BWD_QD_FULL);
+            if (!ok) break;
+            tc_fence_after();
+            sb2 = base + C::ST_OFF + s2 * C::STAGE_BYTES;
+            issue_kq<D>(tmem + C::TM_S, kt, sb2);                                  // S^T(i+1)
+            tc_commit(BAR(C::B_SFULL));
+          }
+          ok = mbar_wait(BAR(C::B_DSREADY), it & 1, wc, SITE_BWD_DS_READY);
+          if (!ok) break;
+          tc_fence_after();
+          issue_acc<D>(tmem + C::TM_DK, tmem + C::TM_DP, sb, i > 0);              // dK += dS^T Q
+          if (it > 0) {
+            ok = mbar_wait(BAR(C::B_DQEMPTY), (it - 1) & 1, wc, SITE_BWD_DQ_EMPTY);
+            if (!ok) break;
+            tc_fence_after();
+          }
+          issue_dq<D>(tmem + C::TM_DQ, kt, base + C::DS_OFF + (it & 1) * C::DS_BYTES);
+          tc_commit(BAR(C::B_DQFULL));
+          tc_commit(BAR(C::B_DSBEMPTY + (it & 1)));
+          tc_commit(BAR(C::B_QDEMPTY + s));
+          if (i + 1 < n) {
+            issue_kq<D>(tmem + C::TM_DP, vt, sb2 + C::Q_TILE);                     // dP^T(i+1)
+            tc_commit(BAR(C::B_DPFULL));
+          } else {
+            tc_commit(BAR(C::B_ACCFULL));
+            tc_commit(BAR(C::B_KVEMPTY));
+          }
+        }
+        ++u_it;
+      }
+      if (!ok) {
+        tc_commit(BAR(C::B_DRAIN));
+        drain_wait(BAR(C::B_DRAIN), 0, 100000000ull);
+      }
+    }
+  } else if (warp < 4) {
+    // ------------------------------------------------------------ P^T / dS^T
+    const int j = warp * 32 + lane;                       // key row within the block
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const float sl2 = p.scale_log2;
+    Walker w;
+    w.init(spec);
+    uint32_t it = 0;
+    int u_it = 0;
+    bool ok = true;
+    uint8_t* dsb_base = smem + C::DS_OFF;
+    for (int k = 0; ok; ++k) {
+      Unit u;
+      if (!w.seek(snake_index(k, G, cta), u)) break;
+      const int g = u.head;
+      const int key = u.m * BN + j;                       // key index within the sequence
+      const bool key_ok = key < u.k_len;
+      __nv_bfloat16* dk_row = p.dk + (((long long)u.k_start + key) * p.Hkv + g) * D;
+      __nv_bfloat16* dv_row = p.dv + (((long long)u.k_start + key) * p.Hkv + g) * D;
+      if (u.cost == 0) {                                   // keys no query sees
+        if (key_ok) {
+          for (int c = 0; c < D; c += 8) {
+            *reinterpret_cast<uint4*>(dk_row + c) = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(dv_row + c) = make_uint4(0, 0, 0, 0);
+          }
+        }
+        continue;
+      }
+      const int n = u.cost * group;
+      const int m_first = first_qblock(u, p.causal);
+      // query q (within the sequence) sees this key iff q >= qmin
+      const int qmin = p.causal ? key - (u.k_len - u.q_len) : -(1 << 30);
+      for (int i = 0; i < n; ++i, ++it) {
+        const StepInfo st = step_of(i, u.cost, m_first, g, group);
+        const int s = it % NSTAGE;
+        const uint8_t* stage = smem + C::ST_OFF + s * C::STAGE_BYTES;
+        const float* lse_s = reinterpret_cast<const float*>(stage + C::ST_LSE);
+        const float* d_s = reinterpret_cast<const float*>(stage + C::ST_D);
+        ok = mbar_wait(BAR(C::B_QDFULL + s), (it / NSTAGE) & 1, wc, SITE_BWD_QD_FULL);
+        if (!ok) break;
+        ok = mbar_wait(BAR(C::B_SFULL), it & 1, wc, SITE_BWD_S_FULL);
+        if (!ok) break;
+        tc_fence_after();
+        float pv[BMQ];
+        {
+          uint32_t a[64];
+          tmem_ld64(tmem + lane_off + C::TM_S, a);
+          // columns c with q0 + c < qmin are masked; a key past the sequence masks all
+          const int cmin = key_ok ? qmin - st.m * BMQ : BMQ;
+#pragma unroll
+          for (int c = 0; c < BMQ; c += 4) {
+            const float4 l4 = *reinterpret_cast<const float4*>(lse_s + c);
+            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float x = __fmaf_rn(u2f(a[c + e]), sl2, -lv[e]);
+              const float pe = ((c + e) & 7) < POLY8 ? exp2_poly(x) : ex2_mufu(x);
+              pv[c + e] = (c + e) < cmin ? 0.f : pe;
+            }
+          }
+        }
+        {
+          uint32_t pk[32];
+#pragma unroll
+          for (int c = 0; c < 32; ++c) pk[c] = pack_bf16x2(pv[2 * c], pv[2 * c + 1]);
+          tmem_st32(tmem + lane_off + C::TM_S, pk);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(BAR(C::B_PREADY));
+        ok = mbar_wait(BAR(C::B_DPFULL), it & 1, wc, SITE_BWD_DP_FULL);
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t pk[32];
+        {
+          uint32_t a[64];
+          tmem_ld64(tmem + lane_off + C::TM_DP, a);
+#pragma unroll
+          for (int c = 0; c < BMQ; c += 8) {
+            const float4 d0 = *reinterpret_cast<const float4*>(d_s + c);
+            const float4 d1 = *reinterpret_cast<const float4*>(d_s + c + 4);
+            const float dv8[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+#pragma unroll
+            for (int e = 0; e < 8; e += 2) {
+              const float ds0 = pv[c + e] * (u2f(a[c + e]) - dv8[e]);
+              const float ds1 = pv[c + e + 1] * (u2f(a[c + e + 1]) - dv8[e + 1]);
+              pk[(c + e) / 2] = pack_bf16x2(ds0, ds1);
+            }
+          }
+        }
+        if (it >= 2) {
+          ok = mbar_wait(BAR(C::B_DSBEMPTY + (it & 1)), ((it >> 1) - 1) & 1, wc, SITE_BWD_DS_READY);
+          if (!ok) break;
+        }
+        tmem_st32(tmem + lane_off + C::TM_DP, pk);
+        {
+          // dS^T row j -> shared memory, [128 keys][64 q] with the 128-byte swizzle
+          uint8_t* row = dsb_base + (it & 1) * C::DS_BYTES + j * 128;
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<uint4*>(row + ((c ^ (j & 7)) << 4)) =
+                make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+        }
+        fence_proxy_async_smem();
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(BAR(C::B_DSREADY));
+      }
+      if (!ok) break;
+      // unit epilogue: dV, dK rows of this key
+      ok = mbar_wait(BAR(C::B_ACCFULL), u_it & 1, wc, SITE_BWD_ACC_FULL);
+      if (!ok) break;
+      tc_fence_after();
+      ++u_it;
+#pragma unroll 1
+      for (int which = 0; which < 2; ++which) {
+        const float mul = which ? p.scale : 1.0f;
+        __nv_bfloat16* dst = which ? dk_row : dv_row;
+        const uint32_t col = which ? C::TM_DK : C::TM_DV;
+#pragma unroll 1
+        for (int c = 0; c < D; c += 32) {
+          uint32_t a[32];
+          tmem_ld32(tmem + lane_off + col + c, a);
+          uint32_t q[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) q[e] = pack_bf16x2(u2f(a[2 * e]) * mul, u2f(a[2 * e + 1]) * mul);
+          if (key_ok) {
+            uint4* o4 = reinterpret_cast<uint4*>(dst + c);
+            o4[0] = make_uint4(q[0], q[1], q[2], q[3]);
+            o4[1] = make_uint4(q[4], q[5], q[6], q[7]);
+            o4[2] = make_uint4(q[8], q[9], q[10], q[11]);
+            o4[3] = make_uint4(q[12], q[13], q[14], q[15]);
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(BAR(C::B_ACCEMPTY));
+    }
+  } else {
+    // ------------------------------------------------------------ dQ drain
+    const int dd = (warp & 3) * 32 + lane;                // head-dim index = TMEM lane
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    Walker w;
+    w.init(spec);
+    uint32_t it = 0;
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      Unit u;
+      if (!w.seek(snake_index(k, G, cta), u)) break;
+      if (u.cost == 0) continue;
+      const int n = u.cost * group;
+      const int m_first = first_qblock(u, p.causal);
+      for (int i = 0; i < n; ++i, ++it) {
+        const StepInfo st = step_of(i, u.cost, m_first, u.head, group);
+        ok = mbar_wait(BAR(C::B_DQFULL), it & 1, wc, SITE_BWD_DQ_FULL);
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t a[64];
+        tmem_ld64(tmem + lane_off + C::TM_DQ, a);
+        tc_fence_before();
+        mbar_arrive(BAR(C::B_DQEMPTY));
+        const int q0 = st.m * BMQ;
+        int nvalid = u.q_len - q0;
+        nvalid = nvalid < BMQ ? nvalid : BMQ;
+        float* dst = p.dq_acc + (((long long)u.q_start + q0) * p.Hq + st.h) * D + dd;
+        const long long rstride = (long long)p.Hq * D;
+#pragma unroll
+        for (int c = 0; c < BMQ; ++c)
+          if (c < nvalid) atomicAdd(dst + c * rstride, u2f(a[c]));
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == MMA_WARP) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+#undef BAR
+}
+
+// D and LSE*log2e into the padded row arrays; zero the dQ accumulator.
+// One warp per (row, head).
+template <int D>
+__global__ void bwd_pre_kernel(BwdParams p, BwdAux aux) {
+  const long long nrows = (long long)p.total_q * p.Hq;
+  const int lane = threadIdx.x & 31;
+  const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
+  for (long long r = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < nrows;
+       r += warps) {
+    const int t = (int)(r / p.Hq), h = (int)(r % p.Hq);
+    int seq, q_start;
+    if (p.cu) {
+      int lo = 0, hi = p.nseq;                 // last seq with cu[seq] <= t (non-empty)
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (p.cu[mid] <= t) lo = mid; else hi = mid;
+      }
+      seq = lo;
+      q_start = p.cu[lo];
+    } else {
+      seq = t / p.Sq;
+      q_start = seq * p.Sq;
+    }
+    const __nv_bfloat16* orow = aux.o + ((long long)t * p.Hq + h) * D;
+    const __nv_bfloat16* grow = aux.dout + ((long long)t * p.Hq + h) * D;
+    float acc = 0.f;
+    for (int c = lane * 4; c < D; c += 128) {
+      const uint2 ov = *reinterpret_cast<const uint2*>(orow + c);
+      const uint2 gv = *reinterpret_cast<const uint2*>(grow + c);
+      const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
+      const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&gv);
+      for (int e = 0; e < 2; ++e) {
+        const float2 of = __bfloat1622float2(o2[e]);
+        const float2 gf = __bfloat1622float2(g2[e]);
+        acc = fmaf(of.x, gf.x, acc);
+        acc = fmaf(of.y, gf.y, acc);
+      }
+    }
+    for (int sh = 16; sh > 0; sh >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, sh);
+    float* zr = p.dq_acc + ((long long)t * p.Hq + h) * D;
+    for (int c = lane * 4; c < D; c += 128)
+      *reinterpret_cast<float4*>(zr + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (lane == 0) {
+      const int row = t - q_start;
+      const float lse = aux.lse[(p.cu ? 0ll : (long long)seq * aux.lse_seqstride) +
+                                (long long)h * aux.lse_hstride + (p.cu ? t : row)];
+      const long long pi = (long long)h * p.pad_hstride + pad_start(seq, q_start) + row;
+      const_cast<float*>(p.lse2)[pi] = lse * 1.4426950408889634f;
+      const_cast<float*>(p.delta)[pi] = acc;
+    }
+  }
+}
+
+// Padding rows [q_len, round_up(q_len, 64)) of every sequence: LSE = +inf, D = 0.
+__global__ void bwd_pad_kernel(BwdParams p) {
+  const int seq = blockIdx.x, h = blockIdx.y, r = threadIdx.x;   // 64 threads
+  int q_start, q_len;
+  if (p.cu) {
+    q_start = p.cu[seq];
+    q_len = p.cu[seq + 1] - q_start;
+  } else {
+    q_start = seq * p.Sq;
+    q_len = p.Sq;
+  }
+  const int row = ((q_len + 63) & ~63) - 64 + r;
+  if (row >= q_len && row >= 0) {
+    const long long pi = (long long)h * p.pad_hstride + pad_start(seq, q_start) + row;
+    const_cast<float*>(p.lse2)[pi] = INFINITY;
+    const_cast<float*>(p.delta)[pi] = 0.f;
+  }
+}
+
+__global__ void bwd_convert_kernel(const float* __restrict__ acc, __nv_bfloat16* __restrict__ dq,
+                                   long long n8, float scale) {
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n8;
+       i += (long long)gridDim.x * blockDim.x) {
+    const float4 a = reinterpret_cast<const float4*>(acc)[2 * i];
+    const float4 b = reinterpret_cast<const float4*>(acc)[2 * i + 1];
+    uint4 o;
+    o.x = pack_bf16x2(a.x * scale, a.y * scale);
+    o.y = pack_bf16x2(a.z * scale, a.w * scale);
+    o.z = pack_bf16x2(b.x * scale, b.y * scale);
+    o.w = pack_bf16x2(b.z * scale, b.w * scale);
+    reinterpret_cast<uint4*>(dq)[i] = o;
+  }
+}
+
+}  // namespace bwdk
+
+template <int D, int POLY8>
+static cudaError_t launch_main(const BwdParams& p, int grid, cudaStream_t stream) {
+  auto kern = bwdk::bwd_kernel<D, POLY8>;
+  const int smem = bwdk::Cfg<D>::SMEM_BYTES;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, bwdk::NUM_THREADS, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd(const BwdParams& p, const BwdAux& aux, int d, int grid,
+                       cudaStream_t stream, int poly8) {
+  if (d != 128) return cudaErrorNotSupported;
+  const long long rows = (long long)p.total_q * p.Hq;
+  if (rows > 0) {
+    const int blocks = (int)((rows + 7) / 8 < 65535 * 8 ? (rows + 7) / 8 : 65535 * 8);
+    bwdk::bwd_pre_kernel<128><<<blocks, 256, 0, stream>>>(p, aux);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    if (p.nseq > 0) {
+      bwdk::bwd_pad_kernel<<<dim3(p.nseq, p.Hq), 64, 0, stream>>>(p);
+      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+  }
+  if (p.total_k > 0) {
+    cudaEvent_t ev0, ev1;
+    take_events(1, &ev0, &ev1);
+    if (ev0) cudaEventRecord(ev0, stream);
+    cudaError_t e;
+    switch (poly8) {
+      case 0: e = launch_main<128, 0>(p, grid, stream); break;
+      case 2: e = launch_main<128, 2>(p, grid, stream); break;
+      case 4: e = launch_main<128, 4>(p, grid, stream); break;
+      default: e = cudaErrorInvalidValue;
+    }
+    if (ev1) cudaEventRecord(ev1, stream);
+    if (e != cudaSuccess) return e;
+  }
+  if (rows > 0) {
+    const long long n8 = rows * d / 8;
+    const int blocks = (int)(n8 / 256 + 1 < 152 * 16 ? n8 / 256 + 1 : 152 * 16);
+    bwdk::bwd_convert_kernel<<<blocks, 256, 0, stream>>>(p.dq_acc, aux.dq, n8, p.scale);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
 }  // namespace fa

@@ -10,11 +10,12 @@
 // lineage described in "FlashAttention-4 Conquers Asymmetric GPU Hardware
 // Scaling" (episode description).
 //
-// One persistent CTA per SM, 10 warps:
+// One persistent CTA per SM, 12 warps (3 warpgroups):
 //   warps 0-3  softmax for Q tile 0 (one thread per row = TMEM lane)
 //   warps 4-7  softmax for Q tile 1
 //   warp  8    TMEM allocation + MMA issue (one elected thread)
 //   warp  9    TMA producer (one elected thread)
+//   warps 10-11 idle (they complete the third warpgroup for the register split)
 // Work unit: 2 x 128 query rows of one (sequence, query head). K/V blocks of 128
 // keys stream through an mbarrier ring of shared-memory stages (K_j, V_j, ...).
 // TMEM (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256,256+d), O_1 after it;
@@ -35,9 +36,14 @@ namespace fwdk {
 constexpr int BM = 128;         // query rows per tile
 constexpr int BN = 128;         // keys per KV block
 constexpr int UNIT_ROWS = 2 * BM;
-constexpr int NUM_THREADS = 320;
+constexpr int NUM_THREADS = 384;   // 3 warpgroups: softmax 0, softmax 1, MMA/TMA (+2 idle warps)
 constexpr int MMA_WARP = 8;
 constexpr int TMA_WARP = 9;
+// Register split: launch gives 168 per thread (65536 / 384, rounded down to 8);
+// the MMA/TMA warpgroup gives back down to 112 and the softmax warpgroups take
+// 192: 2*128*192 + 128*112 = 63488 <= 384*168 = 64512 (no spills either side).
+constexpr int REGS_SOFTMAX = 192;
+constexpr int REGS_CONTROL = 112;
 constexpr int MAX_SEQ_SMEM = 1024;
 
 template <int D>
@@ -152,7 +158,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) fwd_kernel(const __grid_consta
   const int cta = blockIdx.x;
   const int group = p.Hq / p.Hkv;
 
-  if (warp == TMA_WARP) {
+  if (warp >= 8) {
+    regs_dec<REGS_CONTROL>();
+  if (warp >= 10) {
+    // spare warps of the control warpgroup: nothing to do
+  } else if (warp == TMA_WARP) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       Walker w;
@@ -275,7 +285,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) fwd_kernel(const __grid_consta
         drain_wait(BAR(C::B_DRAIN), 0, 100000000ull);
       }
     }
+  }
   } else {
+    regs_inc<REGS_SOFTMAX>();
     // ------------------------------------------------------------ softmax
     const int t = warp >> 2;                 // Q tile of this warpgroup
     const int lg = warp & 3;                 // TMEM lane quarter
@@ -313,7 +325,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) fwd_kernel(const __grid_consta
         const int lim = row + 1 + (u.k_len - u.q_len);
         kv_lim = lim < kv_lim ? lim : kv_lim;
       }
-      float m_ref = -INFINITY, l = 0.f;
+      float m_ref = -INFINITY, l = 0.f, lp = 0.f;
       for (int j = 0; j < n; ++j) {
         ok = mbar_wait(BAR(C::B_SFULL + t), sp_it & 1, wc, SITE_FWD_S_FULL);
         if (!ok) break;
@@ -362,11 +374,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) fwd_kernel(const __grid_consta
               tmem_st32(tO + c, o);
             }
             l *= alpha;
+            lp *= alpha;
             m_ref = m_new;
           }
         }
         const float msub = m_ref == -INFINITY ? 0.f : m_ref;
-        float la[4] = {0.f, 0.f, 0.f, 0.f};
+        // Two row sums: of the fp32 p (for the LSE) and of the bf16-rounded P
+        // that the PV MMA actually multiplies (for normalising O, so that the
+        // weights applied to V sum to one).
+        float la[2] = {0.f, 0.f}, lb[2] = {0.f, 0.f};
         uint32_t pk[64];
 #pragma unroll
         for (int c = 0; c < 64; ++c) {
@@ -374,10 +390,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) fwd_kernel(const __grid_consta
           const float x1 = __fmaf_rn(s[2 * c + 1], sl2, -msub);
           const float p0 = ((2 * c) & 7) < POLY8 ? exp2_poly(x0) : ex2_mufu(x0);
           const float p1 = ((2 * c + 1) & 7) < POLY8 ? exp2_poly(x1) : ex2_mufu(x1);
-          la[c & 3] += p0 + p1;
-          pk[c] = pack_bf16x2(p0, p1);
+          const uint32_t pb = pack_bf16x2(p0, p1);
+          la[c & 1] += p0 + p1;
+          lb[c & 1] += __uint_as_float(pb << 16) + __uint_as_float(pb & 0xffff0000u);
+          pk[c] = pb;
         }
-        l += (la[0] + la[1]) + (la[2] + la[3]);
+        l += la[0] + la[1];
+        lp += lb[0] + lb[1];
         tmem_st32(tS, pk);
         tmem_st32(tS + 32, pk + 32);
         tmem_st_wait();
@@ -390,7 +409,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) fwd_kernel(const __grid_consta
       if (!ok) break;
       tc_fence_after();
       ++u_it;
-      const float inv = l > 0.f ? 1.0f / l : 0.f;
+      const float inv = lp > 0.f ? 1.0f / lp : 0.f;
 #pragma unroll 1
       for (int c = 0; c < D; c += 32) {
         uint32_t o[32];

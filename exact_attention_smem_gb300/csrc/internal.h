@@ -27,8 +27,10 @@ struct Knobs {
   int bwd_poly8 = 0;             // same for the backward
   long long timeout_ns = 2000000000LL;
   int grid_override = 0;         // >0: persistent grid size (schedule permutation tests)
+  cudaEvent_t ev[2][2] = {{nullptr, nullptr}, {nullptr, nullptr}};  // [fwd|bwd][start|stop]
 };
 Knobs knobs_snapshot();
+void take_events(int which, cudaEvent_t* start, cudaEvent_t* stop);  // one-shot timing events
 
 struct FwdParams {
   CUtensorMap tm_q, tm_k, tm_v;  // [T, H, d] views, 64-column x 128-row boxes, 128B swizzle
@@ -47,11 +49,13 @@ struct FwdParams {
 };
 
 struct BwdParams {
-  CUtensorMap tm_q, tm_k, tm_v, tm_do;
+  CUtensorMap tm_q, tm_do;       // [T, Hq, d] views, 64-column x 64-row boxes, 128B swizzle
+  CUtensorMap tm_k, tm_v;        // [T, Hkv, d] views, 64-column x 128-row boxes
   __nv_bfloat16 *dk, *dv;
-  float* dq_acc;                 // fp32 [T, Hq, d]
-  const float* lse_log2;         // fp32 [Hq, T] (LSE * log2 e)
-  const float* delta;            // fp32 [Hq, T]
+  float* dq_acc;                 // fp32 [Tq, Hq, d]
+  const float* lse2;             // fp32 [Hq][pad_hstride] padded per sequence: LSE * log2(e)
+  const float* delta;            // fp32 [Hq][pad_hstride] padded: D_i = sum_c dO_ic O_ic
+  long long pad_hstride;         // floats per head in the padded row arrays
   const int* cu;
   int nseq, Hq, Hkv, Sq, Sk, total_q, total_k, causal;
   float scale_log2, scale;
@@ -59,12 +63,28 @@ struct BwdParams {
   unsigned long long timeout_ns;
 };
 
+// Padded per-sequence row arrays used by the backward: sequence i's rows start
+// at a 64-float boundary, so every 64-row block is one aligned 256-byte copy.
+__host__ __device__ __forceinline__ long long pad_start(int seq_i, int q_start) {
+  return (long long)((q_start + 63) & ~63) + 128ll * seq_i;
+}
+__host__ __device__ __forceinline__ long long pad_hstride(long long T, int nseq) {
+  return ((T + 63) & ~63ll) + 128ll * (nseq + 1);
+}
+
 // Launchers (fwd.cu / bwd.cu). Return a cudaError_t.
 cudaError_t launch_fwd(const FwdParams& p, int d, int grid, cudaStream_t stream, int poly8);
 int fwd_units_total(const FwdParams& p);
-cudaError_t launch_bwd(const BwdParams& p, int d, int grid, cudaStream_t stream, int poly8,
-                       const __nv_bfloat16* o, const __nv_bfloat16* dout, const float* lse,
-                       __nv_bfloat16* dq, int lse_hstride, long long lse_seqstride);
+struct BwdAux {                  // inputs of the preprocess / convert passes
+  const __nv_bfloat16* o;
+  const __nv_bfloat16* dout;
+  const float* lse;              // caller layout (dense [B][Hq][Sq], packed [Hq][T])
+  int lse_hstride;
+  long long lse_seqstride;
+  __nv_bfloat16* dq;
+};
+cudaError_t launch_bwd(const BwdParams& p, const BwdAux& aux, int d, int grid,
+                       cudaStream_t stream, int poly8);
 
 int num_sms();
 int* device_error_word();

@@ -100,6 +100,15 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, uint
       "l"(tmap), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
 }
+// 1-D bulk copy global -> this CTA's shared memory (16-byte aligned, size % 16 == 0).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
 // Generic-proxy writes to shared memory become visible to the async proxy
 // (tensor core operand reads, TMA stores).
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -239,6 +248,16 @@ __device__ __forceinline__ void tmem_st_wait() {
 
 #undef FA_R8
 #undef FA_S8
+
+// Register reallocation between warpgroups (executed by all warps of a warpgroup).
+template <int N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
 
 // ------------------------------------------------------------------ numerics
 __device__ __forceinline__ float ex2_mufu(float x) {

@@ -122,6 +122,16 @@ FA_API int fa_get_device_error(int* code, int clear);
  */
 FA_API int fa_debug_set(const char* key, double value);
 
+/*
+ * Measurement hook: the next fa_fwd call records `start` on its stream right
+ * before its kernel and `stop` right after; the next fa_bwd call does the same
+ * around its main kernel (not the preprocess/convert passes). Each event pair
+ * is used once and then forgotten. Arguments are cudaEvent_t handles created by
+ * the caller on the current device (NULL clears). Process-wide, like the knobs.
+ */
+FA_API int fa_debug_set_events(int which /* 0 = forward, 1 = backward */, void* start,
+                               void* stop);
+
 /* ---- test hooks (exercise single device primitives; not the attention path) ---- */
 
 /* y[i] = 2^x[i] on the device: mode 0 software polynomial, mode 1 MUFU ex2. */
