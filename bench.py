@@ -97,6 +97,22 @@ class Clocks:
                 "reasons": reasons, "samples": len(rows)}
 
 
+def max_over_ranks(x: float, device=None) -> float:
+    """Largest value of x over all ranks (identity when not distributed)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(flops_per_step: float, steps: int, world: int, ms: float) -> float:
+    """Whole-job throughput: every rank ran `steps` steps of `flops_per_step` in `ms` (max)."""
+    return flops_per_step * steps * world / (ms * 1e-3) / 1e12
+
+
 def flops(w, lengths=None):
     from attn_inputs import flops_forward
     f = flops_forward(w, lengths)
@@ -158,10 +174,7 @@ def run_ours(args):
     ms = t0.elapsed_time(t1)
     fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
     bwd_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
-    if ws > 1:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, device="cuda")
 
     # end-to-end through the public API with host buffers (pinned), copies timed
     e2e = run_e2e(fa, w, x, args, stream) if rank == 0 else None
@@ -172,7 +185,7 @@ def run_ours(args):
         return
     peak_b, peak_s, kind = _peaks()
     per_step = (f_fwd + f_bwd)
-    value = per_step * args.steps * ws / (ms * 1e-3) / 1e12
+    value = job_tflops(per_step, args.steps, ws, ms)
     bwd_tf = f_bwd / (bwd_ms * 1e-3) / 1e12
     fwd_tf = f_fwd / (fwd_ms * 1e-3) / 1e12
     cpu = cpu_baseline(args) if not args.no_cpu else None

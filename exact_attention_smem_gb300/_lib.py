@@ -40,6 +40,7 @@ _SIGS = {
     "fa_debug_set_events": (_I, [_I, _P, _P]),
     "fa_test_exp2": (_I, [_P, _P, _I, _I, _P]),
     "fa_exp2_poly_host": (_F, [_F]),
+    "fa_micro": (_I, [_I, _I, _P, _I, _P]),
     "fa_test_mma": (_I, [_P, _P, _P, _I, _I, _P]),
     "fa_test_wait_timeout": (_I, [_P, ctypes.c_double, _P]),
     "fa_sched_list": (_I, [_I, _I, _P, _I, _I, _I, _I, _I, _I, _P, _I]),
@@ -134,6 +135,10 @@ def fa_debug_set_events(which, start=None, stop=None):
 
 def fa_test_exp2(x, y, mode, stream=None):
     _check(load().fa_test_exp2(_ptr(x), _ptr(y), x.numel(), mode, _stream(stream)), "fa_test_exp2")
+
+
+def fa_micro(kind, iters, out_dev, ctas, stream=None):
+    _check(load().fa_micro(kind, iters, _ptr(out_dev), ctas, _stream(stream)), "fa_micro")
 
 
 def fa_exp2_poly_host(x: float) -> float:

@@ -21,6 +21,7 @@ cudaError_t launch_mma_probe(const __nv_bfloat16* A, const __nv_bfloat16* B, flo
                              int N, cudaStream_t st);
 cudaError_t launch_wait_timeout_probe(int* status, unsigned long long timeout_ns,
                                       cudaStream_t st);
+cudaError_t launch_micro(int kind, int iters, double* out, int ctas, cudaStream_t st);
 
 __device__ int g_error_word;  // first expired bounded wait (site code), per device
 
@@ -376,6 +377,17 @@ extern "C" int fa_test_exp2(const float* x, float* y, int n, int mode, void* str
 }
 
 extern "C" float fa_exp2_poly_host(float x) { return fa::exp2_poly(x); }
+
+extern "C" int fa_micro(int kind, int iters, double* out_dev, int ctas, void* stream) {
+  if (kind < 0 || kind > 2 || iters <= 0 || iters > (1 << 24) || !out_dev || ctas <= 0 ||
+      ctas > 4096)
+    return fail(FA_ERR_INVALID_ARG, "fa_micro arguments");
+  DevInfo* di = nullptr;
+  int st = device_info(&di);
+  if (st != FA_OK) return st;
+  cudaError_t e = launch_micro(kind, iters, out_dev, ctas, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : fail(FA_ERR_CUDA, "%s", cudaGetErrorString(e));
+}
 
 extern "C" int fa_test_mma(const void* A, const void* B, float* C, int mode, int N,
                            void* stream) {

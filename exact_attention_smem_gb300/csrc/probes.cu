@@ -166,3 +166,108 @@ cudaError_t launch_wait_timeout_probe(int* status, unsigned long long timeout_ns
 }
 
 }  // namespace fa
+
+namespace fa {
+
+// ---------------------------------------------------------------------------
+// Microbenchmarks (one CTA per SM; each CTA writes its clock64 span and op
+// count to out[2*blockIdx.x + {0,1}] as doubles).
+//   kind 0: MUFU ex2.approx throughput      (ops = exponentials)
+//   kind 1: software exp2 throughput        (ops = exponentials)
+//   kind 2: tcgen05 bf16 MMA throughput, M128 N256 K16, smem operands (ops = FLOPs)
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256, 1) micro_exp_kernel(int iters, int poly, double* out,
+                                                           float seed) {
+  float a[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) a[i] = -(seed + 0.001f * (threadIdx.x + i));
+  __syncthreads();
+  const long long t0 = clock64();
+  for (int it = 0; it < iters; ++it) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float y = poly ? exp2_poly(a[i]) : ex2_mufu(a[i]);
+      a[i] = -y - 0.5f;   // stays in (-1.5, -0.5): keeps a dependency chain per lane
+    }
+  }
+  __syncthreads();
+  const long long t1 = clock64();
+  float acc = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc += a[i];
+  if (acc == 12345.f) out[0] = acc;   // keep the work
+  if (threadIdx.x == 0) {
+    out[2 * blockIdx.x] = (double)(t1 - t0);
+    out[2 * blockIdx.x + 1] = (double)iters * 8.0 * blockDim.x;
+  }
+}
+
+__global__ void __launch_bounds__(128, 1) micro_mma_kernel(int iters, double* out, int* err) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (base - raw);
+  const uint32_t bar = base + 65536;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + 65536 + 64);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 65536 + 72);
+  const int warp = threadIdx.x >> 5;
+  for (int i = threadIdx.x; i < 65536 / 16; i += 128)
+    reinterpret_cast<uint4*>(smem)[i] = make_uint4(0x3c003c00u, 0, 0x3c003c00u, 0);
+  if (threadIdx.x == 0) {
+    mbar_init(bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  constexpr uint32_t idesc = idesc_bf16(128, 256, false, false);
+  long long t0 = 0, t1 = 0;
+  if (threadIdx.x == 0) {
+    t0 = clock64();
+    for (int it = 0; it < iters; ++it) {
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+        mma_ss(tmem, sdesc_sw128(base + kk * 32, 16384, 1024),
+               sdesc_sw128(base + 16384 + kk * 32, 32768, 1024), idesc, 1u);
+    }
+    tc_commit(bar);
+  }
+  const WaitCtl wc{err, abort_flag, 2000000000ull};
+  mbar_wait(bar, 0, wc, SITE_TEST);
+  if (threadIdx.x == 0) {
+    t1 = clock64();
+    out[2 * blockIdx.x] = (double)(t1 - t0);
+    out[2 * blockIdx.x + 1] = (double)iters * 4.0 * 2.0 * 128 * 256 * 16;
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+cudaError_t launch_micro(int kind, int iters, double* out, int ctas, cudaStream_t st) {
+  if (kind == 0 || kind == 1) {
+    micro_exp_kernel<<<ctas, 256, 0, st>>>(iters, kind, out, 0.37f);
+    return cudaGetLastError();
+  }
+  if (kind == 2) {
+    const int smem = 65536 + 128 + 1024;
+    cudaError_t e =
+        cudaFuncSetAttribute(micro_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    micro_mma_kernel<<<ctas, 128, smem, st>>>(iters, out, device_error_word());
+    return cudaGetLastError();
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace fa

@@ -137,6 +137,15 @@ FA_API int fa_debug_set_events(int which /* 0 = forward, 1 = backward */, void* 
 /* y[i] = 2^x[i] on the device: mode 0 software polynomial, mode 1 MUFU ex2. */
 FA_API int fa_test_exp2(const float* x, float* y, int n, int mode, void* stream);
 
+/*
+ * Microbenchmarks, one CTA per SM (`ctas` CTAs): each CTA writes two doubles to
+ * out_dev[2*cta + {0, 1}]: its clock64 span and the operations it performed.
+ *   kind 0: MUFU ex2 throughput, kind 1: software exp2 throughput (operations =
+ *   exponentials, 256 threads per CTA); kind 2: tcgen05 bf16 MMA throughput
+ *   (M128 N256 K16 from shared memory; operations = FLOPs). iters <= 2^24.
+ */
+FA_API int fa_micro(int kind, int iters, double* out_dev, int ctas, void* stream);
+
 /* Host twin of the device polynomial exp2 (identical operation sequence). */
 FA_API float fa_exp2_poly_host(float x);
 
