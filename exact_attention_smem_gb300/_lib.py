@@ -43,7 +43,7 @@ _SIGS = {
     "fa_micro": (_I, [_I, _I, _P, _I, _P]),
     "fa_test_mma": (_I, [_P, _P, _P, _I, _I, _P]),
     "fa_test_wait_timeout": (_I, [_P, ctypes.c_double, _P]),
-    "fa_sched_list": (_I, [_I, _I, _P, _I, _I, _I, _I, _I, _I, _P, _I]),
+    "fa_sched_list": (_I, [_I, _I, _P, _I, _I, _I, _I, _I, _I, _I, _P, _I]),
 }
 
 
@@ -154,17 +154,18 @@ def fa_test_wait_timeout(status_dev, timeout_ms, stream=None):
            "fa_test_wait_timeout")
 
 
-def fa_sched_list(kind, B, cu_seqlens_host, Sq, Sk, heads, causal, grid, cta):
+def fa_sched_list(kind, B, cu_seqlens_host, Sq, Sk, heads, causal, grid, cta, heads_per_group=0):
     """Return the (seq, row block, head, cost) units of one CTA, in order."""
     lib = load()
     cu = None
     if cu_seqlens_host is not None:
         arr = (ctypes.c_int * len(cu_seqlens_host))(*[int(x) for x in cu_seqlens_host])
         cu = ctypes.cast(arr, ctypes.c_void_p)
-    n = lib.fa_sched_list(kind, B, cu, Sq, Sk, heads, int(causal), grid, cta, None, 0)
+    n = lib.fa_sched_list(kind, B, cu, Sq, Sk, heads, int(causal), grid, cta, heads_per_group,
+                          None, 0)
     if n < 0:
         raise ValueError("fa_sched_list: bad arguments")
     out = (ctypes.c_int * (4 * max(n, 1)))()
-    lib.fa_sched_list(kind, B, cu, Sq, Sk, heads, int(causal), grid, cta,
+    lib.fa_sched_list(kind, B, cu, Sq, Sk, heads, int(causal), grid, cta, heads_per_group,
                       ctypes.cast(out, ctypes.c_void_p), n)
     return [tuple(out[4 * i:4 * i + 4]) for i in range(n)]

@@ -210,14 +210,15 @@ extern "C" int fa_fwd(const void* q, const void* k, const void* v, void* o, floa
   p.timeout_ns = (unsigned long long)kn.timeout_ns;
 
   // persistent grid: one CTA per SM, capped by an upper bound on the unit count
-  long long units;
-  if (sh.packed)
-    units = (long long)Hq * ((sh.Tq + 255) / 256 + B);
-  else
-    units = (long long)Hq * B * ((Sq + 255) / 256);
+  const long long units_per_head =
+      sh.packed ? (sh.Tq + 255) / 256 + B : (long long)B * ((Sq + 255) / 256);
+  const long long units = units_per_head * Hq;
   int grid = kn.grid_override > 0 ? kn.grid_override : di->sms;
   if (units < grid) grid = (int)units;
   if (grid < 1) grid = 1;
+  // The forward keeps one group (pure LPT): its K/V traffic is far from the
+  // DRAM roof, and static snake rounds balance best over a single LPT list.
+  p.hblock = Hq;
   cudaEvent_t ev0, ev1;
   take_events(0, &ev0, &ev1);
   if (ev0) cudaEventRecord(ev0, static_cast<cudaStream_t>(stream));
@@ -299,6 +300,9 @@ extern "C" int fa_bwd(const void* q, const void* k, const void* v, const void* o
   aux.lse_seqstride = sh.packed ? 0 : (long long)Hq * Sq;
   aux.dq = static_cast<__nv_bfloat16*>(dq);
   int grid = kn.grid_override > 0 ? kn.grid_override : di->sms;
+  const long long kv_units_per_head =
+      sh.packed ? (sh.Tk + 127) / 128 + B : (long long)B * ((Sk + 127) / 128);
+  p.hblock = pick_hblock(kv_units_per_head, Hkv, grid);
   cudaError_t e = launch_bwd(p, aux, d, grid, static_cast<cudaStream_t>(stream), kn.bwd_poly8);
   if (e == cudaErrorNotSupported)
     return fail(FA_ERR_UNSUPPORTED, "backward supports head dim 128 only");
@@ -414,12 +418,22 @@ extern "C" int fa_test_wait_timeout(int* status_dev, double timeout_ms, void* st
 }
 
 extern "C" int fa_sched_list(int kind, int B, const int* cu_seqlens_host, int Sq, int Sk,
-                             int heads, int causal, int grid, int cta, int* out, int max_units) {
+                             int heads, int causal, int grid, int cta, int heads_per_group,
+                             int* out, int max_units) {
   if ((kind != 0 && kind != 1) || B < 0 || Sq < 0 || Sk < 0 || heads <= 0 || grid <= 0 ||
-      cta < 0 || cta >= grid || max_units < 0 || (max_units > 0 && !out))
+      cta < 0 || cta >= grid || heads_per_group < 0 || max_units < 0 || (max_units > 0 && !out))
     return -1;
   SchedSpec s{cu_seqlens_host, B, Sq, Sk, heads, causal ? 1 : 0, kind == 0 ? 256 : 128,
-              kind == 0 ? 128 : 64, kind};
+              kind == 0 ? 128 : 64, kind, heads_per_group};
+  if (heads_per_group == 0) {
+    long long per_head = 0;
+    for (int i = 0; i < B; ++i) {
+      int qs, ql, ks, kl;
+      s.seq(i, qs, ql, ks, kl);
+      per_head += s.nblocks(ql, kl);
+    }
+    s.hblock = pick_hblock(per_head, heads, grid);
+  }
   Walker w;
   w.init(s);
   int count = 0;

@@ -24,8 +24,11 @@
 //
 // Warps: 0-3 P/dS (one thread per key row = TMEM lane), 4-7 dQ drain (one
 // thread per head-dim row of dQ^T), 8 MMA issue + TMEM allocation, 9 TMA.
-// TMEM columns: dV [0,d) dK [d,2d) S^T/P^T [2d,2d+64) dP^T/dS^T [2d+64,2d+128)
-// dQ^T [2d+128,2d+192).
+// TMEM columns: dV [0,d) dK [d,2d); S buffers [2d,2d+128) (two of 64 columns:
+// S^T of a step, then its P^T in bf16, then its dQ^T once dV has read P^T);
+// dP buffers [2d+128,2d+256) (dP^T, then dS^T in bf16). Steps alternate
+// buffers, so the MMAs of step i+2 are issued as soon as step i's buffers are
+// free while the P/dS warps work on step i+1.
 #include "exp2_poly.cuh"
 #include "internal.h"
 #include "ptx.cuh"
@@ -40,9 +43,14 @@ namespace bwdk {
 
 constexpr int BN = 128;   // keys per unit
 constexpr int BMQ = 64;   // query rows per step
-constexpr int NUM_THREADS = 320;
+constexpr int NUM_THREADS = 384;   // 3 warpgroups: P/dS, dQ drain, MMA/TMA (+2 idle warps)
 constexpr int MMA_WARP = 8;
 constexpr int TMA_WARP = 9;
+// Register split (launch: 168 per thread = 65536 / 384 rounded down to 8):
+// 128 * (REGS_PDS + REGS_DRAIN + REGS_CONTROL) <= 384 * 168.
+constexpr int REGS_PDS = 200;
+constexpr int REGS_DRAIN = 152;
+constexpr int REGS_CONTROL = 152;
 constexpr int NSTAGE = 3;
 constexpr int MAX_SEQ_SMEM = 1024;
 
@@ -64,15 +72,20 @@ struct Cfg {
   static constexpr int DS_OFF = ST_OFF + NSTAGE * STAGE_BYTES;
   static constexpr int BAR_OFF = DS_OFF + 2 * DS_BYTES;
   static constexpr int B_KVFULL = 0, B_KVEMPTY = 1, B_QDFULL = 2, B_QDEMPTY = 2 + NSTAGE,
-                       B_SFULL = 2 + 2 * NSTAGE, B_DPFULL = B_SFULL + 1, B_PREADY = B_SFULL + 2,
-                       B_DSREADY = B_SFULL + 3, B_DQFULL = B_SFULL + 4, B_DQEMPTY = B_SFULL + 5,
-                       B_DSBEMPTY = B_SFULL + 6, B_ACCFULL = B_DSBEMPTY + 2,
-                       B_ACCEMPTY = B_ACCFULL + 1, B_DRAIN = B_ACCFULL + 2, NBAR = B_DRAIN + 1;
+                       B_SFULL = 2 + 2 * NSTAGE,  // [2]
+                       B_DPFULL = B_SFULL + 2,    // [2]
+                       B_PREADY = B_DPFULL + 2, B_DSREADY = B_PREADY + 1,
+                       B_DQFULL = B_DSREADY + 1,  // [2]
+                       B_DQEMPTY = B_DQFULL + 2,  // [2]
+                       B_DSBEMPTY = B_DQEMPTY + 2,  // [2]
+                       B_ACCFULL = B_DSBEMPTY + 2, B_ACCEMPTY = B_ACCFULL + 1,
+                       B_DRAIN = B_ACCEMPTY + 1, NBAR = B_DRAIN + 1;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int CU_OFF = MISC_OFF + 16;
   static constexpr int SMEM_BYTES = CU_OFF + (MAX_SEQ_SMEM + 1) * 4 + 1024;
-  static constexpr uint32_t TM_DV = 0, TM_DK = D, TM_S = 2 * D, TM_DP = 2 * D + 64,
-                            TM_DQ = 2 * D + 128;
+  // dV, dK accumulators; two S^T buffers (also P^T, then dQ^T) and two dP^T
+  // buffers (also dS^T), so step i+1's S^T/dP^T MMAs run during step i's math.
+  static constexpr uint32_t TM_DV = 0, TM_DK = D, TM_SB = 2 * D, TM_DB = 2 * D + 128;
   static constexpr uint32_t IDESC_SDP = idesc_bf16(128, 64, false, false);  // S^T, dP^T
   static constexpr uint32_t IDESC_ACC = idesc_bf16(128, D, false, true);    // dV, dK (A in TMEM)
   static constexpr uint32_t IDESC_DQ = idesc_bf16(D, 64, true, true);       // dQ^T
@@ -162,14 +175,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_kernel(const __grid_consta
       mbar_init(BAR(C::B_QDFULL + s), 1);
       mbar_init(BAR(C::B_QDEMPTY + s), 1);
     }
-    mbar_init(BAR(C::B_SFULL), 1);
-    mbar_init(BAR(C::B_DPFULL), 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(BAR(C::B_SFULL + b), 1);
+      mbar_init(BAR(C::B_DPFULL + b), 1);
+      mbar_init(BAR(C::B_DQFULL + b), 1);
+      mbar_init(BAR(C::B_DQEMPTY + b), 128);
+      mbar_init(BAR(C::B_DSBEMPTY + b), 1);
+    }
     mbar_init(BAR(C::B_PREADY), 128);
     mbar_init(BAR(C::B_DSREADY), 128);
-    mbar_init(BAR(C::B_DQFULL), 1);
-    mbar_init(BAR(C::B_DQEMPTY), 128);
-    mbar_init(BAR(C::B_DSBEMPTY + 0), 1);
-    mbar_init(BAR(C::B_DSBEMPTY + 1), 1);
     mbar_init(BAR(C::B_ACCFULL), 1);
     mbar_init(BAR(C::B_ACCEMPTY), 128);
     mbar_init(BAR(C::B_DRAIN), 1);
@@ -194,13 +208,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_kernel(const __grid_consta
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  const SchedSpec spec{cu_in_smem ? cu_s : p.cu, p.nseq, p.Sq, p.Sk, p.Hkv, p.causal, BN, BMQ, 1};
+  const SchedSpec spec{cu_in_smem ? cu_s : p.cu, p.nseq, p.Sq, p.Sk, p.Hkv, p.causal, BN, BMQ, 1,
+                       p.hblock};
   const WaitCtl wc{p.err, abort_flag, p.timeout_ns};
   const int G = gridDim.x;
   const int cta = blockIdx.x;
   const int group = p.Hq / p.Hkv;
 
-  if (warp == TMA_WARP) {
+  if (warp >= 8) {
+    regs_dec<REGS_CONTROL>();
+  if (warp >= 10) {
+    // spare warps of the control warpgroup
+  } else if (warp == TMA_WARP) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       Walker w;
@@ -272,19 +291,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_kernel(const __grid_consta
         ok = mbar_wait(BAR(C::B_KVFULL), u_it & 1, wc, SITE_BWD_KV_FULL);
         if (!ok) break;
         tc_fence_after();
-        // prologue: S^T(0), dP^T(0)
-        {
-          const int s = it % NSTAGE;
-          ok = mbar_wait(BAR(C::B_QDFULL + s), (it / NSTAGE) & 1, wc, SITE_BWD_QD_FULL);
+        // prologue: S^T and dP^T of the unit's first two steps
+        for (int j = 0; j < 2 && j < n && ok; ++j) {
+          const uint32_t st = it + j, b = st & 1;
+          ok = mbar_wait(BAR(C::B_QDFULL + st % NSTAGE), (st / NSTAGE) & 1, wc, SITE_BWD_QD_FULL);
           if (!ok) break;
+          if (st >= 2) {   // the buffer's last dQ^T must have been drained
+            ok = mbar_wait(BAR(C::B_DQEMPTY + b), ((st >> 1) - 1) & 1, wc, SITE_BWD_DQ_EMPTY);
+            if (!ok) break;
+          }
           tc_fence_after();
-          const uint32_t sb = base + C::ST_OFF + s * C::STAGE_BYTES;
-          issue_kq<D>(tmem + C::TM_S, kt, sb);
-          tc_commit(BAR(C::B_SFULL));
-          issue_kq<D>(tmem + C::TM_DP, vt, sb + C::Q_TILE);
-          tc_commit(BAR(C::B_DPFULL));
+          const uint32_t sb = base + C::ST_OFF + (st % NSTAGE) * C::STAGE_BYTES;
+          issue_kq<D>(tmem + C::TM_SB + 64 * b, kt, sb);
+          tc_commit(BAR(C::B_SFULL + b));
+          issue_kq<D>(tmem + C::TM_DB + 64 * b, vt, sb + C::Q_TILE);
+          tc_commit(BAR(C::B_DPFULL + b));
         }
-        for (int i = 0; i < n; ++i, ++it) {
+        for (int i = 0; i < n && ok; ++i, ++it) {
+          const uint32_t b = it & 1;
           const int s = it % NSTAGE;
           const uint32_t sb = base + C::ST_OFF + s * C::STAGE_BYTES;
           ok = mbar_wait(BAR(C::B_PREADY), it & 1, wc, SITE_BWD_P_READY);
@@ -294,34 +318,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_kernel(const __grid_consta
             if (!ok) break;
           }
           tc_fence_after();
-          issue_acc<D>(tmem + C::TM_DV, tmem + C::TM_S, sb + C::Q_TILE, i > 0);   // dV += P^T dO
-          uint32_t sb2 = 0;
-          if (i + 1 < n) {
-            const int s2 = (it + 1) % NSTAGE;
-            ok = mbar_wait(BAR(C::B_QDFULL + s2), ((it + 1) / NSTAGE) & 1, wc, SITE_BWD_QD_FULL);
-            if (!ok) break;
-            tc_fence_after();
-            sb2 = base + C::ST_OFF + s2 * C::STAGE_BYTES;
-            issue_kq<D>(tmem + C::TM_S, kt, sb2);                                  // S^T(i+1)
-            tc_commit(BAR(C::B_SFULL));
-          }
+          issue_acc<D>(tmem + C::TM_DV, tmem + C::TM_SB + 64 * b, sb + C::Q_TILE, i > 0);  // dV += P^T dO
           ok = mbar_wait(BAR(C::B_DSREADY), it & 1, wc, SITE_BWD_DS_READY);
           if (!ok) break;
           tc_fence_after();
-          issue_acc<D>(tmem + C::TM_DK, tmem + C::TM_DP, sb, i > 0);              // dK += dS^T Q
-          if (it > 0) {
-            ok = mbar_wait(BAR(C::B_DQEMPTY), (it - 1) & 1, wc, SITE_BWD_DQ_EMPTY);
+          issue_acc<D>(tmem + C::TM_DK, tmem + C::TM_DB + 64 * b, sb, i > 0);  // dK += dS^T Q
+          issue_dq<D>(tmem + C::TM_SB + 64 * b, kt, base + C::DS_OFF + b * C::DS_BYTES);
+          tc_commit(BAR(C::B_DQFULL + b));
+          tc_commit(BAR(C::B_DSBEMPTY + b));
+          tc_commit(BAR(C::B_QDEMPTY + s));
+          if (i + 2 < n) {
+            const uint32_t st = it + 2;
+            ok = mbar_wait(BAR(C::B_QDFULL + st % NSTAGE), (st / NSTAGE) & 1, wc,
+                           SITE_BWD_QD_FULL);
             if (!ok) break;
             tc_fence_after();
+            const uint32_t sb2 = base + C::ST_OFF + (st % NSTAGE) * C::STAGE_BYTES;
+            issue_kq<D>(tmem + C::TM_DB + 64 * b, vt, sb2 + C::Q_TILE);             // dP^T(i+2)
+            tc_commit(BAR(C::B_DPFULL + b));
+            ok = mbar_wait(BAR(C::B_DQEMPTY + b), (it >> 1) & 1, wc, SITE_BWD_DQ_EMPTY);
+            if (!ok) break;
+            tc_fence_after();
+            issue_kq<D>(tmem + C::TM_SB + 64 * b, kt, sb2);                         // S^T(i+2)
+            tc_commit(BAR(C::B_SFULL + b));
           }
-          issue_dq<D>(tmem + C::TM_DQ, kt, base + C::DS_OFF + (it & 1) * C::DS_BYTES);
-          tc_commit(BAR(C::B_DQFULL));
-          tc_commit(BAR(C::B_DSBEMPTY + (it & 1)));
-          tc_commit(BAR(C::B_QDEMPTY + s));
-          if (i + 1 < n) {
-            issue_kq<D>(tmem + C::TM_DP, vt, sb2 + C::Q_TILE);                     // dP^T(i+1)
-            tc_commit(BAR(C::B_DPFULL));
-          } else {
+          if (i + 1 == n) {
             tc_commit(BAR(C::B_ACCFULL));
             tc_commit(BAR(C::B_KVEMPTY));
           }
@@ -333,7 +354,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_kernel(const __grid_consta
         drain_wait(BAR(C::B_DRAIN), 0, 100000000ull);
       }
     }
+  }
   } else if (warp < 4) {
+    regs_inc<REGS_PDS>();
     // ------------------------------------------------------------ P^T / dS^T
     const int j = warp * 32 + lane;                       // key row within the block
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
@@ -373,13 +396,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_kernel(const __grid_consta
         const float* d_s = reinterpret_cast<const float*>(stage + C::ST_D);
         ok = mbar_wait(BAR(C::B_QDFULL + s), (it / NSTAGE) & 1, wc, SITE_BWD_QD_FULL);
         if (!ok) break;
-        ok = mbar_wait(BAR(C::B_SFULL), it & 1, wc, SITE_BWD_S_FULL);
+        const uint32_t b = it & 1;
+        const uint32_t t_s = tmem + lane_off + C::TM_SB + 64 * b;
+        const uint32_t t_dp = tmem + lane_off + C::TM_DB + 64 * b;
+        ok = mbar_wait(BAR(C::B_SFULL + b), (it >> 1) & 1, wc, SITE_BWD_S_FULL);
         if (!ok) break;
         tc_fence_after();
         float pv[BMQ];
         {
           uint32_t a[64];
-          tmem_ld64(tmem + lane_off + C::TM_S, a);
+          tmem_ld64(t_s, a);
           // columns c with q0 + c < qmin are masked; a key past the sequence masks all
           const int cmin = key_ok ? qmin - st.m * BMQ : BMQ;
 #pragma unroll
@@ -398,18 +424,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_kernel(const __grid_consta
           uint32_t pk[32];
 #pragma unroll
           for (int c = 0; c < 32; ++c) pk[c] = pack_bf16x2(pv[2 * c], pv[2 * c + 1]);
-          tmem_st32(tmem + lane_off + C::TM_S, pk);
+          tmem_st32(t_s, pk);
         }
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(BAR(C::B_PREADY));
-        ok = mbar_wait(BAR(C::B_DPFULL), it & 1, wc, SITE_BWD_DP_FULL);
+        ok = mbar_wait(BAR(C::B_DPFULL + b), (it >> 1) & 1, wc, SITE_BWD_DP_FULL);
         if (!ok) break;
         tc_fence_after();
         uint32_t pk[32];
         {
           uint32_t a[64];
-          tmem_ld64(tmem + lane_off + C::TM_DP, a);
+          tmem_ld64(t_dp, a);
 #pragma unroll
           for (int c = 0; c < BMQ; c += 8) {
             const float4 d0 = *reinterpret_cast<const float4*>(d_s + c);
@@ -424,13 +450,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_kernel(const __grid_consta
           }
         }
         if (it >= 2) {
-          ok = mbar_wait(BAR(C::B_DSBEMPTY + (it & 1)), ((it >> 1) - 1) & 1, wc, SITE_BWD_DS_READY);
+          ok = mbar_wait(BAR(C::B_DSBEMPTY + b), ((it >> 1) - 1) & 1, wc, SITE_BWD_DS_READY);
           if (!ok) break;
         }
-        tmem_st32(tmem + lane_off + C::TM_DP, pk);
+        tmem_st32(t_dp, pk);
         {
           // dS^T row j -> shared memory, [128 keys][64 q] with the 128-byte swizzle
-          uint8_t* row = dsb_base + (it & 1) * C::DS_BYTES + j * 128;
+          uint8_t* row = dsb_base + b * C::DS_BYTES + j * 128;
 #pragma unroll
           for (int c = 0; c < 8; ++c)
             *reinterpret_cast<uint4*>(row + ((c ^ (j & 7)) << 4)) =
@@ -472,6 +498,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_kernel(const __grid_consta
       mbar_arrive(BAR(C::B_ACCEMPTY));
     }
   } else {
+    regs_dec<REGS_DRAIN>();
     // ------------------------------------------------------------ dQ drain
     const int dd = (warp & 3) * 32 + lane;                // head-dim index = TMEM lane
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
@@ -487,21 +514,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_kernel(const __grid_consta
       const int m_first = first_qblock(u, p.causal);
       for (int i = 0; i < n; ++i, ++it) {
         const StepInfo st = step_of(i, u.cost, m_first, u.head, group);
-        ok = mbar_wait(BAR(C::B_DQFULL), it & 1, wc, SITE_BWD_DQ_FULL);
+        const uint32_t b = it & 1;
+        ok = mbar_wait(BAR(C::B_DQFULL + b), (it >> 1) & 1, wc, SITE_BWD_DQ_FULL);
         if (!ok) break;
         tc_fence_after();
         uint32_t a[64];
-        tmem_ld64(tmem + lane_off + C::TM_DQ, a);
+        tmem_ld64(tmem + lane_off + C::TM_SB + 64 * b, a);
         tc_fence_before();
-        mbar_arrive(BAR(C::B_DQEMPTY));
+        mbar_arrive(BAR(C::B_DQEMPTY + b));
         const int q0 = st.m * BMQ;
-        int nvalid = u.q_len - q0;
-        nvalid = nvalid < BMQ ? nvalid : BMQ;
+        const int nvalid = u.q_len - q0;
         float* dst = p.dq_acc + (((long long)u.q_start + q0) * p.Hq + st.h) * D + dd;
         const long long rstride = (long long)p.Hq * D;
+        if (nvalid >= BMQ) {
 #pragma unroll
-        for (int c = 0; c < BMQ; ++c)
-          if (c < nvalid) atomicAdd(dst + c * rstride, u2f(a[c]));
+          for (int c = 0; c < BMQ; ++c) atomicAdd(dst + c * rstride, u2f(a[c]));
+        } else {
+#pragma unroll
+          for (int c = 0; c < BMQ; ++c)
+            if (c < nvalid) atomicAdd(dst + c * rstride, u2f(a[c]));
+        }
       }
     }
   }

@@ -152,7 +152,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) fwd_kernel(const __grid_consta
   const uint32_t tmem = *tmem_slot;
 
   const SchedSpec spec{cu_in_smem ? cu_s : p.cu, p.nseq, p.Sq, p.Sk, p.Hq, p.causal,
-                       UNIT_ROWS, BN, 0};
+                       UNIT_ROWS, BN, 0, p.hblock};
   const WaitCtl wc{p.err, abort_flag, p.timeout_ns};
   const int G = gridDim.x;
   const int cta = blockIdx.x;

@@ -44,6 +44,7 @@ struct FwdParams {
   long long lse_seqstride;       // dense: Hq*Sq per batch entry; packed: unused (0)
   float scale_log2;              // softmax scale * log2(e)
   float tau;                     // rescale threshold (base 2)
+  int hblock;                    // heads per scheduler group
   int* err;
   unsigned long long timeout_ns;
 };
@@ -59,6 +60,7 @@ struct BwdParams {
   const int* cu;
   int nseq, Hq, Hkv, Sq, Sk, total_q, total_k, causal;
   float scale_log2, scale;
+  int hblock;                    // KV heads per scheduler group
   int* err;
   unsigned long long timeout_ns;
 };

@@ -5,10 +5,17 @@
 //
 // A work unit is (sequence, row block, head). Its cost is the number of inner
 // blocks it walks: for the forward, KV blocks of 128 keys seen by a block of
-// query rows; for the backward, query blocks seen by a block of keys. Units are
-// listed in non-increasing cost (Graham's LPT list order); ties go by sequence,
-// then row block, then head, so the query heads sharing one KV head sit next
-// to each other and read the same K/V from L2 at about the same time.
+// query rows; for the backward, query blocks seen by a block of keys.
+//
+// The list is cut into head groups (`hblock` consecutive heads, all sequences)
+// processed one after the other; inside a group units are listed in
+// non-increasing cost (Graham's LPT list order), ties by sequence, row block,
+// then head. Grouping keeps the data the concurrently running CTAs share —
+// K/V of the forward, the fp32 dQ accumulator and Q/dO of the backward — small
+// enough to stay in L2 (the host picks `hblock` so that one group holds at
+// least one unit per CTA); LPT inside each group keeps the long units first,
+// and since groups follow each other without a barrier, only the last group's
+// short tail limits the balance at the end.
 //
 // The persistent grid deals the list out in "snake" rounds: in round r the G
 // CTAs take the next G units, in CTA order for even r and reversed for odd r,
@@ -32,6 +39,7 @@ struct SchedSpec {
   int unit_rows;   // rows per unit: fwd query rows, bwd keys
   int inner;       // rows per inner block: fwd keys per KV block, bwd query rows per block
   int kind;        // 0 forward, 1 backward
+  int hblock;      // heads per group (>= 1)
 
   __host__ __device__ __forceinline__ void seq(int i, int& qs, int& ql, int& ks, int& kl) const {
     if (cu) {
@@ -108,40 +116,50 @@ struct Unit {
   int q_start, q_len, k_start, k_len;
 };
 
-// Walks the LPT list: groups (cost level desc, sequence asc), inside a group row
-// blocks ascending then heads.
+// Walks the list: head groups in order; inside a group (cost level desc,
+// sequence asc) groups of units, inside those row blocks ascending then heads.
 struct Walker {
   SchedSpec s;
-  int level, seq_i, lo, hi;      // current group
-  long long gstart;              // list index of the group's first unit
+  int maxc, hb, h0, hcount;      // current head group: heads [h0, h0 + hcount)
+  int level, seq_i, lo, hi;      // current (level, sequence) run
+  long long gstart;              // list index of the run's first unit
   int qs, ql, ks, kl;
   bool done;
 
+  __host__ __device__ __forceinline__ void set_hblock(int b) {
+    hb = b;
+    h0 = b * s.hblock;
+    const int left = s.heads - h0;
+    hcount = left < s.hblock ? left : s.hblock;
+  }
   __host__ __device__ __forceinline__ void init(const SchedSpec& spec) {
     s = spec;
-    level = s.max_cost();
+    if (s.hblock < 1) s.hblock = 1;
+    maxc = s.max_cost();
+    set_hblock(0);
+    level = maxc;
     seq_i = -1;
     gstart = 0;
     lo = hi = 0;
-    done = false;
-    advance_group();
+    done = s.nseq == 0 || s.heads <= 0;
+    if (!done) advance_group();
   }
   __host__ __device__ __forceinline__ void advance_group() {
-    gstart += (long long)(hi - lo) * s.heads;
+    gstart += (long long)(hi - lo) * hcount;
+    lo = hi = 0;
     for (;;) {
       ++seq_i;
       if (seq_i >= s.nseq) {
         seq_i = 0;
         --level;
         if (level < 0) {
-          done = true;
-          lo = hi = 0;
-          return;
+          if (h0 + hcount >= s.heads) {
+            done = true;
+            return;
+          }
+          set_hblock(hb + 1);
+          level = maxc;
         }
-      }
-      if (s.nseq == 0) {
-        done = true;
-        return;
       }
       s.seq(seq_i, qs, ql, ks, kl);
       if (s.nblocks(ql, kl) == 0) continue;
@@ -151,12 +169,12 @@ struct Walker {
   }
   // Position on list entry `target` (targets must not decrease between calls).
   __host__ __device__ __forceinline__ bool seek(long long target, Unit& u) {
-    while (!done && target >= gstart + (long long)(hi - lo) * s.heads) advance_group();
+    while (!done && target >= gstart + (long long)(hi - lo) * hcount) advance_group();
     if (done) return false;
     const long long off = target - gstart;
     u.seq = seq_i;
-    u.m = lo + (int)(off / s.heads);
-    u.head = (int)(off % s.heads);
+    u.m = lo + (int)(off / hcount);
+    u.head = h0 + (int)(off % hcount);
     u.cost = level;
     u.q_start = qs;
     u.q_len = ql;
@@ -165,6 +183,15 @@ struct Walker {
     return true;
   }
 };
+
+// Heads per group: the fewest heads whose units cover `grid` CTAs at least once.
+__host__ __device__ __forceinline__ int pick_hblock(long long units_per_head, int heads, int grid) {
+  if (units_per_head <= 0) return heads > 0 ? heads : 1;
+  long long hb = (grid + units_per_head - 1) / units_per_head;
+  if (hb < 1) hb = 1;
+  if (hb > heads) hb = heads;
+  return (int)hb;
+}
 
 // List index of the k-th unit of CTA b among G (snake rounds).
 __host__ __device__ __forceinline__ long long snake_index(int k, int G, int b) {

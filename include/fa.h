@@ -168,13 +168,15 @@ FA_API int fa_test_wait_timeout(int* status_dev, double timeout_ms, void* stream
  * Host run of the work scheduler: writes, for CTA `cta` of a persistent grid
  * of `grid` CTAs, its units in execution order as 4 ints each
  * (sequence, row block, head, cost) into out (room for max_units units).
+ * heads_per_group: heads per scheduler group (0 = the kernels' own choice: the
+ * fewest heads whose units cover the grid).
  * kind 0 = forward (units of 256 query rows, cost = KV blocks of 128), kind 1
  * = backward (units of 128 keys, cost = query blocks of 64). cu_seqlens_host
  * is a HOST array (or NULL for dense B x Sq/Sk). Returns the number of units
  * (may exceed max_units; only max_units are written), or -1 on bad arguments.
  */
 FA_API int fa_sched_list(int kind, int B, const int* cu_seqlens_host, int Sq, int Sk, int heads,
-                  int causal, int grid, int cta, int* out, int max_units);
+                  int causal, int grid, int cta, int heads_per_group, int* out, int max_units);
 
 #ifdef __cplusplus
 }

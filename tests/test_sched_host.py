@@ -58,25 +58,28 @@ CASES = [
 ]
 
 
+@pytest.mark.parametrize("hpg", [0, 1, 2])
 @pytest.mark.parametrize("grid", [1, 5, 152])
 @pytest.mark.parametrize("case", CASES)
-def test_every_unit_once_with_its_cost(case, grid):
+def test_every_unit_once_with_its_cost(case, grid, hpg):
     kind, B, cu, Sq, Sk, heads, causal = case
     want = _brute_units(kind, B, cu, Sq, Sk, heads, causal)
     got = {}
     for cta in range(grid):
-        for (s, m, h, c) in fa_sched_list(kind, B, cu, Sq, Sk, heads, causal, grid, cta):
+        for (s, m, h, c) in fa_sched_list(kind, B, cu, Sq, Sk, heads, causal, grid, cta, hpg):
             assert (s, m, h) not in got
             got[(s, m, h)] = c
     assert got == want
 
 
+@pytest.mark.parametrize("hpg", [0, 1, 2, 3])
 @pytest.mark.parametrize("case", CASES)
-def test_list_order_is_longest_first(case):
-    """Interleaving the CTAs' lists back into list order gives non-increasing cost."""
+def test_list_order_is_grouped_then_longest_first(case, hpg):
+    """Interleaving the CTAs' lists back into list order gives head groups in
+    order, each in non-increasing cost (pure LPT when one group holds all heads)."""
     kind, B, cu, Sq, Sk, heads, causal = case
     G = 7
-    per = [fa_sched_list(kind, B, cu, Sq, Sk, heads, causal, G, b) for b in range(G)]
+    per = [fa_sched_list(kind, B, cu, Sq, Sk, heads, causal, G, b, hpg) for b in range(G)]
     order = []
     for k in itertools.count():
         row = [per[b][k] if k < len(per[b]) else None for b in range(G)]
@@ -85,13 +88,29 @@ def test_list_order_is_longest_first(case):
         if k % 2:
             row = row[::-1]
         order += [x for x in row if x is not None]
-    costs = [u[3] for u in order]
-    assert costs == sorted(costs, reverse=True)
+    if hpg == 0:
+        return   # group size chosen from the grid; covered by the other values
+    groups = [u[2] // hpg for u in order]
+    assert groups == sorted(groups)
+    for g in set(groups):
+        costs = [u[3] for u in order if u[2] // hpg == g]
+        assert costs == sorted(costs, reverse=True)
+
+
+def test_auto_group_covers_the_grid():
+    """The kernels' own group size: the fewest heads whose units fill the grid."""
+    units = fa_sched_list(1, 1, None, 32768, 32768, 32, True, 152, 0)
+    assert len({u[2] for u in units[:1]}) == 1
+    # 256 key blocks per head >= 152 CTAs: one head per group, so CTA 0's first
+    # two units come from heads 0 and 0 or 1, never from far-apart heads
+    assert units[0][2] == 0 and units[1][2] <= 1
 
 
 def test_causal_balance_near_lpt_bound():
     """Long causal batch: per-CTA total cost within a few percent of the mean."""
     G = 152
-    loads = [sum(u[3] for u in fa_sched_list(0, 1, None, 32768, 32768, 32, True, G, b)) for b in range(G)]
-    mean = sum(loads) / G
-    assert max(loads) <= 1.03 * mean
+    for kind, hpg in ((0, 32), (1, 0)):     # the kernels' choices: fwd one group, bwd auto
+        loads = [sum(u[3] for u in fa_sched_list(kind, 1, None, 32768, 32768, 32, True, G, b, hpg))
+                 for b in range(G)]
+        mean = sum(loads) / G
+        assert max(loads) <= 1.03 * mean, (kind, max(loads) / mean)
