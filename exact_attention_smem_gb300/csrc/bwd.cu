@@ -1,9 +1,10 @@
 // Backward attention for sm_103a: dQ, dK, dV from Q, K, V, O, dO and LSE.
 //
 // Three kernels on one stream:
-//   1. preprocess: D_i = sum_c dO_ic O_ic and LSE_i * log2(e) into padded row
-//      arrays (each sequence starts on a 64-row boundary so one 64-row block is
-//      one aligned 256-byte bulk copy), padding rows get LSE = +inf and D = 0,
+//   1. preprocess: -D_i = -sum_c dO_ic O_ic and -LSE_i * log2(e) into padded
+//      row arrays (each sequence starts on a 64-row boundary so one 64-row
+//      block is one aligned 256-byte bulk copy; stored negated so the main
+//      kernel uses them as FMA addends), padding rows get LSE = +inf and D = 0,
 //      and the fp32 dQ accumulator is zeroed;
 //   2. main: one persistent CTA per SM walks (sequence, 128-key block, KV head)
 //      units longest-first. For each query head of the KV group and each block
@@ -48,8 +49,8 @@ constexpr int MMA_WARP = 8;
 constexpr int TMA_WARP = 9;
 // Register split (launch: 168 per thread = 65536 / 384 rounded down to 8):
 // 128 * (REGS_PDS + REGS_DRAIN + REGS_CONTROL) <= 384 * 168.
-constexpr int REGS_PDS = 200;
-constexpr int REGS_DRAIN = 152;
+constexpr int REGS_PDS = 224;
+constexpr int REGS_DRAIN = 128;
 constexpr int REGS_CONTROL = 152;
 constexpr int NSTAGE = 3;
 constexpr int MAX_SEQ_SMEM = 1024;
@@ -74,8 +75,13 @@ struct Cfg {
   static constexpr int B_KVFULL = 0, B_KVEMPTY = 1, B_QDFULL = 2, B_QDEMPTY = 2 + NSTAGE,
                        B_SFULL = 2 + 2 * NSTAGE,  // [2]
                        B_DPFULL = B_SFULL + 2,    // [2]
-                       B_PREADY = B_DPFULL + 2, B_DSREADY = B_PREADY + 1,
-                       B_DQFULL = B_DSREADY + 1,  // [2]
+                       // P/dS ready: one barrier per buffer. A single barrier
+                       // could be arrived on for steps i and i+1 before the MMA
+                       // thread waits on step i (S^T(i+1) is issued early), and
+                       // a parity wait cannot tell phases two apart.
+                       B_PREADY = B_DPFULL + 2,   // [2]
+                       B_DSREADY = B_PREADY + 2,  // [2]
+                       B_DQFULL = B_DSREADY + 2,  // [2]
                        B_DQEMPTY = B_DQFULL + 2,  // [2]
                        B_DSBEMPTY = B_DQEMPTY + 2,  // [2]
                        B_ACCFULL = B_DSBEMPTY + 2, B_ACCEMPTY = B_ACCFULL + 1,
@@ -181,9 +187,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_kernel(const __grid_consta
       mbar_init(BAR(C::B_DQFULL + b), 1);
       mbar_init(BAR(C::B_DQEMPTY + b), 128);
       mbar_init(BAR(C::B_DSBEMPTY + b), 1);
+      mbar_init(BAR(C::B_PREADY + b), 128);
+      mbar_init(BAR(C::B_DSREADY + b), 128);
     }
-    mbar_init(BAR(C::B_PREADY), 128);
-    mbar_init(BAR(C::B_DSREADY), 128);
     mbar_init(BAR(C::B_ACCFULL), 1);
     mbar_init(BAR(C::B_ACCEMPTY), 128);
     mbar_init(BAR(C::B_DRAIN), 1);
@@ -311,7 +317,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_kernel(const __grid_consta
           const uint32_t b = it & 1;
           const int s = it % NSTAGE;
           const uint32_t sb = base + C::ST_OFF + s * C::STAGE_BYTES;
-          ok = mbar_wait(BAR(C::B_PREADY), it & 1, wc, SITE_BWD_P_READY);
+          ok = mbar_wait(BAR(C::B_PREADY + b), (it >> 1) & 1, wc, SITE_BWD_P_READY);
           if (!ok) break;
           if (i == 0 && u_it > 0) {
             ok = mbar_wait(BAR(C::B_ACCEMPTY), (u_it - 1) & 1, wc, SITE_BWD_ACC_FULL);
@@ -319,7 +325,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_kernel(const __grid_consta
           }
           tc_fence_after();
           issue_acc<D>(tmem + C::TM_DV, tmem + C::TM_SB + 64 * b, sb + C::Q_TILE, i > 0);  // dV += P^T dO
-          ok = mbar_wait(BAR(C::B_DSREADY), it & 1, wc, SITE_BWD_DS_READY);
+          ok = mbar_wait(BAR(C::B_DSREADY + b), (it >> 1) & 1, wc, SITE_BWD_DS_READY);
           if (!ok) break;
           tc_fence_after();
           issue_acc<D>(tmem + C::TM_DK, tmem + C::TM_DB + 64 * b, sb, i > 0);  // dK += dS^T Q
@@ -392,8 +398,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_kernel(const __grid_consta
         const StepInfo st = step_of(i, u.cost, m_first, g, group);
         const int s = it % NSTAGE;
         const uint8_t* stage = smem + C::ST_OFF + s * C::STAGE_BYTES;
-        const float* lse_s = reinterpret_cast<const float*>(stage + C::ST_LSE);
-        const float* d_s = reinterpret_cast<const float*>(stage + C::ST_D);
+        const float* nlse_s = reinterpret_cast<const float*>(stage + C::ST_LSE);  // -LSE*log2e
+        const float* nd_s = reinterpret_cast<const float*>(stage + C::ST_D);      // -D
         ok = mbar_wait(BAR(C::B_QDFULL + s), (it / NSTAGE) & 1, wc, SITE_BWD_QD_FULL);
         if (!ok) break;
         const uint32_t b = it & 1;
@@ -402,33 +408,47 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_kernel(const __grid_consta
         ok = mbar_wait(BAR(C::B_SFULL + b), (it >> 1) & 1, wc, SITE_BWD_S_FULL);
         if (!ok) break;
         tc_fence_after();
-        float pv[BMQ];
+        // The row arrays hold -LSE*log2(e) and -D, so both phases are packed
+        // fp32 pairs: x = s*scale*log2e - LSE*log2e (one FFMA2 per pair) and
+        // dS = P * (dP - D) (one FADD2 + one FMUL2 per pair).
+        uint64_t p2[BMQ / 2];
         {
           uint32_t a[64];
           tmem_ld64(t_s, a);
           // columns c with q0 + c < qmin are masked; a key past the sequence masks all
           const int cmin = key_ok ? qmin - st.m * BMQ : BMQ;
+          const uint64_t sl2x2 = f2pack(sl2, sl2);
+          const bool mask = __any_sync(0xffffffffu, cmin > 0);
 #pragma unroll
           for (int c = 0; c < BMQ; c += 4) {
-            const float4 l4 = *reinterpret_cast<const float4*>(lse_s + c);
-            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+            const float4 l4 = *reinterpret_cast<const float4*>(nlse_s + c);
+            float x[4];
+            f2unpack(ffma2(f2pack(u2f(a[c]), u2f(a[c + 1])), sl2x2, f2pack(l4.x, l4.y)), x[0], x[1]);
+            f2unpack(ffma2(f2pack(u2f(a[c + 2]), u2f(a[c + 3])), sl2x2, f2pack(l4.z, l4.w)), x[2],
+                     x[3]);
+            float pe[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const float x = __fmaf_rn(u2f(a[c + e]), sl2, -lv[e]);
-              const float pe = ((c + e) & 7) < POLY8 ? exp2_poly(x) : ex2_mufu(x);
-              pv[c + e] = (c + e) < cmin ? 0.f : pe;
+              pe[e] = ((c + e) & 7) < POLY8 ? exp2_poly(x[e]) : ex2_mufu(x[e]);
+              if (mask) pe[e] = (c + e) < cmin ? 0.f : pe[e];
             }
+            p2[c / 2] = f2pack(pe[0], pe[1]);
+            p2[c / 2 + 1] = f2pack(pe[2], pe[3]);
           }
         }
         {
           uint32_t pk[32];
 #pragma unroll
-          for (int c = 0; c < 32; ++c) pk[c] = pack_bf16x2(pv[2 * c], pv[2 * c + 1]);
+          for (int c = 0; c < 32; ++c) {
+            float lo, hi;
+            f2unpack(p2[c], lo, hi);
+            pk[c] = pack_bf16x2(lo, hi);
+          }
           tmem_st32(t_s, pk);
         }
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(BAR(C::B_PREADY));
+        mbar_arrive(BAR(C::B_PREADY + b));
         ok = mbar_wait(BAR(C::B_DPFULL + b), (it >> 1) & 1, wc, SITE_BWD_DP_FULL);
         if (!ok) break;
         tc_fence_after();
@@ -437,16 +457,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_kernel(const __grid_consta
           uint32_t a[64];
           tmem_ld64(t_dp, a);
 #pragma unroll
-          for (int c = 0; c < BMQ; c += 8) {
-            const float4 d0 = *reinterpret_cast<const float4*>(d_s + c);
-            const float4 d1 = *reinterpret_cast<const float4*>(d_s + c + 4);
-            const float dv8[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
-#pragma unroll
-            for (int e = 0; e < 8; e += 2) {
-              const float ds0 = pv[c + e] * (u2f(a[c + e]) - dv8[e]);
-              const float ds1 = pv[c + e + 1] * (u2f(a[c + e + 1]) - dv8[e + 1]);
-              pk[(c + e) / 2] = pack_bf16x2(ds0, ds1);
-            }
+          for (int c = 0; c < BMQ; c += 4) {
+            const float4 d4 = *reinterpret_cast<const float4*>(nd_s + c);
+            float d0, d1, d2, d3;
+            f2unpack(fmul2(p2[c / 2], fadd2(f2pack(u2f(a[c]), u2f(a[c + 1])), f2pack(d4.x, d4.y))),
+                     d0, d1);
+            f2unpack(fmul2(p2[c / 2 + 1],
+                           fadd2(f2pack(u2f(a[c + 2]), u2f(a[c + 3])), f2pack(d4.z, d4.w))),
+                     d2, d3);
+            pk[c / 2] = pack_bf16x2(d0, d1);
+            pk[c / 2 + 1] = pack_bf16x2(d2, d3);
           }
         }
         if (it >= 2) {
@@ -465,7 +485,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_kernel(const __grid_consta
         fence_proxy_async_smem();
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(BAR(C::B_DSREADY));
+        mbar_arrive(BAR(C::B_DSREADY + b));
       }
       if (!ok) break;
       // unit epilogue: dV, dK rows of this key
@@ -548,7 +568,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_kernel(const __grid_consta
 #undef BAR
 }
 
-// D and LSE*log2e into the padded row arrays; zero the dQ accumulator.
+// -D and -LSE*log2e into the padded row arrays; zero the dQ accumulator.
 // One warp per (row, head).
 template <int D>
 __global__ void bwd_pre_kernel(BwdParams p, BwdAux aux) {
@@ -595,8 +615,8 @@ __global__ void bwd_pre_kernel(BwdParams p, BwdAux aux) {
       const float lse = aux.lse[(p.cu ? 0ll : (long long)seq * aux.lse_seqstride) +
                                 (long long)h * aux.lse_hstride + (p.cu ? t : row)];
       const long long pi = (long long)h * p.pad_hstride + pad_start(seq, q_start) + row;
-      const_cast<float*>(p.lse2)[pi] = lse * 1.4426950408889634f;
-      const_cast<float*>(p.delta)[pi] = acc;
+      const_cast<float*>(p.lse2)[pi] = -lse * 1.4426950408889634f;
+      const_cast<float*>(p.delta)[pi] = -acc;
     }
   }
 }
@@ -615,7 +635,7 @@ __global__ void bwd_pad_kernel(BwdParams p) {
   const int row = ((q_len + 63) & ~63) - 64 + r;
   if (row >= q_len && row >= 0) {
     const long long pi = (long long)h * p.pad_hstride + pad_start(seq, q_start) + row;
-    const_cast<float*>(p.lse2)[pi] = INFINITY;
+    const_cast<float*>(p.lse2)[pi] = -INFINITY;
     const_cast<float*>(p.delta)[pi] = 0.f;
   }
 }

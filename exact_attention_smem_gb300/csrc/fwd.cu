@@ -330,34 +330,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) fwd_kernel(const __grid_consta
         ok = mbar_wait(BAR(C::B_SFULL + t), sp_it & 1, wc, SITE_FWD_S_FULL);
         if (!ok) break;
         tc_fence_after();
-        float s[BN];
-        {
-          uint32_t a[64];
-          tmem_ld64(tS, a);
-#pragma unroll
-          for (int c = 0; c < 64; ++c) s[c] = u2f(a[c]);
-        }
-        {
-          uint32_t a[64];
-          tmem_ld64(tS + 64, a);
-#pragma unroll
-          for (int c = 0; c < 64; ++c) s[64 + c] = u2f(a[c]);
-        }
+        uint32_t sr[BN];                       // S row, raw fp32 bits
+        tmem_ld128(tS, sr);
         const int lim = kv_lim - j * BN;
         if (__any_sync(0xffffffffu, lim < BN)) {
 #pragma unroll
-          for (int c = 0; c < BN; ++c) s[c] = c < lim ? s[c] : -INFINITY;
+          for (int c = 0; c < BN; ++c) sr[c] = c < lim ? sr[c] : f2u(-INFINITY);
         }
-        float mx[8];
+        float mx[4];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) mx[i] = s[i];
+        for (int i = 0; i < 4; ++i) mx[i] = u2f(sr[i]);
 #pragma unroll
-        for (int c = 8; c < BN; c += 8)
+        for (int c = 4; c < BN; c += 8)
 #pragma unroll
-          for (int i = 0; i < 8; ++i) mx[i] = fmaxf(mx[i], s[c + i]);
-        const float mxa = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-        const float m_blk = mxa * sl2;
+          for (int i = 0; i < 4; ++i) mx[i] = fmax3(mx[i], u2f(sr[c + i]), u2f(sr[c + 4 + i]));
+        const float m_blk = fmaxf(fmax3(mx[0], mx[1], mx[2]), mx[3]) * sl2;
         if (j == 0) {
           m_ref = m_blk;
         } else {
@@ -365,12 +352,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) fwd_kernel(const __grid_consta
           if (__any_sync(0xffffffffu, need)) {
             const float m_new = need ? m_blk : m_ref;
             const float alpha = need ? ex2_mufu(m_ref - m_new) : 1.0f;
+            const uint64_t a2 = f2pack(alpha, alpha);
 #pragma unroll 1
             for (int c = 0; c < D; c += 32) {
               uint32_t o[32];
               tmem_ld32(tO + c, o);
 #pragma unroll
-              for (int i = 0; i < 32; ++i) o[i] = f2u(u2f(o[i]) * alpha);
+              for (int i = 0; i < 32; i += 2) {
+                float x0, x1;
+                f2unpack(fmul2(f2pack(u2f(o[i]), u2f(o[i + 1])), a2), x0, x1);
+                o[i] = f2u(x0);
+                o[i + 1] = f2u(x1);
+              }
               tmem_st32(tO + c, o);
             }
             l *= alpha;
@@ -381,24 +374,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) fwd_kernel(const __grid_consta
         const float msub = m_ref == -INFINITY ? 0.f : m_ref;
         // Two row sums: of the fp32 p (for the LSE) and of the bf16-rounded P
         // that the PV MMA actually multiplies (for normalising O, so that the
-        // weights applied to V sum to one).
-        float la[2] = {0.f, 0.f}, lb[2] = {0.f, 0.f};
+        // weights applied to V sum to one). Pairs use the f32x2 pipe.
+        const uint64_t sl2x2 = f2pack(sl2, sl2), negm2 = f2pack(-msub, -msub);
+        uint64_t la2[2] = {f2pack(0.f, 0.f), f2pack(0.f, 0.f)};
+        uint64_t lb2[2] = {f2pack(0.f, 0.f), f2pack(0.f, 0.f)};
         uint32_t pk[64];
 #pragma unroll
         for (int c = 0; c < 64; ++c) {
-          const float x0 = __fmaf_rn(s[2 * c], sl2, -msub);
-          const float x1 = __fmaf_rn(s[2 * c + 1], sl2, -msub);
+          float x0, x1;
+          f2unpack(ffma2(f2pack(u2f(sr[2 * c]), u2f(sr[2 * c + 1])), sl2x2, negm2), x0, x1);
           const float p0 = ((2 * c) & 7) < POLY8 ? exp2_poly(x0) : ex2_mufu(x0);
           const float p1 = ((2 * c + 1) & 7) < POLY8 ? exp2_poly(x1) : ex2_mufu(x1);
           const uint32_t pb = pack_bf16x2(p0, p1);
-          la[c & 1] += p0 + p1;
-          lb[c & 1] += __uint_as_float(pb << 16) + __uint_as_float(pb & 0xffff0000u);
+          la2[c & 1] = fadd2(la2[c & 1], f2pack(p0, p1));
+          lb2[c & 1] = fadd2(lb2[c & 1], f2pack(__uint_as_float(pb << 16),
+                                                __uint_as_float(pb & 0xffff0000u)));
           pk[c] = pb;
         }
-        l += la[0] + la[1];
-        lp += lb[0] + lb[1];
-        tmem_st32(tS, pk);
-        tmem_st32(tS + 32, pk + 32);
+        {
+          float a0, a1, b0, b1;
+          f2unpack(fadd2(la2[0], la2[1]), a0, a1);
+          f2unpack(fadd2(lb2[0], lb2[1]), b0, b1);
+          l += a0 + a1;
+          lp += b0 + b1;
+        }
+        tmem_st64(tS, pk);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(BAR(C::B_PFULL + t));

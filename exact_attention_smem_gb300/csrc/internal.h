@@ -54,8 +54,8 @@ struct BwdParams {
   CUtensorMap tm_k, tm_v;        // [T, Hkv, d] views, 64-column x 128-row boxes
   __nv_bfloat16 *dk, *dv;
   float* dq_acc;                 // fp32 [Tq, Hq, d]
-  const float* lse2;             // fp32 [Hq][pad_hstride] padded per sequence: LSE * log2(e)
-  const float* delta;            // fp32 [Hq][pad_hstride] padded: D_i = sum_c dO_ic O_ic
+  const float* lse2;             // fp32 [Hq][pad_hstride] padded per sequence: -LSE * log2(e)
+  const float* delta;            // fp32 [Hq][pad_hstride] padded: -D_i = -sum_c dO_ic O_ic
   long long pad_hstride;         // floats per head in the padded row arrays
   const int* cu;
   int nseq, Hq, Hkv, Sq, Sk, total_q, total_k, causal;
