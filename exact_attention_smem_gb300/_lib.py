@@ -33,6 +33,8 @@ _SIGS = {
     "fa_bwd_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I, _I]),
     "fa_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P,
                     ctypes.c_size_t, _P]),
+    "fa_bwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F,
+                            _P, _P]),
     "fa_status_string": (ctypes.c_char_p, [_I]),
     "fa_last_error": (ctypes.c_char_p, []),
     "fa_get_device_error": (_I, [ctypes.POINTER(_I), _I]),
@@ -109,6 +111,15 @@ def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, Sq, Sk, d, causal, sca
                          _ptr(dk), _ptr(dv), B, Hq, Hkv, Sq, Sk, d, int(causal), float(scale),
                          _ptr(cu_seqlens), _ptr(workspace), int(workspace_bytes),
                          _stream(stream)), "fa_bwd")
+
+
+def fa_bwd_noalloc(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, Sq, Sk, d, causal, scale,
+                   cu_seqlens=None, stream=None):
+    """fa_bwd with the library's built-in scratch instead of a caller workspace."""
+    _check(load().fa_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout),
+                                 _ptr(dq), _ptr(dk), _ptr(dv), B, Hq, Hkv, Sq, Sk, d, int(causal),
+                                 float(scale), _ptr(cu_seqlens), _stream(stream)),
+           "fa_bwd_noalloc")
 
 
 def fa_get_device_error(clear=True):

@@ -142,6 +142,16 @@ int validate_common(const void* const* ptrs, int nptrs, int B, int Hq, int Hkv, 
 
 }  // namespace
 
+int report_error(int status, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  t_last_error = buf;
+  return status;
+}
+
 Knobs knobs_snapshot() {
   std::lock_guard<std::mutex> lk(g_mu);
   return g_knobs;

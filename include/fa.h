@@ -94,6 +94,26 @@ FA_API int fa_bwd(const void* q, const void* k, const void* v, const void* o, co
            int Sk, int d, int causal, float scale, const int* cu_seqlens, void* workspace,
            size_t workspace_bytes, void* stream);
 
+/*
+ * Backward without a caller workspace, for callers that cannot allocate
+ * device memory (e.g. a runtime whose memory is all owned by its own pool
+ * allocator, or a latency-critical path where cudaMalloc, which can
+ * synchronise the device, is not allowed). Same arguments and results as
+ * fa_bwd minus the workspace: the scratch is a fixed array of
+ * FA_BWD_NOALLOC_SCRATCH_BYTES inside the library (held on every GPU that
+ * loads the library until exit). Problems needing more scratch than that
+ * (fa_bwd_workspace_bytes) are rejected with FA_ERR_WORKSPACE before any
+ * work. The first call on a device looks up the array's device address (make
+ * it before any stream capture). All calls share the array: calls that
+ * overlap on the GPU race and must be serialised by the caller. Allocates no
+ * memory. The FlashAttention-4 pages have no counterpart of this entry point.
+ */
+#define FA_BWD_NOALLOC_SCRATCH_BYTES (32u << 20)
+FA_API int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
+                          const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
+                          int Hq, int Hkv, int Sq, int Sk, int d, int causal, float scale,
+                          const int* cu_seqlens, void* stream);
+
 /* Static text for a status code. */
 FA_API const char* fa_status_string(int status);
 
