@@ -40,6 +40,7 @@ _SIGS = {
     "fa_get_device_error": (_I, [ctypes.POINTER(_I), _I]),
     "fa_debug_set": (_I, [ctypes.c_char_p, ctypes.c_double]),
     "fa_debug_set_events": (_I, [_I, _P, _P]),
+    "fa_debug_set_trace": (_I, [_P, ctypes.c_size_t]),
     "fa_test_exp2": (_I, [_P, _P, _I, _I, _P]),
     "fa_exp2_poly_host": (_F, [_F]),
     "fa_micro": (_I, [_I, _I, _P, _I, _P]),
@@ -142,6 +143,12 @@ def fa_debug_set_events(which, start=None, stop=None):
             ev.synchronize()
         return ctypes.c_void_p(ev.cuda_event)
     _check(load().fa_debug_set_events(which, h(start), h(stop)), "fa_debug_set_events")
+
+
+def fa_debug_set_trace(buf=None):
+    """Arm (device int64 tensor) or disarm (None) the backward role timeline."""
+    _check(load().fa_debug_set_trace(_ptr(buf), 0 if buf is None else buf.numel() * 8),
+           "fa_debug_set_trace")
 
 
 def fa_test_exp2(x, y, mode, stream=None):

@@ -302,6 +302,7 @@ extern "C" int fa_bwd(const void* q, const void* k, const void* v, const void* o
   p.scale = scale;
   p.err = di->err_word;
   p.timeout_ns = (unsigned long long)kn.timeout_ns;
+  p.trace = kn.trace;
   BwdAux aux;
   aux.o = static_cast<const __nv_bfloat16*>(o);
   aux.dout = static_cast<const __nv_bfloat16*>(dout);
@@ -377,6 +378,15 @@ extern "C" int fa_debug_set_events(int which, void* start, void* stop) {
   std::lock_guard<std::mutex> lk(g_mu);
   g_knobs.ev[which][0] = static_cast<cudaEvent_t>(start);
   g_knobs.ev[which][1] = static_cast<cudaEvent_t>(stop);
+  return FA_OK;
+}
+
+extern "C" int fa_debug_set_trace(void* trace_dev, size_t bytes) {
+  if (trace_dev && bytes < sizeof(long long) * TRACE_STEPS * TR_NUM)
+    return fail(FA_ERR_INVALID_ARG, "trace buffer needs %zu bytes",
+                sizeof(long long) * TRACE_STEPS * TR_NUM);
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_knobs.trace = static_cast<long long*>(trace_dev);
   return FA_OK;
 }
 

@@ -140,6 +140,13 @@ __device__ __forceinline__ void issue_dq(uint32_t tm, uint32_t kt, uint32_t dsb)
   }
 }
 
+// Role timeline for tuning (CTA 0 only, when a trace buffer is armed).
+#define FA_TRACE(ev, step)                                                        \
+  do {                                                                            \
+    if (p.trace != nullptr && blockIdx.x == 0 && (step) < (uint32_t)TRACE_STEPS) \
+      p.trace[(ev) * TRACE_STEPS + (step)] = clock64();                           \
+  } while (0)
+
 struct StepInfo {
   int h, m;
 };
@@ -319,6 +326,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_kernel(const __grid_consta
           const uint32_t sb = base + C::ST_OFF + s * C::STAGE_BYTES;
           ok = mbar_wait(BAR(C::B_PREADY + b), (it >> 1) & 1, wc, SITE_BWD_P_READY);
           if (!ok) break;
+          FA_TRACE(TR_MMA_P, it);
           if (i == 0 && u_it > 0) {
             ok = mbar_wait(BAR(C::B_ACCEMPTY), (u_it - 1) & 1, wc, SITE_BWD_ACC_FULL);
             if (!ok) break;
@@ -327,6 +335,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_kernel(const __grid_consta
           issue_acc<D>(tmem + C::TM_DV, tmem + C::TM_SB + 64 * b, sb + C::Q_TILE, i > 0);  // dV += P^T dO
           ok = mbar_wait(BAR(C::B_DSREADY + b), (it >> 1) & 1, wc, SITE_BWD_DS_READY);
           if (!ok) break;
+          FA_TRACE(TR_MMA_DS, it);
           tc_fence_after();
           issue_acc<D>(tmem + C::TM_DK, tmem + C::TM_DB + 64 * b, sb, i > 0);  // dK += dS^T Q
           issue_dq<D>(tmem + C::TM_SB + 64 * b, kt, base + C::DS_OFF + b * C::DS_BYTES);
@@ -338,12 +347,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_kernel(const __grid_consta
             ok = mbar_wait(BAR(C::B_QDFULL + st % NSTAGE), (st / NSTAGE) & 1, wc,
                            SITE_BWD_QD_FULL);
             if (!ok) break;
+            FA_TRACE(TR_MMA_QD2, it);
             tc_fence_after();
             const uint32_t sb2 = base + C::ST_OFF + (st % NSTAGE) * C::STAGE_BYTES;
             issue_kq<D>(tmem + C::TM_DB + 64 * b, vt, sb2 + C::Q_TILE);             // dP^T(i+2)
             tc_commit(BAR(C::B_DPFULL + b));
             ok = mbar_wait(BAR(C::B_DQEMPTY + b), (it >> 1) & 1, wc, SITE_BWD_DQ_EMPTY);
             if (!ok) break;
+            FA_TRACE(TR_MMA_DQE, it);
             tc_fence_after();
             issue_kq<D>(tmem + C::TM_SB + 64 * b, kt, sb2);                         // S^T(i+2)
             tc_commit(BAR(C::B_SFULL + b));
@@ -407,6 +418,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_kernel(const __grid_consta
         const uint32_t t_dp = tmem + lane_off + C::TM_DB + 64 * b;
         ok = mbar_wait(BAR(C::B_SFULL + b), (it >> 1) & 1, wc, SITE_BWD_S_FULL);
         if (!ok) break;
+        if (j == 0) FA_TRACE(TR_PDS_S, it);
         tc_fence_after();
         // The row arrays hold -LSE*log2(e) and -D, so both phases are packed
         // fp32 pairs: x = s*scale*log2e - LSE*log2e (one FFMA2 per pair) and
@@ -449,8 +461,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_kernel(const __grid_consta
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(BAR(C::B_PREADY + b));
+        if (j == 0) FA_TRACE(TR_PDS_P, it);
         ok = mbar_wait(BAR(C::B_DPFULL + b), (it >> 1) & 1, wc, SITE_BWD_DP_FULL);
         if (!ok) break;
+        if (j == 0) FA_TRACE(TR_PDS_DP, it);
         tc_fence_after();
         uint32_t pk[32];
         {
@@ -486,6 +500,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_kernel(const __grid_consta
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(BAR(C::B_DSREADY + b));
+        if (j == 0) FA_TRACE(TR_PDS_DS, it);
       }
       if (!ok) break;
       // unit epilogue: dV, dK rows of this key
@@ -537,6 +552,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_kernel(const __grid_consta
         const uint32_t b = it & 1;
         ok = mbar_wait(BAR(C::B_DQFULL + b), (it >> 1) & 1, wc, SITE_BWD_DQ_FULL);
         if (!ok) break;
+        if (dd == 0) FA_TRACE(TR_DRN_FULL, it);
         tc_fence_after();
         uint32_t a[64];
         tmem_ld64(tmem + lane_off + C::TM_SB + 64 * b, a);
@@ -554,6 +570,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_kernel(const __grid_consta
           for (int c = 0; c < BMQ; ++c)
             if (c < nvalid) atomicAdd(dst + c * rstride, u2f(a[c]));
         }
+        if (dd == 0) FA_TRACE(TR_DRN_DONE, it);
       }
     }
   }

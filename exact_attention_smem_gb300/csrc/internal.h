@@ -28,6 +28,15 @@ struct Knobs {
   long long timeout_ns = 2000000000LL;
   int grid_override = 0;         // >0: persistent grid size (schedule permutation tests)
   cudaEvent_t ev[2][2] = {{nullptr, nullptr}, {nullptr, nullptr}};  // [fwd|bwd][start|stop]
+  long long* trace = nullptr;    // device buffer for the backward role timeline
+};
+// Backward timeline: trace[event * TRACE_STEPS + step] = clock64 of CTA 0.
+constexpr int TRACE_STEPS = 512;
+enum TraceEvent : int {
+  TR_MMA_P = 0, TR_MMA_DS, TR_MMA_QD2, TR_MMA_DQE,     // MMA thread: after each wait
+  TR_PDS_S, TR_PDS_P, TR_PDS_DP, TR_PDS_DS,            // P/dS warps (thread 0)
+  TR_DRN_FULL, TR_DRN_DONE,                            // dQ drain (thread 128)
+  TR_NUM
 };
 Knobs knobs_snapshot();
 void take_events(int which, cudaEvent_t* start, cudaEvent_t* stop);  // one-shot timing events
@@ -61,6 +70,7 @@ struct BwdParams {
   int nseq, Hq, Hkv, Sq, Sk, total_q, total_k, causal;
   float scale_log2, scale;
   int hblock;                    // KV heads per scheduler group
+  long long* trace;              // optional role timeline of CTA 0 (nullptr = off)
   int* err;
   unsigned long long timeout_ns;
 };

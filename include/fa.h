@@ -152,6 +152,13 @@ FA_API int fa_debug_set(const char* key, double value);
 FA_API int fa_debug_set_events(int which /* 0 = forward, 1 = backward */, void* start,
                                void* stop);
 
+/*
+ * Tuning hook: while armed, each fa_bwd main kernel writes a role timeline of
+ * CTA 0 (clock64 after each cross-role wait, for its first 512 steps) into
+ * trace_dev (device buffer of at least 10*512 int64). NULL disarms.
+ */
+FA_API int fa_debug_set_trace(void* trace_dev, size_t bytes);
+
 /* ---- test hooks (exercise single device primitives; not the attention path) ---- */
 
 /* y[i] = 2^x[i] on the device: mode 0 software polynomial, mode 1 MUFU ex2. */
