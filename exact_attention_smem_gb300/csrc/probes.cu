@@ -202,7 +202,12 @@ __global__ void __launch_bounds__(256, 1) micro_exp_kernel(int iters, int poly, 
   }
 }
 
-__global__ void __launch_bounds__(128, 1) micro_mma_kernel(int iters, double* out, int* err) {
+// tcgen05 MMA throughput for one instruction shape: M=128, N in {64,128,256},
+// K=16, operands from shared memory (ts = 0) or A from TMEM (ts = 1).
+template <int N, int TS>
+__global__ void __launch_bounds__(128, 1) micro_mma_kernel(int iters, int style, double* out,
+                                                           int* err) {
+  constexpr int ts = TS;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -227,7 +232,98 @@ __global__ void __launch_bounds__(128, 1) micro_mma_kernel(int iters, double* ou
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  constexpr uint32_t idesc = idesc_bf16(128, 256, false, false);
+  constexpr uint32_t idesc = idesc_bf16(128, N, false, false);
+  // D in columns [0, N); the TMEM A operand (ts) in columns [256, 320).
+  // style 0: lane 0 alone runs the loop; style 1: the whole warp runs it and
+  // one elected lane issues; both with the descriptors computed up front.
+  uint64_t ad[4], bd[4];
+#pragma unroll
+  for (int kk = 0; kk < 4; ++kk) {
+    ad[kk] = sdesc_sw128(base + kk * 32, 16384, 1024);
+    bd[kk] = sdesc_sw128(base + 16384 + kk * 32, 32768, 1024);
+  }
+  long long t0 = 0, t1 = 0;
+  if (style == 0) {
+    if (threadIdx.x == 0) {
+      t0 = clock64();
+      for (int it = 0; it < iters; ++it) {
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          if constexpr (TS != 0)
+            mma_ts(tmem, tmem + 256 + kk * 8, bd[kk], idesc, 1u);
+          else
+            mma_ss(tmem, ad[kk], bd[kk], idesc, 1u);
+        }
+      }
+      tc_commit(bar);
+    }
+  } else if (warp == 0) {
+    t0 = clock64();
+    for (int it = 0; it < iters; ++it) {
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        if (elect_one()) {
+          if constexpr (TS != 0)
+            mma_ts(tmem, tmem + 256 + kk * 8, bd[kk], idesc, 1u);
+          else
+            mma_ss(tmem, ad[kk], bd[kk], idesc, 1u);
+        }
+        __syncwarp();
+      }
+    }
+    if (elect_one()) tc_commit(bar);
+    __syncwarp();
+  }
+  const WaitCtl wc{err, abort_flag, 2000000000ull};
+  mbar_wait(bar, 0, wc, SITE_TEST);
+  if (threadIdx.x == 0) {
+    t1 = clock64();
+    out[2 * blockIdx.x] = (double)(t1 - t0);
+    out[2 * blockIdx.x + 1] = (double)iters * 4.0 * 2.0 * 128 * N * 16;
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// Issue-cost probe: SS N=128 MMAs in groups of 4, with optional extras after
+// each group (mods bit 0: tcgen05 fence::after_thread_sync; bit 1: a commit to a
+// spare mbarrier; bit 2: a try_wait on an already completed mbarrier; bit 3: a
+// runtime accumulate flag on every MMA).
+__global__ void __launch_bounds__(128, 1) micro_issue_kernel(int iters, int mods, double* out,
+                                                             int* err) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (base - raw);
+  const uint32_t bar = base + 65536, spare = bar + 8, done = bar + 16;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + 65536 + 64);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 65536 + 72);
+  const int warp = threadIdx.x >> 5;
+  for (int i = threadIdx.x; i < 65536 / 16; i += 128)
+    reinterpret_cast<uint4*>(smem)[i] = make_uint4(0x3c003c00u, 0, 0x3c003c00u, 0);
+  if (threadIdx.x == 0) {
+    mbar_init(bar, 1);
+    mbar_init(spare, 1);
+    mbar_init(done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_arrive(done);   // phase 0 of `done` completes
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  constexpr uint32_t idesc = idesc_bf16(128, 128, false, false);
   long long t0 = 0, t1 = 0;
   if (threadIdx.x == 0) {
     t0 = clock64();
@@ -235,7 +331,11 @@ __global__ void __launch_bounds__(128, 1) micro_mma_kernel(int iters, double* ou
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk)
         mma_ss(tmem, sdesc_sw128(base + kk * 32, 16384, 1024),
-               sdesc_sw128(base + 16384 + kk * 32, 32768, 1024), idesc, 1u);
+               sdesc_sw128(base + 16384 + kk * 32, 16384, 1024), idesc,
+               (mods & 8) ? (uint32_t)(it > 0 || kk > 0) : 1u);
+      if (mods & 1) tc_fence_after();
+      if (mods & 2) tc_commit(spare);
+      if (mods & 4) mbar_try_wait(done, 0);
     }
     tc_commit(bar);
   }
@@ -244,7 +344,119 @@ __global__ void __launch_bounds__(128, 1) micro_mma_kernel(int iters, double* ou
   if (threadIdx.x == 0) {
     t1 = clock64();
     out[2 * blockIdx.x] = (double)(t1 - t0);
-    out[2 * blockIdx.x + 1] = (double)iters * 4.0 * 2.0 * 128 * 256 * 16;
+    out[2 * blockIdx.x + 1] = (double)iters * 4.0 * 2.0 * 128 * 128 * 16;
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// Issue-style probe with the descriptors computed next to each MMA from a
+// loop-varying stage offset (as the attention kernels do):
+//   style 0: lane 0 alone runs the loop; 1: the converged warp runs it and an
+//   elected lane issues; 2: lane 0, descriptors hoisted out of the loop.
+template <int STYLE, int X>
+__global__ void __launch_bounds__(128, 1) micro_style_kernel(int iters, double* out, int* err,
+                                                             int one) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (base - raw);
+  const uint32_t bar = base + 65536, spare = bar + 8, done = bar + 16;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + 65536 + 64);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 65536 + 72);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = threadIdx.x; i < 65536 / 16; i += 128)
+    reinterpret_cast<uint4*>(smem)[i] = make_uint4(0x3c003c00u, 0, 0x3c003c00u, 0);
+  if (threadIdx.x == 0) {
+    mbar_init(bar, 1);
+    mbar_init(spare, 1);
+    mbar_init(done, 1);
+    mbar_arrive(done);
+    *abort_flag = 0;
+    *reinterpret_cast<volatile int*>(smem + 65536 + 80) = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  constexpr uint32_t idesc = idesc_bf16(128, 128, false, false);
+  long long t0 = 0;
+  if (warp == 0 && (STYLE == 1 || lane == 0 || X == 7)) {
+    t0 = clock64();
+    uint64_t ah[4], bh[4];
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      ah[kk] = sdesc_sw128(base + kk * 32, 16384, 1024);
+      bh[kk] = sdesc_sw128(base + 16384 + kk * 32, 16384, 1024);
+    }
+    for (int it = 0; it < iters; ++it) {
+      const uint32_t stage = (it & 1) * 8192;   // loop-varying operand offset
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        const uint64_t a = STYLE == 2 ? ah[kk] : sdesc_sw128(base + stage + kk * 32, 16384, 1024);
+        const uint64_t b =
+            STYLE == 2 ? bh[kk] : sdesc_sw128(base + 16384 + stage + kk * 32, 16384, 1024);
+        // X = 1: accumulate flag is a runtime value (always 1 here)
+        const uint32_t acc = X == 1 ? (uint32_t)(one != 0) : 1u;
+        if (STYLE == 1) {
+          if (elect_one()) mma_ss(tmem, a, b, idesc, acc);
+          __syncwarp();
+        } else {
+          mma_ss(tmem, a, b, idesc, acc);
+        }
+      }
+      if (X == 2) tc_fence_after();
+      if (X == 3) tc_commit(spare);
+      if (X == 4) {
+        const WaitCtl w2{err, abort_flag, 2000000000ull};
+        mbar_wait(done, 0, w2, SITE_TEST);
+      }
+      if (X == 5) {   // bare try_wait on the completed phase
+        while (!mbar_try_wait(done, 0)) {
+        }
+      }
+      if (X == 6) {   // non-blocking test_wait on the completed phase
+        while (!mbar_test_wait(done, 0)) {
+        }
+      }
+      if (X == 7) {   // named-barrier handshake with warp 1
+        asm volatile("bar.sync 1, 64;" ::: "memory");
+      }
+      if (X == 8) {   // plain shared-memory flag read
+        while (*reinterpret_cast<volatile int*>(smem + 65536 + 80) != 0) {
+        }
+      }
+      if (X == 9) {   // global-memory read
+        while (*reinterpret_cast<volatile int*>(err) == 12345) {
+        }
+      }
+
+    }
+    if (STYLE == 1) {
+      if (elect_one()) tc_commit(bar);
+      __syncwarp();
+    } else {
+      tc_commit(bar);
+    }
+  }
+  if (X == 7 && warp == 1) {
+    for (int it = 0; it < iters; ++it) asm volatile("bar.sync 1, 64;" ::: "memory");
+  }
+  const WaitCtl wc{err, abort_flag, 2000000000ull};
+  mbar_wait(bar, 0, wc, SITE_TEST);
+  if (threadIdx.x == 0) {
+    out[2 * blockIdx.x] = (double)(clock64() - t0);
+    out[2 * blockIdx.x + 1] = (double)iters * 4.0 * 2.0 * 128 * 128 * 16;
   }
   tc_fence_before();
   __syncthreads();
@@ -255,16 +467,46 @@ __global__ void __launch_bounds__(128, 1) micro_mma_kernel(int iters, double* ou
 }
 
 cudaError_t launch_micro(int kind, int iters, double* out, int ctas, cudaStream_t st) {
+  if (kind >= 28 && kind <= 39) {
+    // 28-30: styles 0/1/2; 31-39: style 0 with extras X = 1..9 per group of 4
+    const int smem = 65536 + 128 + 1024;
+    void (*kern)(int, double*, int*, int) =
+        kind == 28 ? micro_style_kernel<0, 0> : kind == 29 ? micro_style_kernel<1, 0>
+        : kind == 30 ? micro_style_kernel<2, 0> : kind == 31 ? micro_style_kernel<0, 1>
+        : kind == 32 ? micro_style_kernel<0, 2> : kind == 33 ? micro_style_kernel<0, 3>
+        : kind == 34 ? micro_style_kernel<0, 4> : kind == 35 ? micro_style_kernel<0, 5>
+        : kind == 36 ? micro_style_kernel<0, 6> : kind == 37 ? micro_style_kernel<1, 7>
+        : kind == 38 ? micro_style_kernel<0, 8> : micro_style_kernel<0, 9>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    kern<<<ctas, 128, smem, st>>>(iters, out, device_error_word(), 1);
+    return cudaGetLastError();
+  }
+  if (kind >= 12 && kind <= 27) {
+    const int smem = 65536 + 128 + 1024;
+    cudaError_t e = cudaFuncSetAttribute(micro_issue_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    micro_issue_kernel<<<ctas, 128, smem, st>>>(iters, kind - 12, out, device_error_word());
+    return cudaGetLastError();
+  }
   if (kind == 0 || kind == 1) {
     micro_exp_kernel<<<ctas, 256, 0, st>>>(iters, kind, out, 0.37f);
     return cudaGetLastError();
   }
-  if (kind == 2) {
+  if (kind >= 2 && kind <= 11) {
+    // 2: N=256 SS, 3: N=128 SS, 4: N=64 SS, 5: N=128 A-in-TMEM, 6: N=64 A-in-TMEM;
+    // 7-11: the same shapes issued by an elected lane of a converged warp
+    const int style = kind >= 7 ? 1 : 0;
+    const int k5 = (kind - 2) % 5;
     const int smem = 65536 + 128 + 1024;
-    cudaError_t e =
-        cudaFuncSetAttribute(micro_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    void (*kern)(int, int, double*, int*) =
+        k5 == 0 ? micro_mma_kernel<256, 0> : k5 == 1 ? micro_mma_kernel<128, 0>
+        : k5 == 2 ? micro_mma_kernel<64, 0> : k5 == 3 ? micro_mma_kernel<128, 1>
+                                             : micro_mma_kernel<64, 1>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    micro_mma_kernel<<<ctas, 128, smem, st>>>(iters, out, device_error_word());
+    kern<<<ctas, 128, smem, st>>>(iters, style, out, device_error_word());
     return cudaGetLastError();
   }
   return cudaErrorInvalidValue;

@@ -56,6 +56,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking probe of a phase (no suspend hint): true if it has completed.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Shared state of the bounded waits of one CTA.
 struct WaitCtl {
   int* err;              // device error word (first failure wins)
@@ -279,6 +292,34 @@ __device__ __forceinline__ void tmem_st_wait() {
 
 #undef FA_R8
 #undef FA_S8
+
+// Named-barrier rendezvous of `count` threads (whole warps) that also ANDs a
+// predicate across them. Unlike any memory access, it does not wait behind the
+// tcgen05 instructions an MMA-issuing warp has queued, so the MMA warp learns
+// that a dependency is satisfied (and whether a wait timed out) for free.
+__device__ __forceinline__ bool bar_and(uint32_t id, uint32_t count, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "barrier.cta.red.and.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
+}
+
+// One lane of the (converged) warp is elected; returns true on that lane.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b32 r;\n\t"
+      "elect.sync r|p, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
 
 // Register reallocation between warpgroups (executed by all warps of a warpgroup).
 template <int N>

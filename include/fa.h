@@ -168,8 +168,22 @@ FA_API int fa_test_exp2(const float* x, float* y, int n, int mode, void* stream)
  * Microbenchmarks, one CTA per SM (`ctas` CTAs): each CTA writes two doubles to
  * out_dev[2*cta + {0, 1}]: its clock64 span and the operations it performed.
  *   kind 0: MUFU ex2 throughput, kind 1: software exp2 throughput (operations =
- *   exponentials, 256 threads per CTA); kind 2: tcgen05 bf16 MMA throughput
- *   (M128 N256 K16 from shared memory; operations = FLOPs). iters <= 2^24.
+ *   exponentials, 256 threads per CTA); kinds 2-6: tcgen05 bf16 MMA throughput
+ *   for M128 K16 and N = 256, 128, 64 with both operands in shared memory
+ *   (kinds 2, 3, 4) or N = 128, 64 with A in TMEM (kinds 5, 6), issued by one
+ *   thread; kinds 7-11: the same five shapes issued by an elected lane of a
+ *   converged warp; kinds 12-27: SS N=128 MMAs in groups of 4 with extras
+ *   after each group selected by the bits of (kind - 12): 1 tcgen05 fence, 2 a
+ *   commit, 4 an mbarrier poll, 8 a runtime accumulate flag; kinds 28-30: SS
+ *   N=128 MMAs with descriptors built next to each MMA from a loop-varying
+ *   offset, issued by lane 0 (28) or an elected lane of the converged warp
+ *   (29), or with hoisted descriptors (30); kinds 31-34: kind 28 plus, per group
+ *   of 4 MMAs, a runtime accumulate flag (31), a tcgen05 fence (32), a commit
+ *   (33), a bounded mbarrier wait on a completed phase (34), a bare try_wait
+ *   loop (35) or a test_wait loop (36) on it, a named-barrier handshake with a
+ *   second warp (37, warp-wide issue), a shared-memory flag read (38) or a
+ *   global-memory read (39); operations =
+ *   FLOPs. iters <= 2^24.
  */
 FA_API int fa_micro(int kind, int iters, double* out_dev, int ctas, void* stream);
 

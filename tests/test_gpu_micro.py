@@ -31,9 +31,21 @@ def test_microbenchmarks():
     mufu, sms = _rate(0, 20000)
     poly, _ = _rate(1, 20000)
     mma, _ = _rate(2, 2000)
+    shapes = {name: _rate(kind, 2000)[0] for kind, name in
+              ((3, "ss_n128"), (4, "ss_n64"), (5, "ts_n128"), (6, "ts_n64"),
+               (7, "elect_ss_n256"), (8, "elect_ss_n128"), (9, "elect_ss_n64"),
+               (10, "elect_ts_n128"), (11, "elect_ts_n64"))}
+    issue = {f"mods{m}": _rate(12 + m, 2000)[0] for m in (0, 1, 2, 4, 8, 15)}
+    issue.update({name: _rate(kind, 2000)[0] for kind, name in
+                  ((28, "lane0_inloop_desc"), (29, "elect_inloop_desc"), (30, "lane0_hoisted_desc"),
+                   (31, "lane0_runtime_acc"), (32, "lane0_fence"), (33, "lane0_commit"),
+                   (34, "lane0_mbar_wait"), (35, "lane0_bare_try_wait"),
+                   (36, "lane0_test_wait"), (37, "elect_named_barrier"),
+                   (38, "lane0_smem_flag"), (39, "lane0_global_read"))})
     assert fa.fa_get_device_error(clear=True) == 0
-    res = {"sms": sms, "mufu_ex2_per_clk_per_sm": mufu, "poly_exp2_per_clk_per_sm": poly,
-           "mma_bf16_flop_per_clk_per_sm": mma}
+    res = {"issue_ss_n128_by_extras": issue,"sms": sms, "mufu_ex2_per_clk_per_sm": mufu, "poly_exp2_per_clk_per_sm": poly,
+           "mma_bf16_flop_per_clk_per_sm": mma,
+           "mma_flop_per_clk_per_sm_by_shape": dict(ss_n256=mma, **shapes)}
     print(json.dumps(res))
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
     if os.path.isdir(os.path.join(root, "gpurun_out")):
