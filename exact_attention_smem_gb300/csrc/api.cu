@@ -403,7 +403,7 @@ extern "C" int fa_test_exp2(const float* x, float* y, int n, int mode, void* str
 extern "C" float fa_exp2_poly_host(float x) { return fa::exp2_poly(x); }
 
 extern "C" int fa_micro(int kind, int iters, double* out_dev, int ctas, void* stream) {
-  if (kind < 0 || kind > 39 || iters <= 0 || iters > (1 << 24) || !out_dev || ctas <= 0 ||
+  if (kind < 0 || kind > 51 || iters <= 0 || iters > (1 << 24) || !out_dev || ctas <= 0 ||
       ctas > 4096)
     return fail(FA_ERR_INVALID_ARG, "fa_micro arguments");
   DevInfo* di = nullptr;

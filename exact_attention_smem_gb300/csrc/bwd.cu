@@ -26,10 +26,9 @@
 // Warps: 0-3 P/dS (one thread per key row = TMEM lane), 4-7 dQ drain (one
 // thread per head-dim row of dQ^T), 8 MMA issue + TMEM allocation, 9 TMA.
 // TMEM columns: dV [0,d) dK [d,2d); S buffers [2d,2d+128) (two of 64 columns:
-// S^T of a step, then its P^T in bf16, then its dQ^T once dV has read P^T);
-// dP buffers [2d+128,2d+256) (dP^T, then dS^T in bf16). Steps alternate
-// buffers, so the MMAs of step i+2 are issued as soon as step i's buffers are
-// free while the P/dS warps work on step i+1.
+// S^T of a step, then its P^T in bf16); dP buffers [2d+128,2d+256) (dP^T, then
+// dS^T in bf16, then the step's dQ^T once dK has read dS^T). Steps alternate
+// buffers, so S^T runs two steps ahead of the P/dS warps and dP^T one.
 #include "exp2_poly.cuh"
 #include "internal.h"
 #include "ptx.cuh"
@@ -49,10 +48,10 @@ constexpr int MMA_WARP = 8;
 constexpr int TMA_WARP = 9;
 // Register split (launch: 168 per thread = 65536 / 384 rounded down to 8):
 // 128 * (REGS_PDS + REGS_DRAIN + REGS_CONTROL) <= 384 * 168.
-constexpr int REGS_PDS = 224;
-constexpr int REGS_DRAIN = 128;
+constexpr int REGS_PDS = 232;
+constexpr int REGS_DRAIN = 120;
 constexpr int REGS_CONTROL = 152;
-constexpr int NSTAGE = 3;
+constexpr int NSTAGE = 4;
 constexpr int MAX_SEQ_SMEM = 1024;
 
 template <int D>
@@ -71,7 +70,7 @@ struct Cfg {
   static constexpr int V_OFF = KV_TILE;
   static constexpr int ST_OFF = 2 * KV_TILE;
   static constexpr int DS_OFF = ST_OFF + NSTAGE * STAGE_BYTES;
-  static constexpr int BAR_OFF = DS_OFF + 2 * DS_BYTES;
+  static constexpr int BAR_OFF = DS_OFF + DS_BYTES;   // one dS^T staging buffer
   static constexpr int B_KVFULL = 0, B_KVEMPTY = 1, B_QDFULL = 2, B_QDEMPTY = 2 + NSTAGE,
                        B_SFULL = 2 + 2 * NSTAGE,  // [2]
                        B_DPFULL = B_SFULL + 2,    // [2]
@@ -83,14 +82,14 @@ struct Cfg {
                        B_DSREADY = B_PREADY + 2,  // [2]
                        B_DQFULL = B_DSREADY + 2,  // [2]
                        B_DQEMPTY = B_DQFULL + 2,  // [2]
-                       B_DSBEMPTY = B_DQEMPTY + 2,  // [2]
-                       B_ACCFULL = B_DSBEMPTY + 2, B_ACCEMPTY = B_ACCFULL + 1,
+                       B_DSBEMPTY = B_DQEMPTY + 2,  // staging buffer free (once per step)
+                       B_ACCFULL = B_DSBEMPTY + 1, B_ACCEMPTY = B_ACCFULL + 1,
                        B_DRAIN = B_ACCEMPTY + 1, NBAR = B_DRAIN + 1;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int CU_OFF = MISC_OFF + 16;
   static constexpr int SMEM_BYTES = CU_OFF + (MAX_SEQ_SMEM + 1) * 4 + 1024;
-  // dV, dK accumulators; two S^T buffers (also P^T, then dQ^T) and two dP^T
-  // buffers (also dS^T), so step i+1's S^T/dP^T MMAs run during step i's math.
+  // dV, dK accumulators; two S^T buffers (also P^T) and two dP^T buffers (also
+  // dS^T, then dQ^T), so later steps' S^T/dP^T MMAs run during step i's math.
   static constexpr uint32_t TM_DV = 0, TM_DK = D, TM_SB = 2 * D, TM_DB = 2 * D + 128;
   static constexpr uint32_t IDESC_SDP = idesc_bf16(128, 64, false, false);  // S^T, dP^T
   static constexpr uint32_t IDESC_ACC = idesc_bf16(128, D, false, true);    // dV, dK (A in TMEM)
@@ -193,10 +192,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_kernel(const __grid_consta
       mbar_init(BAR(C::B_DPFULL + b), 1);
       mbar_init(BAR(C::B_DQFULL + b), 1);
       mbar_init(BAR(C::B_DQEMPTY + b), 128);
-      mbar_init(BAR(C::B_DSBEMPTY + b), 1);
       mbar_init(BAR(C::B_PREADY + b), 128);
       mbar_init(BAR(C::B_DSREADY + b), 128);
     }
+    mbar_init(BAR(C::B_DSBEMPTY), 1);
     mbar_init(BAR(C::B_ACCFULL), 1);
     mbar_init(BAR(C::B_ACCEMPTY), 128);
     mbar_init(BAR(C::B_DRAIN), 1);
@@ -301,65 +300,76 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_kernel(const __grid_consta
         if (!w.seek(snake_index(k, G, cta), u)) break;
         if (u.cost == 0) continue;
         const int n = u.cost * group;
-        ok = mbar_wait(BAR(C::B_KVFULL), u_it & 1, wc, SITE_BWD_KV_FULL);
-        if (!ok) break;
-        tc_fence_after();
-        // prologue: S^T and dP^T of the unit's first two steps
+        // Two sync points per step, each probing all it needs at once:
+        //   A(i): P(i) ready, Q(i+2) loaded, dQ^T(i-1) drained
+        //         -> dV(i), S^T(i+2) (into the S buffer dV(i) has just read),
+        //            dP^T(i+1) (into the dP buffer the drain has just emptied)
+        //   B(i): dS(i) ready -> dK(i), dQ^T(i) (into the dP buffer of step i,
+        //         after dK(i) has read its dS^T)
+        // S^T runs two steps ahead of the P/dS warps and dP^T one. The unit
+        // prologue issues S^T(0), S^T(1) and dP^T(0).
         for (int j = 0; j < 2 && j < n && ok; ++j) {
           const uint32_t st = it + j, b = st & 1;
-          ok = mbar_wait(BAR(C::B_QDFULL + st % NSTAGE), (st / NSTAGE) & 1, wc, SITE_BWD_QD_FULL);
+          const bool dqe = j == 0 && st >= 2;            // dP buffer b last held dQ^T(st-2)
+          ok = mbar_wait3(BAR(C::B_KVFULL), u_it & 1, SITE_BWD_KV_FULL,
+                          BAR(C::B_QDFULL + st % NSTAGE), (st / NSTAGE) & 1, SITE_BWD_QD_FULL,
+                          dqe ? BAR(C::B_DQEMPTY + b) : BAR(C::B_KVFULL),
+                          dqe ? ((st >> 1) - 1) & 1 : u_it & 1, SITE_BWD_DQ_EMPTY, wc);
           if (!ok) break;
-          if (st >= 2) {   // the buffer's last dQ^T must have been drained
-            ok = mbar_wait(BAR(C::B_DQEMPTY + b), ((st >> 1) - 1) & 1, wc, SITE_BWD_DQ_EMPTY);
-            if (!ok) break;
-          }
           tc_fence_after();
-          const uint32_t sb = base + C::ST_OFF + (st % NSTAGE) * C::STAGE_BYTES;
-          issue_kq<D>(tmem + C::TM_SB + 64 * b, kt, sb);
+          const uint32_t sbj = base + C::ST_OFF + (st % NSTAGE) * C::STAGE_BYTES;
+          issue_kq<D>(tmem + C::TM_SB + 64 * b, kt, sbj);
           tc_commit(BAR(C::B_SFULL + b));
-          issue_kq<D>(tmem + C::TM_DB + 64 * b, vt, sb + C::Q_TILE);
-          tc_commit(BAR(C::B_DPFULL + b));
+          if (j == 0) {
+            issue_kq<D>(tmem + C::TM_DB + 64 * b, vt, sbj + C::Q_TILE);
+            tc_commit(BAR(C::B_DPFULL + b));
+          }
         }
         for (int i = 0; i < n && ok; ++i, ++it) {
-          const uint32_t b = it & 1;
+          const uint32_t b = it & 1, b1 = b ^ 1;
           const int s = it % NSTAGE;
           const uint32_t sb = base + C::ST_OFF + s * C::STAGE_BYTES;
-          ok = mbar_wait(BAR(C::B_PREADY + b), (it >> 1) & 1, wc, SITE_BWD_P_READY);
-          if (!ok) break;
-          FA_TRACE(TR_MMA_P, it);
-          if (i == 0 && u_it > 0) {
-            ok = mbar_wait(BAR(C::B_ACCEMPTY), (u_it - 1) & 1, wc, SITE_BWD_ACC_FULL);
+          const bool more = i + 1 < n, more2 = i + 2 < n;
+          const uint32_t st1 = it + 1, st2 = it + 2;
+          const uint32_t sb1 = base + C::ST_OFF + (st1 % NSTAGE) * C::STAGE_BYTES;
+          const uint32_t sb2 = base + C::ST_OFF + (st2 % NSTAGE) * C::STAGE_BYTES;
+          // ---- sync point A(i)
+          {
+            const uint32_t bq = more2 ? BAR(C::B_QDFULL + st2 % NSTAGE) : BAR(C::B_PREADY + b);
+            const uint32_t pq = more2 ? (st2 / NSTAGE) & 1 : (it >> 1) & 1;
+            const bool dqe = more && st1 >= 2;           // dP buffer b1 last held dQ^T(it-1)
+            const uint32_t bd = dqe ? BAR(C::B_DQEMPTY + b1) : BAR(C::B_PREADY + b);
+            const uint32_t pd = dqe ? ((st1 >> 1) - 1) & 1 : (it >> 1) & 1;
+            ok = mbar_wait3(BAR(C::B_PREADY + b), (it >> 1) & 1, SITE_BWD_P_READY, bq, pq,
+                            SITE_BWD_QD_FULL, bd, pd, SITE_BWD_DQ_EMPTY, wc);
             if (!ok) break;
+            FA_TRACE(TR_MMA_P, it);
+            if (i == 0 && u_it > 0) {
+              ok = mbar_wait(BAR(C::B_ACCEMPTY), (u_it - 1) & 1, wc, SITE_BWD_ACC_FULL);
+              if (!ok) break;
+            }
+            tc_fence_after();
+            issue_acc<D>(tmem + C::TM_DV, tmem + C::TM_SB + 64 * b, sb + C::Q_TILE, i > 0);
+            if (more2) {
+              issue_kq<D>(tmem + C::TM_SB + 64 * b, kt, sb2);                         // S^T(i+2)
+              tc_commit(BAR(C::B_SFULL + b));
+            }
+            if (more) {
+              issue_kq<D>(tmem + C::TM_DB + 64 * b1, vt, sb1 + C::Q_TILE);            // dP^T(i+1)
+              tc_commit(BAR(C::B_DPFULL + b1));
+            }
           }
-          tc_fence_after();
-          issue_acc<D>(tmem + C::TM_DV, tmem + C::TM_SB + 64 * b, sb + C::Q_TILE, i > 0);  // dV += P^T dO
+          // ---- sync point B(i)
           ok = mbar_wait(BAR(C::B_DSREADY + b), (it >> 1) & 1, wc, SITE_BWD_DS_READY);
           if (!ok) break;
           FA_TRACE(TR_MMA_DS, it);
           tc_fence_after();
-          issue_acc<D>(tmem + C::TM_DK, tmem + C::TM_DB + 64 * b, sb, i > 0);  // dK += dS^T Q
-          issue_dq<D>(tmem + C::TM_SB + 64 * b, kt, base + C::DS_OFF + b * C::DS_BYTES);
+          issue_acc<D>(tmem + C::TM_DK, tmem + C::TM_DB + 64 * b, sb, i > 0);       // dK += dS^T Q
+          issue_dq<D>(tmem + C::TM_DB + 64 * b, kt, base + C::DS_OFF);
           tc_commit(BAR(C::B_DQFULL + b));
-          tc_commit(BAR(C::B_DSBEMPTY + b));
+          tc_commit(BAR(C::B_DSBEMPTY));
           tc_commit(BAR(C::B_QDEMPTY + s));
-          if (i + 2 < n) {
-            const uint32_t st = it + 2;
-            ok = mbar_wait(BAR(C::B_QDFULL + st % NSTAGE), (st / NSTAGE) & 1, wc,
-                           SITE_BWD_QD_FULL);
-            if (!ok) break;
-            FA_TRACE(TR_MMA_QD2, it);
-            tc_fence_after();
-            const uint32_t sb2 = base + C::ST_OFF + (st % NSTAGE) * C::STAGE_BYTES;
-            issue_kq<D>(tmem + C::TM_DB + 64 * b, vt, sb2 + C::Q_TILE);             // dP^T(i+2)
-            tc_commit(BAR(C::B_DPFULL + b));
-            ok = mbar_wait(BAR(C::B_DQEMPTY + b), (it >> 1) & 1, wc, SITE_BWD_DQ_EMPTY);
-            if (!ok) break;
-            FA_TRACE(TR_MMA_DQE, it);
-            tc_fence_after();
-            issue_kq<D>(tmem + C::TM_SB + 64 * b, kt, sb2);                         // S^T(i+2)
-            tc_commit(BAR(C::B_SFULL + b));
-          }
-          if (i + 1 == n) {
+          if (!more) {
             tc_commit(BAR(C::B_ACCFULL));
             tc_commit(BAR(C::B_KVEMPTY));
           }
@@ -416,17 +426,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_kernel(const __grid_consta
         const uint32_t b = it & 1;
         const uint32_t t_s = tmem + lane_off + C::TM_SB + 64 * b;
         const uint32_t t_dp = tmem + lane_off + C::TM_DB + 64 * b;
-        ok = mbar_wait(BAR(C::B_SFULL + b), (it >> 1) & 1, wc, SITE_BWD_S_FULL);
+        // S^T(i) and dP^T(i) are both issued well ahead: load them in one TMEM
+        // round trip (dP^T is ready no later than S^T in the MMA order).
+        ok = mbar_wait3(BAR(C::B_SFULL + b), (it >> 1) & 1, SITE_BWD_S_FULL,
+                        BAR(C::B_DPFULL + b), (it >> 1) & 1, SITE_BWD_DP_FULL,
+                        BAR(C::B_SFULL + b), (it >> 1) & 1, SITE_BWD_S_FULL, wc);
         if (!ok) break;
         if (j == 0) FA_TRACE(TR_PDS_S, it);
         tc_fence_after();
+        uint32_t sa[64], dpa[64];
+        tmem_ld64x2(t_s, sa, t_dp, dpa);
         // The row arrays hold -LSE*log2(e) and -D, so both phases are packed
         // fp32 pairs: x = s*scale*log2e - LSE*log2e (one FFMA2 per pair) and
         // dS = P * (dP - D) (one FADD2 + one FMUL2 per pair).
         uint64_t p2[BMQ / 2];
         {
-          uint32_t a[64];
-          tmem_ld64(t_s, a);
           // columns c with q0 + c < qmin are masked; a key past the sequence masks all
           const int cmin = key_ok ? qmin - st.m * BMQ : BMQ;
           const uint64_t sl2x2 = f2pack(sl2, sl2);
@@ -435,9 +449,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_kernel(const __grid_consta
           for (int c = 0; c < BMQ; c += 4) {
             const float4 l4 = *reinterpret_cast<const float4*>(nlse_s + c);
             float x[4];
-            f2unpack(ffma2(f2pack(u2f(a[c]), u2f(a[c + 1])), sl2x2, f2pack(l4.x, l4.y)), x[0], x[1]);
-            f2unpack(ffma2(f2pack(u2f(a[c + 2]), u2f(a[c + 3])), sl2x2, f2pack(l4.z, l4.w)), x[2],
-                     x[3]);
+            f2unpack(ffma2(f2pack(u2f(sa[c]), u2f(sa[c + 1])), sl2x2, f2pack(l4.x, l4.y)), x[0],
+                     x[1]);
+            f2unpack(ffma2(f2pack(u2f(sa[c + 2]), u2f(sa[c + 3])), sl2x2, f2pack(l4.z, l4.w)),
+                     x[2], x[3]);
             float pe[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -462,35 +477,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_kernel(const __grid_consta
         tc_fence_before();
         mbar_arrive(BAR(C::B_PREADY + b));
         if (j == 0) FA_TRACE(TR_PDS_P, it);
-        ok = mbar_wait(BAR(C::B_DPFULL + b), (it >> 1) & 1, wc, SITE_BWD_DP_FULL);
-        if (!ok) break;
-        if (j == 0) FA_TRACE(TR_PDS_DP, it);
-        tc_fence_after();
         uint32_t pk[32];
-        {
-          uint32_t a[64];
-          tmem_ld64(t_dp, a);
 #pragma unroll
-          for (int c = 0; c < BMQ; c += 4) {
-            const float4 d4 = *reinterpret_cast<const float4*>(nd_s + c);
-            float d0, d1, d2, d3;
-            f2unpack(fmul2(p2[c / 2], fadd2(f2pack(u2f(a[c]), u2f(a[c + 1])), f2pack(d4.x, d4.y))),
-                     d0, d1);
-            f2unpack(fmul2(p2[c / 2 + 1],
-                           fadd2(f2pack(u2f(a[c + 2]), u2f(a[c + 3])), f2pack(d4.z, d4.w))),
-                     d2, d3);
-            pk[c / 2] = pack_bf16x2(d0, d1);
-            pk[c / 2 + 1] = pack_bf16x2(d2, d3);
-          }
+        for (int c = 0; c < BMQ; c += 4) {
+          const float4 d4 = *reinterpret_cast<const float4*>(nd_s + c);
+          float d0, d1, d2, d3;
+          f2unpack(fmul2(p2[c / 2], fadd2(f2pack(u2f(dpa[c]), u2f(dpa[c + 1])), f2pack(d4.x, d4.y))),
+                   d0, d1);
+          f2unpack(fmul2(p2[c / 2 + 1],
+                         fadd2(f2pack(u2f(dpa[c + 2]), u2f(dpa[c + 3])), f2pack(d4.z, d4.w))),
+                   d2, d3);
+          pk[c / 2] = pack_bf16x2(d0, d1);
+          pk[c / 2 + 1] = pack_bf16x2(d2, d3);
         }
-        if (it >= 2) {
-          ok = mbar_wait(BAR(C::B_DSBEMPTY + b), ((it >> 1) - 1) & 1, wc, SITE_BWD_DS_READY);
+        if (j == 0) FA_TRACE(TR_PDS_DP, it);
+        if (it >= 1) {   // the staging buffer still feeds dQ^T(it-1) until that completes
+          ok = mbar_wait(BAR(C::B_DSBEMPTY), (it - 1) & 1, wc, SITE_BWD_DS_READY);
           if (!ok) break;
         }
         tmem_st32(t_dp, pk);
         {
           // dS^T row j -> shared memory, [128 keys][64 q] with the 128-byte swizzle
-          uint8_t* row = dsb_base + b * C::DS_BYTES + j * 128;
+          uint8_t* row = dsb_base + j * 128;
 #pragma unroll
           for (int c = 0; c < 8; ++c)
             *reinterpret_cast<uint4*>(row + ((c ^ (j & 7)) << 4)) =
@@ -555,7 +563,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_kernel(const __grid_consta
         if (dd == 0) FA_TRACE(TR_DRN_FULL, it);
         tc_fence_after();
         uint32_t a[64];
-        tmem_ld64(tmem + lane_off + C::TM_SB + 64 * b, a);
+        tmem_ld64(tmem + lane_off + C::TM_DB + 64 * b, a);
         tc_fence_before();
         mbar_arrive(BAR(C::B_DQEMPTY + b));
         const int q0 = st.m * BMQ;

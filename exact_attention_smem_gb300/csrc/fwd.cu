@@ -243,32 +243,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) fwd_kernel(const __grid_consta
         ++kv_it;
         if (n == 1) tc_commit(BAR(C::B_QEMPTY));
         for (int j = 0; j < n; ++j) {
+          // sync point 1: V_j, P_0(j) and (if any) K_{j+1}, probed together
           const int sv = kv_it % C::NSTAGE;
-          ok = mbar_wait(BAR(C::B_KVFULL + sv), (kv_it / C::NSTAGE) & 1, wc, SITE_FWD_KV_FULL);
+          const bool more = j + 1 < n;
+          const int sk2 = (kv_it + 1) % C::NSTAGE;
+          ok = mbar_wait3(BAR(C::B_KVFULL + sv), (kv_it / C::NSTAGE) & 1, SITE_FWD_KV_FULL,
+                          BAR(C::B_PFULL + 0), sp_it & 1, SITE_FWD_P_FULL,
+                          more ? BAR(C::B_KVFULL + sk2) : BAR(C::B_KVFULL + sv),
+                          more ? ((kv_it + 1) / C::NSTAGE) & 1 : (kv_it / C::NSTAGE) & 1,
+                          SITE_FWD_KV_FULL, wc);
           if (!ok) break;
           ++kv_it;
-          ok = mbar_wait(BAR(C::B_PFULL + 0), sp_it & 1, wc, SITE_FWD_P_FULL);
-          if (!ok) break;
           tc_fence_after();
           issue_pv<D>(tO0, tS0, kvb + sv * C::TILE_BYTES, j > 0);
-          int sk2 = 0;
-          if (j + 1 < n) {
-            sk2 = kv_it % C::NSTAGE;
-            ok = mbar_wait(BAR(C::B_KVFULL + sk2), (kv_it / C::NSTAGE) & 1, wc,
-                           SITE_FWD_KV_FULL);
-            if (!ok) break;
-            tc_fence_after();
+          if (more) {
             issue_s<D>(tS0, q0, kvb + sk2 * C::TILE_BYTES);
             tc_commit(BAR(C::B_SFULL + 0));
           } else {
             tc_commit(BAR(C::B_OFULL + 0));
           }
+          // sync point 2: P_1(j)
           ok = mbar_wait(BAR(C::B_PFULL + 1), sp_it & 1, wc, SITE_FWD_P_FULL);
           if (!ok) break;
           tc_fence_after();
           issue_pv<D>(tO1, tS1, kvb + sv * C::TILE_BYTES, j > 0);
           tc_commit(BAR(C::B_KVEMPTY + sv));
-          if (j + 1 < n) {
+          if (more) {
             issue_s<D>(tS1, q1, kvb + sk2 * C::TILE_BYTES);
             tc_commit(BAR(C::B_SFULL + 1));
             tc_commit(BAR(C::B_KVEMPTY + sk2));

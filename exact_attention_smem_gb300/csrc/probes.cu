@@ -466,7 +466,107 @@ __global__ void __launch_bounds__(128, 1) micro_style_kernel(int iters, double* 
   }
 }
 
+// Load latency seen by another warp while warp 0 streams MMAs (or not):
+// OP 0 tcgen05.ld x32 (+wait), 1 ld.shared.v4, 2 mbarrier.test_wait; the probe
+// warp is warp 4 (same SM sub-partition as warp 0) or warp 5 (another one).
+template <int OP, int SAME, int MMA>
+__global__ void __launch_bounds__(256, 1) micro_lat_kernel(int iters, double* out, int* err) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (base - raw);
+  const uint32_t bar = base + 65536, done = bar + 8;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + 65536 + 64);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 65536 + 72);
+  volatile int* stop = reinterpret_cast<volatile int*>(smem + 65536 + 76);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = threadIdx.x; i < 65536 / 16; i += 256)
+    reinterpret_cast<uint4*>(smem)[i] = make_uint4(0x3c003c00u, 0, 0x3c003c00u, 0);
+  if (threadIdx.x == 0) {
+    mbar_init(bar, 1);
+    mbar_init(done, 1);
+    mbar_arrive(done);
+    *abort_flag = 0;
+    *stop = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  constexpr uint32_t idesc = idesc_bf16(128, 256, false, false);
+  const int probe_warp = SAME ? 4 : 5;
+  if (warp == 0 && lane == 0 && MMA) {
+    // stream MMAs (D in columns [0,256)) for a fixed number of groups
+    for (int it = 0; it < iters * 4; ++it) {
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+        mma_ss(tmem, sdesc_sw128(base + kk * 32, 16384, 1024),
+               sdesc_sw128(base + 16384 + kk * 32, 32768, 1024), idesc, 1u);
+    }
+    tc_commit(bar);
+  }
+  if (warp == probe_warp) {
+    // probes on TMEM columns [256, 288) of this warp's lane quarter
+    const uint32_t taddr = tmem + ((uint32_t)((warp & 3) * 32) << 16) + 256;
+    uint32_t acc = 0;
+    const long long t0 = clock64();
+    for (int it = 0; it < iters; ++it) {
+      if (OP == 0) {
+        uint32_t r[32];
+        tmem_ld32(taddr, r);
+        acc += r[lane & 31];
+      } else if (OP == 1) {
+        uint32_t v;
+        asm volatile("ld.volatile.shared.u32 %0, [%1];"
+                     : "=r"(v)
+                     : "r"(base + 40960 + ((it * 16 + lane * 16) & 8191))
+                     : "memory");
+        acc += v;
+      } else {
+        acc += mbar_test_wait(done, 0) ? 1u : 0u;
+      }
+    }
+    const long long t1 = clock64();
+    if (lane == 0) {
+      out[2 * blockIdx.x] = (double)(t1 - t0);
+      out[2 * blockIdx.x + 1] = (double)iters;   // "ops" = probes; rate = probes per clock
+    }
+    if (acc == 0xdeadbeef) out[0] = 0;
+  }
+  if (MMA) {
+    const WaitCtl wc{err, abort_flag, 4000000000ull};
+    mbar_wait(bar, 0, wc, SITE_TEST);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
 cudaError_t launch_micro(int kind, int iters, double* out, int ctas, cudaStream_t st) {
+  if (kind >= 40 && kind <= 51) {
+    const int k = kind - 40, op = k / 4, same = (k >> 1) & 1, mma = k & 1;
+    void (*kern)(int, double*, int*) =
+        op == 0 ? (same ? (mma ? micro_lat_kernel<0, 1, 1> : micro_lat_kernel<0, 1, 0>)
+                        : (mma ? micro_lat_kernel<0, 0, 1> : micro_lat_kernel<0, 0, 0>))
+      : op == 1 ? (same ? (mma ? micro_lat_kernel<1, 1, 1> : micro_lat_kernel<1, 1, 0>)
+                        : (mma ? micro_lat_kernel<1, 0, 1> : micro_lat_kernel<1, 0, 0>))
+                : (same ? (mma ? micro_lat_kernel<2, 1, 1> : micro_lat_kernel<2, 1, 0>)
+                        : (mma ? micro_lat_kernel<2, 0, 1> : micro_lat_kernel<2, 0, 0>));
+    const int smem = 65536 + 128 + 1024;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    kern<<<ctas, 256, smem, st>>>(iters, out, device_error_word());
+    return cudaGetLastError();
+  }
   if (kind >= 28 && kind <= 39) {
     // 28-30: styles 0/1/2; 31-39: style 0 with extras X = 1..9 per group of 4
     const int smem = 65536 + 128 + 1024;

@@ -92,12 +92,42 @@ __device__ __forceinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, co
   }
 }
 
+// Probe three phases at once: the non-blocking test_waits are issued back to
+// back in one block, so their latencies overlap. (Pass a barrier twice to probe
+// fewer.) True when all three have completed.
+__device__ __forceinline__ bool mbar_test3(uint32_t b0, uint32_t p0, uint32_t b1, uint32_t p1,
+                                           uint32_t b2, uint32_t p2) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred q0, q1, q2;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 q0, [%1], %2;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 q1, [%3], %4;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 q2, [%5], %6;\n\t"
+      "and.pred q0, q0, q1;\n\t"
+      "and.pred q0, q0, q2;\n\t"
+      "selp.u32 %0, 1, 0, q0;\n\t}"
+      : "=r"(ok)
+      : "r"(b0), "r"(p0), "r"(b1), "r"(p1), "r"(b2), "r"(p2)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait for the phase with the given parity to complete. Returns false when the
 // CTA is aborting (timeout here or elsewhere).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtl& w,
                                           int site) {
   if (mbar_try_wait(bar, parity)) return true;
   return mbar_wait_slow(bar, parity, w, site);
+}
+
+// Wait for three phases (one probe round trip when all are already complete,
+// which matters to a thread that issues tcgen05 MMAs: each of its memory
+// accesses waits behind the MMAs it has queued).
+__device__ __forceinline__ bool mbar_wait3(uint32_t b0, uint32_t p0, int s0, uint32_t b1,
+                                           uint32_t p1, int s1, uint32_t b2, uint32_t p2, int s2,
+                                           const WaitCtl& w) {
+  if (mbar_test3(b0, p0, b1, p1, b2, p2)) return true;
+  return mbar_wait(b0, p0, w, s0) && mbar_wait(b1, p1, w, s1) && mbar_wait(b2, p2, w, s2);
 }
 
 // ---------------------------------------------------------------------- TMA
@@ -208,6 +238,8 @@ __device__ __forceinline__ uint32_t tmem_addr(uint32_t base, uint32_t lane, uint
 
 #define FA_R8(i) "=r"(r[i]), "=r"(r[i + 1]), "=r"(r[i + 2]), "=r"(r[i + 3]), "=r"(r[i + 4]), \
                  "=r"(r[i + 5]), "=r"(r[i + 6]), "=r"(r[i + 7])
+#define FA_Q8(i) "=r"(q[i]), "=r"(q[i + 1]), "=r"(q[i + 2]), "=r"(q[i + 3]), "=r"(q[i + 4]), \
+                 "=r"(q[i + 5]), "=r"(q[i + 6]), "=r"(q[i + 7])
 #define FA_S8(i) "r"(r[i]), "r"(r[i + 1]), "r"(r[i + 2]), "r"(r[i + 3]), "r"(r[i + 4]), \
                  "r"(r[i + 5]), "r"(r[i + 6]), "r"(r[i + 7])
 
@@ -269,6 +301,27 @@ __device__ __forceinline__ void tmem_st64(uint32_t taddr, const uint32_t* r) {
       : "memory");
 }
 
+// Two 64-column loads (e.g. two different buffers) behind one wait.
+__device__ __forceinline__ void tmem_ld64x2(uint32_t ta, uint32_t (&r)[64], uint32_t tb,
+                                            uint32_t (&q)[64]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+      "%28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, "
+      "%45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, "
+      "%62, %63}, [%128];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%64, %65, %66, %67, %68, %69, %70, %71, %72, "
+      "%73, %74, %75, %76, %77, %78, %79, %80, %81, %82, %83, %84, %85, %86, %87, %88, %89, "
+      "%90, %91, %92, %93, %94, %95, %96, %97, %98, %99, %100, %101, %102, %103, %104, %105, "
+      "%106, %107, %108, %109, %110, %111, %112, %113, %114, %115, %116, %117, %118, %119, "
+      "%120, %121, %122, %123, %124, %125, %126, %127}, [%129];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : FA_R8(0), FA_R8(8), FA_R8(16), FA_R8(24), FA_R8(32), FA_R8(40), FA_R8(48), FA_R8(56),
+        FA_Q8(0), FA_Q8(8), FA_Q8(16), FA_Q8(24), FA_Q8(32), FA_Q8(40), FA_Q8(48), FA_Q8(56)
+      : "r"(ta), "r"(tb)
+      : "memory");
+}
+
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
@@ -291,6 +344,7 @@ __device__ __forceinline__ void tmem_st_wait() {
 }
 
 #undef FA_R8
+#undef FA_Q8
 #undef FA_S8
 
 // Named-barrier rendezvous of `count` threads (whole warps) that also ANDs a

@@ -182,7 +182,11 @@ FA_API int fa_test_exp2(const float* x, float* y, int n, int mode, void* stream)
  *   (33), a bounded mbarrier wait on a completed phase (34), a bare try_wait
  *   loop (35) or a test_wait loop (36) on it, a named-barrier handshake with a
  *   second warp (37, warp-wide issue), a shared-memory flag read (38) or a
- *   global-memory read (39); operations =
+ *   global-memory read (39); kinds 40-51: latency of probes made by another warp
+ *   while warp 0 streams MMAs or not: (kind-40)/4 selects the probe (0 TMEM
+ *   load, 1 shared load, 2 mbarrier test_wait), bit 1 whether the probing warp
+ *   shares warp 0's SM sub-partition, bit 0 whether MMAs run; operations =
+ *   probes; operations =
  *   FLOPs. iters <= 2^24.
  */
 FA_API int fa_micro(int kind, int iters, double* out_dev, int ctas, void* stream);

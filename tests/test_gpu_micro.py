@@ -42,8 +42,14 @@ def test_microbenchmarks():
                    (34, "lane0_mbar_wait"), (35, "lane0_bare_try_wait"),
                    (36, "lane0_test_wait"), (37, "elect_named_barrier"),
                    (38, "lane0_smem_flag"), (39, "lane0_global_read"))})
+    lat = {}
+    for op, oname in ((0, "tmem_ld"), (1, "smem_ld"), (2, "mbar_test")):
+        for same in (0, 1):
+            for busy in (0, 1):
+                r, _ = _rate(40 + op * 4 + same * 2 + busy, 2000)
+                lat[f"{oname}_{'same' if same else 'other'}_sub_{'mma' if busy else 'idle'}"] = 1.0 / r
     assert fa.fa_get_device_error(clear=True) == 0
-    res = {"issue_ss_n128_by_extras": issue,"sms": sms, "mufu_ex2_per_clk_per_sm": mufu, "poly_exp2_per_clk_per_sm": poly,
+    res = {"probe_latency_clk": lat, "issue_ss_n128_by_extras": issue,"sms": sms, "mufu_ex2_per_clk_per_sm": mufu, "poly_exp2_per_clk_per_sm": poly,
            "mma_bf16_flop_per_clk_per_sm": mma,
            "mma_flop_per_clk_per_sm_by_shape": dict(ss_n256=mma, **shapes)}
     print(json.dumps(res))
