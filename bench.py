@@ -113,6 +113,24 @@ def job_tflops(flops_per_step: float, steps: int, world: int, ms: float) -> floa
     return flops_per_step * steps * world / (ms * 1e-3) / 1e12
 
 
+def profiled_traffic(kernel_file: str, profile: str):
+    """DRAM bytes per launch recorded by an ncu capture, if the kernel source
+    still matches the one profiled (else None)."""
+    import hashlib
+    try:
+        text = open(os.path.join(ROOT, "profiles", profile)).read()
+        src = open(os.path.join(ROOT, "exact_attention_smem_gb300", "csrc", kernel_file), "rb").read()
+    except OSError:
+        return None
+    tb = [l for l in text.splitlines() if l.startswith("traffic_bytes_per_launch:")]
+    sh = [l for l in text.splitlines() if l.startswith("source_sha256_16:")]
+    if not tb or not sh:
+        return None
+    if hashlib.sha256(src).hexdigest()[:16] != sh[0].split(":")[1].split()[0]:
+        return None
+    return int(tb[0].split(":")[1])
+
+
 def flops(w, lengths=None):
     from attn_inputs import flops_forward
     f = flops_forward(w, lengths)
@@ -202,8 +220,11 @@ def run_ours(args):
         "frac_of_peak": round(value / ws / peak_s, 4),
         "roofline": {"bound": "tensor", "kernel": "bwd main (tcgen05)", "achieved": round(bwd_tf, 1),
                      "peak": peak_s, "unit": "TFLOP/s", "frac": round(bwd_tf / peak_s, 4),
-                     "peak_kind": f"{kind} sustained bf16", "traffic": None,
-                     "fwd": {"achieved": round(fwd_tf, 1), "frac": round(fwd_tf / peak_s, 4)}},
+                     "peak_kind": f"{kind} sustained bf16",
+                     "traffic": profiled_traffic("bwd.cu", "bwd_kernel_long_s32768_causal.md"),
+                     "fwd": {"achieved": round(fwd_tf, 1), "frac": round(fwd_tf / peak_s, 4),
+                             "traffic": profiled_traffic("fwd.cu",
+                                                         "fwd_kernel_long_s32768_causal.md")}},
         "e2e": e2e,
         "gpu_launches": 5 * args.steps,
         "clocks": clk.summary(),
