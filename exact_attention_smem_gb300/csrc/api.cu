@@ -264,14 +264,18 @@ extern "C" int fa_bwd(const void* q, const void* k, const void* v, const void* o
   if ((st = device_info(&di)) != FA_OK) return st;
   const Knobs kn = knobs_snapshot();
 
+  const int mode = kn.bwd_mode;
+  if (mode == 0 && d != 128)
+    return fail(FA_ERR_UNSUPPORTED, "the one-pass backward supports head dim 128 only");
   BwdParams p;
   memset(&p, 0, sizeof(p));
   const long long Tq = sh.Tq > 0 ? sh.Tq : 1, Tk = sh.Tk > 0 ? sh.Tk : 1;
+  const int qbox = mode == 0 ? 64 : 128;
   if ((st = encode_rows(&p.tm_q, sh.Tq > 0 ? q : k, sh.Tq > 0 ? Tq : Tk, sh.Tq > 0 ? Hq : Hkv,
-                        d, 64)) != FA_OK)
+                        d, qbox)) != FA_OK)
     return st;
   if ((st = encode_rows(&p.tm_do, sh.Tq > 0 ? dout : k, sh.Tq > 0 ? Tq : Tk,
-                        sh.Tq > 0 ? Hq : Hkv, d, 64)) != FA_OK)
+                        sh.Tq > 0 ? Hq : Hkv, d, qbox)) != FA_OK)
     return st;
   if ((st = encode_rows(&p.tm_k, sh.Tk > 0 ? k : q, sh.Tk > 0 ? Tk : Tq, sh.Tk > 0 ? Hkv : Hq,
                         d)) != FA_OK)
@@ -283,7 +287,8 @@ extern "C" int fa_bwd(const void* q, const void* k, const void* v, const void* o
   char* ws = static_cast<char*>(workspace);
   const size_t T = (size_t)sh.Tq;
   const size_t P = (size_t)pad_hstride((long long)T, B);
-  p.dq_acc = reinterpret_cast<float*>(ws);
+  p.dq_acc = mode == 0 ? reinterpret_cast<float*>(ws) : nullptr;
+  p.dq = static_cast<__nv_bfloat16*>(dq);
   p.lse2 = reinterpret_cast<float*>(ws + up(T * Hq * d * sizeof(float)));
   p.delta = reinterpret_cast<float*>(ws + up(T * Hq * d * sizeof(float)) + up(P * Hq * sizeof(float)));
   p.pad_hstride = (long long)P;
@@ -314,9 +319,20 @@ extern "C" int fa_bwd(const void* q, const void* k, const void* v, const void* o
   const long long kv_units_per_head =
       sh.packed ? (sh.Tk + 127) / 128 + B : (long long)B * ((Sk + 127) / 128);
   p.hblock = pick_hblock(kv_units_per_head, Hkv, grid);
-  cudaError_t e = launch_bwd(p, aux, d, grid, static_cast<cudaStream_t>(stream), kn.bwd_poly8);
+  // dQ units (128 query rows of one head) walk K/V like the forward: one LPT group.
+  const long long q_units_per_head =
+      sh.packed ? (sh.Tq + 127) / 128 + B : (long long)B * ((Sq + 127) / 128);
+  p.hblock_q = Hq;
+  int grid_q = kn.grid_override > 0 ? kn.grid_override : di->sms;
+  if (mode != 0) {
+    const long long kv_units = kv_units_per_head * Hkv, q_units = q_units_per_head * Hq;
+    if (kv_units < grid) grid = (int)(kv_units > 0 ? kv_units : 1);
+    if (q_units < grid_q) grid_q = (int)(q_units > 0 ? q_units : 1);
+  }
+  cudaError_t e = launch_bwd(p, aux, d, grid, grid_q, static_cast<cudaStream_t>(stream),
+                             kn.bwd_poly8, mode);
   if (e == cudaErrorNotSupported)
-    return fail(FA_ERR_UNSUPPORTED, "backward supports head dim 128 only");
+    return fail(FA_ERR_UNSUPPORTED, "backward head dim %d unsupported", d);
   if (e != cudaSuccess) return fail(FA_ERR_CUDA, "backward launch: %s", cudaGetErrorString(e));
   return FA_OK;
 }
@@ -361,6 +377,9 @@ extern "C" int fa_debug_set(const char* key, double value) {
     const int v = (int)value;
     if (v != 0 && v != 2 && v != 4) return fail(FA_ERR_INVALID_ARG, "poly8 in {0, 2, 4}");
     (key[0] == 'p' ? g_knobs.poly8 : g_knobs.bwd_poly8) = v;
+  } else if (!strcmp(key, "bwd_mode")) {
+    if (value != 0.0 && value != 1.0) return fail(FA_ERR_INVALID_ARG, "bwd_mode in {0, 1}");
+    g_knobs.bwd_mode = (int)value;
   } else if (!strcmp(key, "timeout_ms")) {
     if (!(value >= 1.0 && value <= 60000.0)) return fail(FA_ERR_INVALID_ARG, "timeout_ms");
     g_knobs.timeout_ns = (long long)(value * 1e6);

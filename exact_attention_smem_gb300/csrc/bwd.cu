@@ -593,8 +593,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_kernel(const __grid_consta
 #undef BAR
 }
 
-// -D and -LSE*log2e into the padded row arrays; zero the dQ accumulator.
-// One warp per (row, head).
+// -D and -LSE*log2e into the padded row arrays; zero the dQ accumulator when
+// there is one (one-pass kernel). One warp per (row, head).
 template <int D>
 __global__ void bwd_pre_kernel(BwdParams p, BwdAux aux) {
   const long long nrows = (long long)p.total_q * p.Hq;
@@ -632,9 +632,11 @@ __global__ void bwd_pre_kernel(BwdParams p, BwdAux aux) {
       }
     }
     for (int sh = 16; sh > 0; sh >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, sh);
-    float* zr = p.dq_acc + ((long long)t * p.Hq + h) * D;
-    for (int c = lane * 4; c < D; c += 128)
-      *reinterpret_cast<float4*>(zr + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (p.dq_acc) {
+      float* zr = p.dq_acc + ((long long)t * p.Hq + h) * D;
+      for (int c = lane * 4; c < D; c += 128)
+        *reinterpret_cast<float4*>(zr + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     if (lane == 0) {
       const int row = t - q_start;
       const float lse = aux.lse[(p.cu ? 0ll : (long long)seq * aux.lse_seqstride) +
@@ -646,9 +648,10 @@ __global__ void bwd_pre_kernel(BwdParams p, BwdAux aux) {
   }
 }
 
-// Padding rows [q_len, round_up(q_len, 64)) of every sequence: LSE = +inf, D = 0.
+// Padding rows [q_len, round_up(q_len, 128)) of every sequence: LSE = +inf,
+// D = 0, so the padded query rows of a block contribute exact zeros.
 __global__ void bwd_pad_kernel(BwdParams p) {
-  const int seq = blockIdx.x, h = blockIdx.y, r = threadIdx.x;   // 64 threads
+  const int seq = blockIdx.x, h = blockIdx.y, r = threadIdx.x;   // 128 threads
   int q_start, q_len;
   if (p.cu) {
     q_start = p.cu[seq];
@@ -657,7 +660,7 @@ __global__ void bwd_pad_kernel(BwdParams p) {
     q_start = seq * p.Sq;
     q_len = p.Sq;
   }
-  const int row = ((q_len + 63) & ~63) - 64 + r;
+  const int row = ((q_len + 127) & ~127) - 128 + r;
   if (row >= q_len && row >= 0) {
     const long long pi = (long long)h * p.pad_hstride + pad_start(seq, q_start) + row;
     const_cast<float*>(p.lse2)[pi] = -INFINITY;
@@ -692,19 +695,32 @@ static cudaError_t launch_main(const BwdParams& p, int grid, cudaStream_t stream
   return cudaGetLastError();
 }
 
-cudaError_t launch_bwd(const BwdParams& p, const BwdAux& aux, int d, int grid,
-                       cudaStream_t stream, int poly8) {
-  if (d != 128) return cudaErrorNotSupported;
+cudaError_t launch_bwd(const BwdParams& p, const BwdAux& aux, int d, int grid, int grid_q,
+                       cudaStream_t stream, int poly8, int mode) {
+  if (mode == 0 && d != 128) return cudaErrorNotSupported;
+  if (d != 64 && d != 128) return cudaErrorNotSupported;
   const long long rows = (long long)p.total_q * p.Hq;
   if (rows > 0) {
     const int blocks = (int)((rows + 7) / 8 < 65535 * 8 ? (rows + 7) / 8 : 65535 * 8);
-    bwdk::bwd_pre_kernel<128><<<blocks, 256, 0, stream>>>(p, aux);
+    if (d == 128)
+      bwdk::bwd_pre_kernel<128><<<blocks, 256, 0, stream>>>(p, aux);
+    else
+      bwdk::bwd_pre_kernel<64><<<blocks, 256, 0, stream>>>(p, aux);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if (p.nseq > 0) {
-      bwdk::bwd_pad_kernel<<<dim3(p.nseq, p.Hq), 64, 0, stream>>>(p);
+      bwdk::bwd_pad_kernel<<<dim3(p.nseq, p.Hq), 128, 0, stream>>>(p);
       if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
+  }
+  if (mode != 0) {
+    cudaEvent_t ev0, ev1;
+    take_events(1, &ev0, &ev1);
+    if (ev0) cudaEventRecord(ev0, stream);
+    const cudaError_t e = launch_bwd_split(p, d, p.total_k > 0 ? grid : 0,
+                                           p.total_q > 0 ? grid_q : 0, stream, poly8);
+    if (ev1) cudaEventRecord(ev1, stream);
+    return e;
   }
   if (p.total_k > 0) {
     cudaEvent_t ev0, ev1;

@@ -1,0 +1,864 @@
+// Backward attention for sm_103a in two passes, with every accumulator in
+// tensor memory and no atomics:
+//
+//   dK/dV pass: one persistent CTA per SM walks (sequence, 128-key block, KV
+//     head) units longest-first; for each query head of the KV group and each
+//     block of 128 query rows that sees the keys:
+//        S^T  = K Q^T            P^T  = exp2(S^T * scale*log2e - LSE*log2e)
+//        dP^T = V dO^T           dS^T = P^T o (dP^T - D)
+//        dV  += P^T dO           dK  += dS^T Q
+//     dK and dV stay in TMEM for the whole unit and are written once.
+//   dQ pass: one persistent CTA per SM walks (sequence, 128-query block, query
+//     head) units longest-first; for each 128-key block the rows see:
+//        S  = Q K^T              P  = exp2(S * scale*log2e - LSE*log2e)
+//        dP = dO V^T             dS = P o (dP - D)
+//        dQ += dS K
+//     and writes dQ once, scaled, in bf16.
+//
+// The pages' backward ("FlashAttention-4: Algorithm and Kernel Pipelining
+// Co-Design for Asymmetric Hardware Scaling", abstract item (3) and the
+// Summary) keeps accumulators and the P/dS operands in tensor memory to cut
+// shared-memory traffic and atomic adds, with dQ accumulated by atomics into an
+// fp32 buffer. This form recomputes S and dP once more (seven 128x128xd MMAs
+// per block pair instead of five) and in exchange: every MMA is a full-rate
+// M=128, N=128 shape; P^T/dS^T (and dS) live only in TMEM as the A operand of
+// the accumulating MMA, so shared memory carries nothing but TMA tiles; dQ
+// needs no fp32 buffer, no atomics and no convert pass; and the result is
+// deterministic.
+//
+// Both kernels: 12 warps. Warps 0-3 and 4-7 are two compute warpgroups that
+// split the 128 columns of each score tile (64 each, one thread per TMEM lane =
+// tile row); warp 8 allocates TMEM and one of its threads issues the MMAs; warp
+// 9 is the TMA producer; warps 10-11 only complete the register split.
+// A warpgroup writes its bf16 half of P^T/dS^T/dS over the first 32 of its own
+// 64 fp32 columns, so the A operand of the accumulating MMA sits in columns
+// [0,32) and [64,96) of its buffer.
+#include "exp2_poly.cuh"
+#include "internal.h"
+#include "ptx.cuh"
+#include "sched.cuh"
+
+#include <cmath>
+
+namespace fa {
+using namespace ptx;
+
+namespace bsplit {
+
+constexpr int BN = 128;            // keys per block
+constexpr int BM = 128;            // query rows per block
+constexpr int NUM_THREADS = 384;
+constexpr int MMA_WARP = 8;
+constexpr int TMA_WARP = 9;
+// Launch gives 168 registers per thread (65536 / 384 rounded down to 8);
+// 128 * (2 * REGS_COMPUTE + REGS_CONTROL) <= 384 * 168.
+constexpr int REGS_COMPUTE = 200;
+constexpr int REGS_CONTROL = 104;
+constexpr int SMEM_LIMIT = 232448;
+constexpr int MAX_SEQ_SMEM = 200;  // packed boundaries kept in shared memory up to this
+
+template <int D>
+struct Tile {
+  static constexpr int CHUNKS = D / 64;        // 128-byte column chunks per row
+  static constexpr int CHUNK = 128 * 128;      // 128 rows x 128 bytes, 128B swizzle
+  static constexpr int BYTES = CHUNKS * CHUNK; // one 128-row tile
+};
+
+// dK/dV pass layout. Q slots are held from S^T(i) to dK(i), the longest span,
+// so Q gets three slots and dO two.
+template <int D>
+struct CfgKV {
+  using T = Tile<D>;
+  static constexpr int NQ = 3, NDO = 2;
+  static constexpr int K_OFF = 0, V_OFF = T::BYTES, Q_OFF = 2 * T::BYTES,
+                       DO_OFF = Q_OFF + NQ * T::BYTES, BAR_OFF = DO_OFF + NDO * T::BYTES;
+  static constexpr int B_KVFULL = 0, B_KVEMPTY = 1, B_QFULL = 2, B_QEMPTY = B_QFULL + NQ,
+                       B_DOFULL = B_QEMPTY + NQ, B_DOEMPTY = B_DOFULL + NDO,
+                       B_SFULL = B_DOEMPTY + NDO, B_DPFULL = B_SFULL + 1,
+                       B_PREADY = B_DPFULL + 1, B_DSREADY = B_PREADY + 1,
+                       B_ACCFULL = B_DSREADY + 1, B_DRAIN = B_ACCFULL + 1, NBAR = B_DRAIN + 1;
+  static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
+  static constexpr int CU_OFF = MISC_OFF + 16;
+  static constexpr int SMEM_BYTES = CU_OFF + (MAX_SEQ_SMEM + 1) * 4 + 1024;
+  static_assert(SMEM_BYTES <= SMEM_LIMIT, "dK/dV pass shared memory");
+  // TMEM: dV [0,D), dK [D,2D), S^T/P^T [2D,2D+128), dP^T/dS^T [2D+128,2D+256)
+  static constexpr uint32_t TM_DV = 0, TM_DK = D, TM_SB = 2 * D, TM_DB = 2 * D + 128;
+  static_assert(2 * D + 256 <= 512, "TMEM columns");
+  static constexpr uint32_t IDESC_S = idesc_bf16(128, 128, false, false);  // S^T, dP^T
+  static constexpr uint32_t IDESC_ACC = idesc_bf16(128, D, false, true);   // dV, dK
+};
+
+// dQ pass layout: Q and dO of the unit, and a ring of K/V tiles in the order
+// K_0 V_0 K_1 V_1 ...; K_j is held from S(j) to dQ(j), two steps, so the ring
+// has five slots.
+template <int D>
+struct CfgQ {
+  using T = Tile<D>;
+  static constexpr int NKV = 5;
+  static constexpr int Q_OFF = 0, DO_OFF = T::BYTES, KV_OFF = 2 * T::BYTES,
+                       BAR_OFF = KV_OFF + NKV * T::BYTES;
+  static constexpr int B_QFULL = 0, B_QEMPTY = 1, B_KVFULL = 2, B_KVEMPTY = B_KVFULL + NKV,
+                       B_SFULL = B_KVEMPTY + NKV,   // [2]
+                       B_DPFULL = B_SFULL + 2, B_DSREADY = B_DPFULL + 1,
+                       B_DQFULL = B_DSREADY + 1, B_DRAIN = B_DQFULL + 1, NBAR = B_DRAIN + 1;
+  static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
+  static constexpr int CU_OFF = MISC_OFF + 16;
+  static constexpr int SMEM_BYTES = CU_OFF + (MAX_SEQ_SMEM + 1) * 4 + 1024;
+  static_assert(SMEM_BYTES <= SMEM_LIMIT, "dQ pass shared memory");
+  // TMEM: S/dS buffers [0,128) and [128,256), dP [256,384), dQ [384,384+D)
+  static constexpr uint32_t TM_S = 0, TM_DP = 256, TM_DQ = 384;
+  static constexpr uint32_t IDESC_S = idesc_bf16(128, 128, false, false);  // S, dP
+  static constexpr uint32_t IDESC_DQ = idesc_bf16(128, D, false, true);    // dQ
+};
+
+__device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
+
+// Wait that ignores the abort flag: lets in-flight async work land before an
+// aborting CTA exits.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > limit_ns) return;
+  }
+}
+
+// X (TMEM, 128 x 128 fp32) = A (128 rows x D) * B (128 rows x D)^T, both K-major tiles.
+template <int D, uint32_t IDESC>
+__device__ __forceinline__ void mma_abt(uint32_t tm, uint32_t a, uint32_t b) {
+  using T = Tile<D>;
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t off = (kk >> 2) * T::CHUNK + (kk & 3) * 32;
+    mma_ss(tm, sdesc_sw128(a + off, T::CHUNK, 1024), sdesc_sw128(b + off, T::CHUNK, 1024), IDESC,
+           kk > 0 ? 1u : 0u);
+  }
+}
+
+// Acc (TMEM, 128 x D) (+)= X (TMEM, 128 x 128 bf16 in columns [0,32) and [64,96))
+//                          * Y (128 rows x D tile, MN-major B)
+template <int D, uint32_t IDESC>
+__device__ __forceinline__ void mma_acc(uint32_t tm_acc, uint32_t tm_x, uint32_t y, bool acc) {
+  using T = Tile<D>;
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) {
+    const uint32_t ta = tm_x + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8);
+    mma_ts(tm_acc, ta, sdesc_sw128(y + kk * 2048, T::CHUNK, 1024), IDESC,
+           (acc || kk > 0) ? 1u : 0u);
+  }
+}
+
+__device__ __forceinline__ uint32_t pack2(uint64_t v) {
+  float lo, hi;
+  f2unpack(v, lo, hi);
+  return pack_bf16x2(lo, hi);
+}
+
+// 64 fp32 values -> 32 bf16 pairs, stored over the first 32 of the 64 columns.
+__device__ __forceinline__ void store_bf16_half(uint32_t taddr, const uint64_t (&v2)[32]) {
+  uint32_t pk[32];
+#pragma unroll
+  for (int c = 0; c < 32; ++c) pk[c] = pack2(v2[c]);
+  tmem_st32(taddr, pk);
+}
+
+struct StepInfo {
+  int h, m;
+};
+
+__device__ __forceinline__ StepInfo step_of(int i, int cost, int m_first, int g, int group) {
+  StepInfo s;
+  const int hh = i / cost;
+  s.h = g * group + hh;
+  s.m = m_first + (i - hh * cost);
+  return s;
+}
+
+__device__ __forceinline__ int first_qblock(const Unit& u, int causal) {
+  if (!causal) return 0;
+  int r0 = u.m * BN - (u.k_len - u.q_len);
+  r0 = r0 > 0 ? r0 : 0;
+  return r0 / BM;
+}
+
+// Writes one warpgroup's half (D/2 columns) of a TMEM accumulator row to a bf16 row.
+template <int D>
+__device__ __forceinline__ void store_acc_half(uint32_t t_acc, __nv_bfloat16* dst, float mul,
+                                               bool ok) {
+#pragma unroll 1
+  for (int c = 0; c < D / 2; c += 32) {
+    uint32_t a[32];
+    tmem_ld32(t_acc + c, a);
+    uint32_t q[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) q[e] = pack_bf16x2(u2f(a[2 * e]) * mul, u2f(a[2 * e + 1]) * mul);
+    if (ok) {
+      uint4* o4 = reinterpret_cast<uint4*>(dst + c);
+      o4[0] = make_uint4(q[0], q[1], q[2], q[3]);
+      o4[1] = make_uint4(q[4], q[5], q[6], q[7]);
+      o4[2] = make_uint4(q[8], q[9], q[10], q[11]);
+      o4[3] = make_uint4(q[12], q[13], q[14], q[15]);
+    }
+  }
+}
+
+template <int D>
+__device__ __forceinline__ void zero_half(__nv_bfloat16* dst) {
+#pragma unroll
+  for (int c = 0; c < D / 2; c += 8) *reinterpret_cast<uint4*>(dst + c) = make_uint4(0, 0, 0, 0);
+}
+
+// ============================================================== dK/dV pass
+template <int D, int POLY8>
+__global__ void __launch_bounds__(NUM_THREADS, 1) dkdv_kernel(const __grid_constant__ BwdParams p) {
+  using C = CfgKV<D>;
+  using T = Tile<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (base - raw);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t bars = base + C::BAR_OFF;
+#define BAR(i) (bars + 8u * (uint32_t)(i))
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::MISC_OFF);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
+  int* cu_s = reinterpret_cast<int*>(smem + C::CU_OFF);
+
+  if (threadIdx.x == 0) {
+    mbar_init(BAR(C::B_KVFULL), 1);
+    mbar_init(BAR(C::B_KVEMPTY), 1);
+    for (int s = 0; s < C::NQ; ++s) {
+      mbar_init(BAR(C::B_QFULL + s), 1);
+      mbar_init(BAR(C::B_QEMPTY + s), 1);
+    }
+    for (int s = 0; s < C::NDO; ++s) {
+      mbar_init(BAR(C::B_DOFULL + s), 1);
+      mbar_init(BAR(C::B_DOEMPTY + s), 1);
+    }
+    mbar_init(BAR(C::B_SFULL), 1);
+    mbar_init(BAR(C::B_DPFULL), 1);
+    mbar_init(BAR(C::B_PREADY), 256);
+    mbar_init(BAR(C::B_DSREADY), 256);
+    mbar_init(BAR(C::B_ACCFULL), 1);
+    mbar_init(BAR(C::B_DRAIN), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == TMA_WARP && lane == 0) {
+    tma_prefetch_desc(&p.tm_q);
+    tma_prefetch_desc(&p.tm_do);
+    tma_prefetch_desc(&p.tm_k);
+    tma_prefetch_desc(&p.tm_v);
+  }
+  if (warp == MMA_WARP) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  const bool cu_in_smem = p.cu != nullptr && p.nseq <= MAX_SEQ_SMEM;
+  if (cu_in_smem)
+    for (int i = threadIdx.x; i <= p.nseq; i += NUM_THREADS) cu_s[i] = p.cu[i];
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  const SchedSpec spec{cu_in_smem ? cu_s : p.cu, p.nseq, p.Sq, p.Sk, p.Hkv, p.causal, BN, BM, 1,
+                       p.hblock};
+  const WaitCtl wc{p.err, abort_flag, p.timeout_ns};
+  const int G = gridDim.x;
+  const int cta = blockIdx.x;
+  const int group = p.Hq / p.Hkv;
+
+  if (warp >= 8) {
+    regs_dec<REGS_CONTROL>();
+  if (warp >= 10) {
+    // spare warps of the control warpgroup
+  } else if (warp == TMA_WARP) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      Walker w;
+      w.init(spec);
+      int u_it = 0;
+      bool ok = true;
+      uint32_t nq = 0, nd = 0;                            // Q / dO loads issued
+      for (int k = 0; ok; ++k) {
+        Unit u;
+        if (!w.seek(snake_index(k, G, cta), u)) break;
+        if (u.cost == 0) continue;
+        const int n = u.cost * group;
+        const int m_first = first_qblock(u, p.causal);
+        // The first two steps' Q/dO need only free ring slots: they go out
+        // before the wait for the previous unit to release K/V.
+        const int lead = n < 2 ? n : 2;
+        for (int i = 0; i <= n; ++i) {
+          if (i == lead) {
+            if (u_it > 0) {
+              ok = mbar_wait(BAR(C::B_KVEMPTY), (u_it - 1) & 1, wc, SITE_DKDV_KV_EMPTY);
+              if (!ok) break;
+            }
+            mbar_arrive_expect_tx(BAR(C::B_KVFULL), 2 * T::BYTES);
+            const int krow = u.k_start + u.m * BN;
+            for (int c = 0; c < T::CHUNKS; ++c) {
+              tma_load_3d(base + C::K_OFF + c * T::CHUNK, &p.tm_k, BAR(C::B_KVFULL), c * 64,
+                          u.head, krow);
+              tma_load_3d(base + C::V_OFF + c * T::CHUNK, &p.tm_v, BAR(C::B_KVFULL), c * 64,
+                          u.head, krow);
+            }
+            ++u_it;
+          }
+          if (i == n) break;
+          // Q(s) goes into slot s % NQ once dK(s - NQ) is done, dO(s) into slot
+          // s % NDO once dV(s - NDO) is done.
+          const StepInfo st = step_of(i, u.cost, m_first, u.head, group);
+          const int row = u.q_start + st.m * BM;
+          const int sq = nq % C::NQ, sd = nd % C::NDO;
+          if (nq >= (uint32_t)C::NQ) {
+            ok = mbar_wait(BAR(C::B_QEMPTY + sq), ((nq / C::NQ) - 1) & 1, wc, SITE_DKDV_Q_EMPTY);
+            if (!ok) break;
+          }
+          mbar_arrive_expect_tx(BAR(C::B_QFULL + sq), T::BYTES);
+          for (int c = 0; c < T::CHUNKS; ++c)
+            tma_load_3d(base + C::Q_OFF + sq * T::BYTES + c * T::CHUNK, &p.tm_q,
+                        BAR(C::B_QFULL + sq), c * 64, st.h, row);
+          ++nq;
+          if (nd >= (uint32_t)C::NDO) {
+            ok = mbar_wait(BAR(C::B_DOEMPTY + sd), ((nd / C::NDO) - 1) & 1, wc,
+                           SITE_DKDV_DO_EMPTY);
+            if (!ok) break;
+          }
+          mbar_arrive_expect_tx(BAR(C::B_DOFULL + sd), T::BYTES);
+          for (int c = 0; c < T::CHUNKS; ++c)
+            tma_load_3d(base + C::DO_OFF + sd * T::BYTES + c * T::CHUNK, &p.tm_do,
+                        BAR(C::B_DOFULL + sd), c * 64, st.h, row);
+          ++nd;
+        }
+      }
+      if (!ok) {
+        // let the copies already issued land before the CTA exits
+        for (uint32_t i = nq > (uint32_t)C::NQ ? nq - C::NQ : 0; i < nq; ++i)
+          drain_wait(BAR(C::B_QFULL + i % C::NQ), (i / C::NQ) & 1, 100000000ull);
+        for (uint32_t i = nd > (uint32_t)C::NDO ? nd - C::NDO : 0; i < nd; ++i)
+          drain_wait(BAR(C::B_DOFULL + i % C::NDO), (i / C::NDO) & 1, 100000000ull);
+        if (u_it > 0) drain_wait(BAR(C::B_KVFULL), (u_it - 1) & 1, 100000000ull);
+      }
+    }
+  } else if (warp == MMA_WARP) {
+    // ------------------------------------------------------------ MMA issue
+    if (lane == 0) {
+      Walker w;
+      w.init(spec);
+      uint32_t it = 0;
+      int u_it = 0;
+      bool ok = true;
+      const uint32_t kt = base + C::K_OFF, vt = base + C::V_OFF;
+      const uint32_t tSB = tmem + C::TM_SB, tDB = tmem + C::TM_DB;
+      auto qslot = [&](uint32_t s) { return base + C::Q_OFF + (s % C::NQ) * T::BYTES; };
+      auto dslot = [&](uint32_t s) { return base + C::DO_OFF + (s % C::NDO) * T::BYTES; };
+      for (int k = 0; ok; ++k) {
+        Unit u;
+        if (!w.seek(snake_index(k, G, cta), u)) break;
+        if (u.cost == 0) continue;
+        const int n = u.cost * group;
+        // Per step two sync points, each probing everything it needs at once:
+        //   A(i): P^T(i) ready (+ Q(i+1) loaded) -> dV(i), S^T(i+1)
+        //   B(i): dS^T(i) ready (+ dO(i+1) loaded) -> dK(i), dP^T(i+1)
+        // S^T(i+1) reuses the S buffer right after dV(i) has read P^T(i) from
+        // it (MMAs of one thread execute in order); dP^T(i+1) likewise after
+        // dK(i). The compute warps write the previous unit's dK/dV out before
+        // they arrive for step 0 of this unit, so A(0) also orders dV(0)
+        // (which overwrites the accumulator) after that read.
+        ok = mbar_wait3(BAR(C::B_KVFULL), u_it & 1, SITE_DKDV_KV_FULL,
+                        BAR(C::B_QFULL + it % C::NQ), (it / C::NQ) & 1, SITE_DKDV_Q_FULL,
+                        BAR(C::B_DOFULL + it % C::NDO), (it / C::NDO) & 1, SITE_DKDV_DO_FULL, wc);
+        if (!ok) break;
+        tc_fence_after();
+        mma_abt<D, C::IDESC_S>(tSB, kt, qslot(it));
+        tc_commit(BAR(C::B_SFULL));
+        mma_abt<D, C::IDESC_S>(tDB, vt, dslot(it));
+        tc_commit(BAR(C::B_DPFULL));
+        for (int i = 0; i < n && ok; ++i, ++it) {
+          const bool more = i + 1 < n;
+          const uint32_t it1 = it + 1;
+          // ---- A(i)
+          ok = mbar_wait3(BAR(C::B_PREADY), it & 1, SITE_DKDV_P_READY,
+                          more ? BAR(C::B_QFULL + it1 % C::NQ) : BAR(C::B_PREADY),
+                          more ? (it1 / C::NQ) & 1 : it & 1, SITE_DKDV_Q_FULL,
+                          BAR(C::B_PREADY), it & 1, SITE_DKDV_P_READY, wc);
+          if (!ok) break;
+          tc_fence_after();
+          mma_acc<D, C::IDESC_ACC>(tmem + C::TM_DV, tSB, dslot(it), i > 0);
+          tc_commit(BAR(C::B_DOEMPTY + it % C::NDO));
+          if (more) {
+            mma_abt<D, C::IDESC_S>(tSB, kt, qslot(it1));
+            tc_commit(BAR(C::B_SFULL));
+          }
+          // ---- B(i)
+          ok = mbar_wait3(BAR(C::B_DSREADY), it & 1, SITE_DKDV_DS_READY,
+                          more ? BAR(C::B_DOFULL + it1 % C::NDO) : BAR(C::B_DSREADY),
+                          more ? (it1 / C::NDO) & 1 : it & 1, SITE_DKDV_DO_FULL,
+                          BAR(C::B_DSREADY), it & 1, SITE_DKDV_DS_READY, wc);
+          if (!ok) break;
+          tc_fence_after();
+          mma_acc<D, C::IDESC_ACC>(tmem + C::TM_DK, tDB, qslot(it), i > 0);
+          tc_commit(BAR(C::B_QEMPTY + it % C::NQ));
+          if (more) {
+            mma_abt<D, C::IDESC_S>(tDB, vt, dslot(it1));
+            tc_commit(BAR(C::B_DPFULL));
+          } else {
+            tc_commit(BAR(C::B_ACCFULL));
+            tc_commit(BAR(C::B_KVEMPTY));
+          }
+        }
+        ++u_it;
+      }
+      if (!ok) {
+        tc_commit(BAR(C::B_DRAIN));
+        drain_wait(BAR(C::B_DRAIN), 0, 100000000ull);
+      }
+    }
+  }
+  } else {
+    regs_inc<REGS_COMPUTE>();
+    // ------------------------------------------------------------ P^T / dS^T
+    const int wg = warp >> 2;                             // query-column half
+    const int lg = warp & 3;
+    const int j = lg * 32 + lane;                         // key row within the block
+    const uint32_t lane_off = (uint32_t)(lg * 32) << 16;
+    const int c0 = wg * 64;
+    const uint32_t t_s = tmem + lane_off + C::TM_SB + c0;
+    const uint32_t t_dp = tmem + lane_off + C::TM_DB + c0;
+    const float sl2 = p.scale_log2;
+    Walker w;
+    w.init(spec);
+    uint32_t it = 0;
+    int u_it = 0;
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      Unit u;
+      if (!w.seek(snake_index(k, G, cta), u)) break;
+      const int g = u.head;
+      const int key = u.m * BN + j;                       // key index within the sequence
+      const bool key_ok = key < u.k_len;
+      const long long krow = ((long long)u.k_start + key) * p.Hkv + g;
+      __nv_bfloat16* dk_row = p.dk + krow * D + wg * (D / 2);
+      __nv_bfloat16* dv_row = p.dv + krow * D + wg * (D / 2);
+      if (u.cost == 0) {                                   // keys no query sees
+        if (key_ok) {
+          zero_half<D>(dk_row);
+          zero_half<D>(dv_row);
+        }
+        continue;
+      }
+      const int n = u.cost * group;
+      const int m_first = first_qblock(u, p.causal);
+      // query q (within the sequence) sees this key iff q >= qmin
+      const int qmin = p.causal ? key - (u.k_len - u.q_len) : -(1 << 30);
+      const long long pbase = pad_start(u.seq, u.q_start) + c0;
+      for (int i = 0; i < n; ++i, ++it) {
+        const StepInfo st = step_of(i, u.cost, m_first, g, group);
+        // -LSE*log2(e) and -D of this warpgroup's 64 query rows (padding rows
+        // hold -inf and 0, so they contribute exact zeros)
+        const long long off = (long long)st.h * p.pad_hstride + pbase + (long long)st.m * BM;
+        const float4* nl4 = reinterpret_cast<const float4*>(p.lse2 + off);
+        const float4* nd4 = reinterpret_cast<const float4*>(p.delta + off);
+        ok = mbar_wait(BAR(C::B_SFULL), it & 1, wc, SITE_DKDV_S_FULL);
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t sa[64];
+        tmem_ld64(t_s, sa);
+        // columns c with q0 + c < qmin are masked; a key past the sequence masks all
+        const int cmin = key_ok ? qmin - (st.m * BM + c0) : 64;
+        const bool mask = __any_sync(0xffffffffu, cmin > 0);
+        uint64_t p2[32];
+        {
+          const uint64_t sl2x2 = f2pack(sl2, sl2);
+#pragma unroll
+          for (int c = 0; c < 64; c += 4) {
+            const float4 l4 = __ldg(nl4 + c / 4);
+            float x[4];
+            f2unpack(ffma2(f2pack(u2f(sa[c]), u2f(sa[c + 1])), sl2x2, f2pack(l4.x, l4.y)), x[0],
+                     x[1]);
+            f2unpack(ffma2(f2pack(u2f(sa[c + 2]), u2f(sa[c + 3])), sl2x2, f2pack(l4.z, l4.w)),
+                     x[2], x[3]);
+            float pe[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              pe[e] = ((c + e) & 7) < POLY8 ? exp2_poly(x[e]) : ex2_mufu(x[e]);
+              if (mask) pe[e] = (c + e) < cmin ? 0.f : pe[e];
+            }
+            p2[c / 2] = f2pack(pe[0], pe[1]);
+            p2[c / 2 + 1] = f2pack(pe[2], pe[3]);
+          }
+        }
+        store_bf16_half(t_s, p2);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(BAR(C::B_PREADY));
+        ok = mbar_wait(BAR(C::B_DPFULL), it & 1, wc, SITE_DKDV_DP_FULL);
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t dpa[64];
+        tmem_ld64(t_dp, dpa);
+        uint32_t pk[32];
+#pragma unroll
+        for (int c = 0; c < 64; c += 4) {
+          const float4 d4 = __ldg(nd4 + c / 4);
+          pk[c / 2] = pack2(fmul2(p2[c / 2], fadd2(f2pack(u2f(dpa[c]), u2f(dpa[c + 1])),
+                                                   f2pack(d4.x, d4.y))));
+          pk[c / 2 + 1] = pack2(fmul2(p2[c / 2 + 1],
+                                      fadd2(f2pack(u2f(dpa[c + 2]), u2f(dpa[c + 3])),
+                                            f2pack(d4.z, d4.w))));
+        }
+        tmem_st32(t_dp, pk);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(BAR(C::B_DSREADY));
+      }
+      if (!ok) break;
+      // unit epilogue: this warpgroup's half of the dV and dK rows of this key
+      ok = mbar_wait(BAR(C::B_ACCFULL), u_it & 1, wc, SITE_DKDV_ACC_FULL);
+      if (!ok) break;
+      tc_fence_after();
+      ++u_it;
+      store_acc_half<D>(tmem + lane_off + C::TM_DV + wg * (D / 2), dv_row, 1.0f, key_ok);
+      store_acc_half<D>(tmem + lane_off + C::TM_DK + wg * (D / 2), dk_row, p.scale, key_ok);
+      tc_fence_before();
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == MMA_WARP) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+#undef BAR
+}
+
+// ============================================================== dQ pass
+template <int D, int POLY8>
+__global__ void __launch_bounds__(NUM_THREADS, 1) dq_kernel(const __grid_constant__ BwdParams p) {
+  using C = CfgQ<D>;
+  using T = Tile<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (base - raw);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t bars = base + C::BAR_OFF;
+#define BAR(i) (bars + 8u * (uint32_t)(i))
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::MISC_OFF);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
+  int* cu_s = reinterpret_cast<int*>(smem + C::CU_OFF);
+
+  if (threadIdx.x == 0) {
+    mbar_init(BAR(C::B_QFULL), 1);
+    mbar_init(BAR(C::B_QEMPTY), 1);
+    for (int s = 0; s < C::NKV; ++s) {
+      mbar_init(BAR(C::B_KVFULL + s), 1);
+      mbar_init(BAR(C::B_KVEMPTY + s), 1);
+    }
+    mbar_init(BAR(C::B_SFULL + 0), 1);
+    mbar_init(BAR(C::B_SFULL + 1), 1);
+    mbar_init(BAR(C::B_DPFULL), 1);
+    mbar_init(BAR(C::B_DSREADY), 256);
+    mbar_init(BAR(C::B_DQFULL), 1);
+    mbar_init(BAR(C::B_DRAIN), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == TMA_WARP && lane == 0) {
+    tma_prefetch_desc(&p.tm_q);
+    tma_prefetch_desc(&p.tm_do);
+    tma_prefetch_desc(&p.tm_k);
+    tma_prefetch_desc(&p.tm_v);
+  }
+  if (warp == MMA_WARP) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  const bool cu_in_smem = p.cu != nullptr && p.nseq <= MAX_SEQ_SMEM;
+  if (cu_in_smem)
+    for (int i = threadIdx.x; i <= p.nseq; i += NUM_THREADS) cu_s[i] = p.cu[i];
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  const SchedSpec spec{cu_in_smem ? cu_s : p.cu, p.nseq, p.Sq, p.Sk, p.Hq, p.causal, BM, BN, 0,
+                       p.hblock_q};
+  const WaitCtl wc{p.err, abort_flag, p.timeout_ns};
+  const int G = gridDim.x;
+  const int cta = blockIdx.x;
+  const int group = p.Hq / p.Hkv;
+
+  if (warp >= 8) {
+    regs_dec<REGS_CONTROL>();
+  if (warp >= 10) {
+    // spare warps of the control warpgroup
+  } else if (warp == TMA_WARP) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      Walker w;
+      w.init(spec);
+      uint32_t r = 0;                                     // K/V ring position
+      int u_it = 0;
+      bool ok = true;
+      for (int k = 0; ok; ++k) {
+        Unit u;
+        if (!w.seek(snake_index(k, G, cta), u)) break;
+        const int n = u.cost;
+        if (n == 0) continue;
+        const int kvh = u.head / group;
+        const int row = u.q_start + u.m * BM;
+        if (u_it > 0) {
+          ok = mbar_wait(BAR(C::B_QEMPTY), (u_it - 1) & 1, wc, SITE_DQ_Q_EMPTY);
+          if (!ok) break;
+        }
+        mbar_arrive_expect_tx(BAR(C::B_QFULL), 2 * T::BYTES);
+        for (int c = 0; c < T::CHUNKS; ++c) {
+          tma_load_3d(base + C::Q_OFF + c * T::CHUNK, &p.tm_q, BAR(C::B_QFULL), c * 64, u.head,
+                      row);
+          tma_load_3d(base + C::DO_OFF + c * T::CHUNK, &p.tm_do, BAR(C::B_QFULL), c * 64,
+                      u.head, row);
+        }
+        ++u_it;
+        for (int jb = 0; jb < n && ok; ++jb) {
+          for (int which = 0; which < 2; ++which, ++r) {
+            const int s = r % C::NKV;
+            if (r >= (uint32_t)C::NKV) {
+              ok = mbar_wait(BAR(C::B_KVEMPTY + s), ((r / C::NKV) - 1) & 1, wc, SITE_DQ_KV_EMPTY);
+              if (!ok) break;
+            }
+            mbar_arrive_expect_tx(BAR(C::B_KVFULL + s), T::BYTES);
+            const void* tm = which ? static_cast<const void*>(&p.tm_v)
+                                   : static_cast<const void*>(&p.tm_k);
+            for (int c = 0; c < T::CHUNKS; ++c)
+              tma_load_3d(base + C::KV_OFF + s * T::BYTES + c * T::CHUNK, tm,
+                          BAR(C::B_KVFULL + s), c * 64, kvh, u.k_start + jb * BN);
+          }
+        }
+      }
+      if (!ok) {
+        for (uint32_t i = r > (uint32_t)C::NKV ? r - C::NKV : 0; i < r; ++i)
+          drain_wait(BAR(C::B_KVFULL + i % C::NKV), (i / C::NKV) & 1, 100000000ull);
+        if (u_it > 0) drain_wait(BAR(C::B_QFULL), (u_it - 1) & 1, 100000000ull);
+      }
+    }
+  } else if (warp == MMA_WARP) {
+    // ------------------------------------------------------------ MMA issue
+    if (lane == 0) {
+      Walker w;
+      w.init(spec);
+      uint32_t r = 0, sj = 0;
+      int u_it = 0;
+      bool ok = true;
+      const uint32_t qt = base + C::Q_OFF, dot = base + C::DO_OFF;
+      auto kv = [&](uint32_t x) { return base + C::KV_OFF + (x % C::NKV) * T::BYTES; };
+      auto full = [&](uint32_t x) { return BAR(C::B_KVFULL + x % C::NKV); };
+      auto empty = [&](uint32_t x) { return BAR(C::B_KVEMPTY + x % C::NKV); };
+      auto ph = [&](uint32_t x) { return (x / C::NKV) & 1; };
+      for (int k = 0; ok; ++k) {
+        Unit u;
+        if (!w.seek(snake_index(k, G, cta), u)) break;
+        const int n = u.cost;
+        if (n == 0) continue;
+        // K_j sits at ring position r + 2j, V_j at r + 2j + 1. One sync point
+        // per step: dS(j) ready (+ V_{j+1}, K_{j+2} loaded) -> dQ += dS(j) K_j,
+        // dP(j+1), S(j+2) (into the buffer dQ(j) has just read). S runs two
+        // steps ahead of the compute warps, dP one. The compute warps write
+        // the previous unit's dQ before they arrive for step 0 of this unit,
+        // which orders dQ(0) (overwriting the accumulator) after that read.
+        ok = mbar_wait3(BAR(C::B_QFULL), u_it & 1, SITE_DQ_Q_FULL, full(r), ph(r),
+                        SITE_DQ_KV_FULL, full(r + 1), ph(r + 1), SITE_DQ_KV_FULL, wc);
+        if (!ok) break;
+        tc_fence_after();
+        mma_abt<D, C::IDESC_S>(tmem + C::TM_S + 128 * (sj & 1), qt, kv(r));
+        tc_commit(BAR(C::B_SFULL + (sj & 1)));
+        mma_abt<D, C::IDESC_S>(tmem + C::TM_DP, dot, kv(r + 1));
+        tc_commit(BAR(C::B_DPFULL));
+        tc_commit(empty(r + 1));
+        if (n == 1) tc_commit(BAR(C::B_QEMPTY));
+        if (n > 1) {
+          ok = mbar_wait(full(r + 2), ph(r + 2), wc, SITE_DQ_KV_FULL);
+          if (!ok) break;
+          tc_fence_after();
+          mma_abt<D, C::IDESC_S>(tmem + C::TM_S + 128 * ((sj + 1) & 1), qt, kv(r + 2));
+          tc_commit(BAR(C::B_SFULL + ((sj + 1) & 1)));
+        }
+        for (int jb = 0; jb < n && ok; ++jb, ++sj) {
+          const uint32_t b = sj & 1;
+          const bool more = jb + 1 < n, more2 = jb + 2 < n;
+          const uint32_t rk = r + 2 * jb, rv1 = rk + 3, rk2 = rk + 4;
+          ok = mbar_wait3(BAR(C::B_DSREADY), sj & 1, SITE_DQ_DS_READY,
+                          more ? full(rv1) : BAR(C::B_DSREADY), more ? ph(rv1) : sj & 1,
+                          SITE_DQ_KV_FULL, more2 ? full(rk2) : BAR(C::B_DSREADY),
+                          more2 ? ph(rk2) : sj & 1, SITE_DQ_KV_FULL, wc);
+          if (!ok) break;
+          tc_fence_after();
+          mma_acc<D, C::IDESC_DQ>(tmem + C::TM_DQ, tmem + C::TM_S + 128 * b, kv(rk), jb > 0);
+          tc_commit(empty(rk));
+          if (more) {
+            mma_abt<D, C::IDESC_S>(tmem + C::TM_DP, dot, kv(rv1));
+            tc_commit(BAR(C::B_DPFULL));
+            tc_commit(empty(rv1));
+            if (jb + 2 == n) tc_commit(BAR(C::B_QEMPTY));
+          } else {
+            tc_commit(BAR(C::B_DQFULL));
+          }
+          if (more2) {
+            mma_abt<D, C::IDESC_S>(tmem + C::TM_S + 128 * b, qt, kv(rk2));
+            tc_commit(BAR(C::B_SFULL + b));
+          }
+        }
+        r += 2 * n;
+        ++u_it;
+      }
+      if (!ok) {
+        tc_commit(BAR(C::B_DRAIN));
+        drain_wait(BAR(C::B_DRAIN), 0, 100000000ull);
+      }
+    }
+  }
+  } else {
+    regs_inc<REGS_COMPUTE>();
+    // ------------------------------------------------------------ P / dS
+    const int wg = warp >> 2;                             // key-column half
+    const int lg = warp & 3;
+    const int rr = lg * 32 + lane;                        // query row within the block
+    const uint32_t lane_off = (uint32_t)(lg * 32) << 16;
+    const int c0 = wg * 64;
+    const uint32_t t_s = tmem + lane_off + C::TM_S + c0;
+    const uint32_t t_dp = tmem + lane_off + C::TM_DP + c0;
+    const float sl2 = p.scale_log2;
+    Walker w;
+    w.init(spec);
+    uint32_t sj = 0;
+    int u_it = 0;
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      Unit u;
+      if (!w.seek(snake_index(k, G, cta), u)) break;
+      const int n = u.cost;
+      const int row = u.m * BM + rr;
+      const bool valid = row < u.q_len;
+      __nv_bfloat16* dq_row =
+          p.dq + (((long long)u.q_start + row) * p.Hq + u.head) * D + wg * (D / 2);
+      if (n == 0) {                                        // rows that see no key
+        if (valid) zero_half<D>(dq_row);
+        continue;
+      }
+      const long long pi = (long long)u.head * p.pad_hstride + pad_start(u.seq, u.q_start) + row;
+      const float nlse = p.lse2[pi];                      // -LSE*log2(e); -inf on padding rows
+      const float nd = p.delta[pi];                       // -D
+      int kv_lim = u.k_len;
+      if (p.causal) {
+        const int lim = row + 1 + (u.k_len - u.q_len);
+        kv_lim = lim < kv_lim ? lim : kv_lim;
+      }
+      const uint64_t sl2x2 = f2pack(sl2, sl2), nl2 = f2pack(nlse, nlse), nd2 = f2pack(nd, nd);
+      for (int jb = 0; jb < n; ++jb, ++sj) {
+        const uint32_t b = sj & 1;
+        ok = mbar_wait(BAR(C::B_SFULL + b), (sj >> 1) & 1, wc, SITE_DQ_S_FULL);
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t sa[64];
+        tmem_ld64(t_s + 128 * b, sa);
+        const int lim = kv_lim - (jb * BN + c0);          // columns c >= lim are masked
+        const bool mask = __any_sync(0xffffffffu, lim < 64);
+        uint64_t p2[32];
+#pragma unroll
+        for (int c = 0; c < 64; c += 2) {
+          float x0, x1;
+          f2unpack(ffma2(f2pack(u2f(sa[c]), u2f(sa[c + 1])), sl2x2, nl2), x0, x1);
+          float e0 = (c & 7) < POLY8 ? exp2_poly(x0) : ex2_mufu(x0);
+          float e1 = ((c + 1) & 7) < POLY8 ? exp2_poly(x1) : ex2_mufu(x1);
+          if (mask) {
+            e0 = c < lim ? e0 : 0.f;
+            e1 = c + 1 < lim ? e1 : 0.f;
+          }
+          p2[c / 2] = f2pack(e0, e1);
+        }
+        ok = mbar_wait(BAR(C::B_DPFULL), sj & 1, wc, SITE_DQ_DP_FULL);
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t dpa[64];
+        tmem_ld64(t_dp, dpa);
+        uint32_t pk[32];
+#pragma unroll
+        for (int c = 0; c < 64; c += 2)
+          pk[c / 2] = pack2(fmul2(p2[c / 2], fadd2(f2pack(u2f(dpa[c]), u2f(dpa[c + 1])), nd2)));
+        tmem_st32(t_s + 128 * b, pk);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(BAR(C::B_DSREADY));
+      }
+      if (!ok) break;
+      ok = mbar_wait(BAR(C::B_DQFULL), u_it & 1, wc, SITE_DQ_DQ_FULL);
+      if (!ok) break;
+      tc_fence_after();
+      ++u_it;
+      store_acc_half<D>(tmem + lane_off + C::TM_DQ + wg * (D / 2), dq_row, p.scale, valid);
+      tc_fence_before();
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == MMA_WARP) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+#undef BAR
+}
+
+}  // namespace bsplit
+
+template <int D, int POLY8>
+static cudaError_t launch_split_pair(const BwdParams& p, int grid_kv, int grid_q,
+                                     cudaStream_t stream) {
+  auto kkv = bsplit::dkdv_kernel<D, POLY8>;
+  auto kq = bsplit::dq_kernel<D, POLY8>;
+  const int s_kv = bsplit::CfgKV<D>::SMEM_BYTES, s_q = bsplit::CfgQ<D>::SMEM_BYTES;
+  cudaError_t e = cudaFuncSetAttribute(kkv, cudaFuncAttributeMaxDynamicSharedMemorySize, s_kv);
+  if (e != cudaSuccess) return e;
+  if ((e = cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, s_q)) !=
+      cudaSuccess)
+    return e;
+  if (grid_kv > 0) {
+    kkv<<<grid_kv, bsplit::NUM_THREADS, s_kv, stream>>>(p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  if (grid_q > 0) {
+    kq<<<grid_q, bsplit::NUM_THREADS, s_q, stream>>>(p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+// The two passes of the split backward (after the preprocess pass of bwd.cu).
+cudaError_t launch_bwd_split(const BwdParams& p, int d, int grid_kv, int grid_q,
+                             cudaStream_t stream, int poly8) {
+  if (d == 128) {
+    switch (poly8) {
+      case 0: return launch_split_pair<128, 0>(p, grid_kv, grid_q, stream);
+      case 2: return launch_split_pair<128, 2>(p, grid_kv, grid_q, stream);
+      case 4: return launch_split_pair<128, 4>(p, grid_kv, grid_q, stream);
+      default: return cudaErrorInvalidValue;
+    }
+  }
+  if (d == 64) {
+    switch (poly8) {
+      case 0: return launch_split_pair<64, 0>(p, grid_kv, grid_q, stream);
+      case 2: return launch_split_pair<64, 2>(p, grid_kv, grid_q, stream);
+      case 4: return launch_split_pair<64, 4>(p, grid_kv, grid_q, stream);
+      default: return cudaErrorInvalidValue;
+    }
+  }
+  return cudaErrorNotSupported;
+}
+
+}  // namespace fa

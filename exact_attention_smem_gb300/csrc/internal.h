@@ -17,6 +17,11 @@ enum WaitSite : int {
   SITE_BWD_KV_FULL = 201, SITE_BWD_QD_EMPTY, SITE_BWD_QD_FULL, SITE_BWD_S_FULL,
   SITE_BWD_DP_FULL, SITE_BWD_P_READY, SITE_BWD_DS_READY, SITE_BWD_DQ_FULL,
   SITE_BWD_DQ_EMPTY, SITE_BWD_ACC_FULL, SITE_BWD_KV_EMPTY,
+  SITE_DKDV_KV_FULL = 301, SITE_DKDV_KV_EMPTY, SITE_DKDV_Q_FULL, SITE_DKDV_Q_EMPTY,
+  SITE_DKDV_DO_FULL, SITE_DKDV_DO_EMPTY, SITE_DKDV_S_FULL, SITE_DKDV_DP_FULL,
+  SITE_DKDV_P_READY, SITE_DKDV_DS_READY, SITE_DKDV_ACC_FULL,
+  SITE_DQ_Q_FULL = 401, SITE_DQ_Q_EMPTY, SITE_DQ_KV_FULL, SITE_DQ_KV_EMPTY, SITE_DQ_S_FULL,
+  SITE_DQ_DP_FULL, SITE_DQ_DS_READY, SITE_DQ_DQ_FULL,
   SITE_TEST = 901,
 };
 
@@ -25,6 +30,8 @@ struct Knobs {
   float tau_log2 = 0.0f;         // rescale threshold, base-2 units
   int poly8 = 0;                 // eighths of the exponentials done by the polynomial (fwd)
   int bwd_poly8 = 0;             // same for the backward
+  int bwd_mode = 1;              // 1: two-pass backward (dK/dV pass + dQ pass); 0: one pass
+                                 // with dQ by fp32 atomics and a convert pass
   long long timeout_ns = 2000000000LL;
   int grid_override = 0;         // >0: persistent grid size (schedule permutation tests)
   cudaEvent_t ev[2][2] = {{nullptr, nullptr}, {nullptr, nullptr}};  // [fwd|bwd][start|stop]
@@ -59,29 +66,34 @@ struct FwdParams {
 };
 
 struct BwdParams {
-  CUtensorMap tm_q, tm_do;       // [T, Hq, d] views, 64-column x 64-row boxes, 128B swizzle
+  CUtensorMap tm_q, tm_do;       // [T, Hq, d] views, 64-column boxes of 64 rows (one-pass
+                                 // kernel) or 128 rows (two-pass kernels), 128B swizzle
   CUtensorMap tm_k, tm_v;        // [T, Hkv, d] views, 64-column x 128-row boxes
   __nv_bfloat16 *dk, *dv;
-  float* dq_acc;                 // fp32 [Tq, Hq, d]
+  __nv_bfloat16* dq;             // bf16 [Tq, Hq, d] (written directly by the dQ pass)
+  float* dq_acc;                 // fp32 [Tq, Hq, d] (one-pass kernel only; else nullptr)
   const float* lse2;             // fp32 [Hq][pad_hstride] padded per sequence: -LSE * log2(e)
   const float* delta;            // fp32 [Hq][pad_hstride] padded: -D_i = -sum_c dO_ic O_ic
   long long pad_hstride;         // floats per head in the padded row arrays
   const int* cu;
   int nseq, Hq, Hkv, Sq, Sk, total_q, total_k, causal;
   float scale_log2, scale;
-  int hblock;                    // KV heads per scheduler group
+  int hblock;                    // KV heads per scheduler group (dK/dV units)
+  int hblock_q;                  // query heads per scheduler group (dQ units)
   long long* trace;              // optional role timeline of CTA 0 (nullptr = off)
   int* err;
   unsigned long long timeout_ns;
 };
 
 // Padded per-sequence row arrays used by the backward: sequence i's rows start
-// at a 64-float boundary, so every 64-row block is one aligned 256-byte copy.
+// at a 128-float boundary (every 64- or 128-row block is an aligned copy) and
+// are followed by at least 129 padding rows, so a block that starts inside the
+// sequence never reaches the next sequence's rows.
 __host__ __device__ __forceinline__ long long pad_start(int seq_i, int q_start) {
-  return (long long)((q_start + 63) & ~63) + 128ll * seq_i;
+  return (long long)((q_start + 127) & ~127) + 256ll * seq_i;
 }
 __host__ __device__ __forceinline__ long long pad_hstride(long long T, int nseq) {
-  return ((T + 63) & ~63ll) + 128ll * (nseq + 1);
+  return ((T + 127) & ~127ll) + 256ll * (nseq + 1);
 }
 
 // Launchers (fwd.cu / bwd.cu). Return a cudaError_t.
@@ -95,8 +107,12 @@ struct BwdAux {                  // inputs of the preprocess / convert passes
   long long lse_seqstride;
   __nv_bfloat16* dq;
 };
-cudaError_t launch_bwd(const BwdParams& p, const BwdAux& aux, int d, int grid,
-                       cudaStream_t stream, int poly8);
+// mode 1: preprocess, dK/dV pass (grid), dQ pass (grid_q); mode 0: preprocess,
+// one-pass kernel (grid), convert.
+cudaError_t launch_bwd(const BwdParams& p, const BwdAux& aux, int d, int grid, int grid_q,
+                       cudaStream_t stream, int poly8, int mode);
+cudaError_t launch_bwd_split(const BwdParams& p, int d, int grid_kv, int grid_q,
+                             cudaStream_t stream, int poly8);
 
 int num_sms();
 int* device_error_word();

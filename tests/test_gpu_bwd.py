@@ -1,4 +1,8 @@
-"""Backward parity: dQ, dK, dV from the CUDA path against the fp64 oracle."""
+"""Backward parity: dQ, dK, dV from the CUDA path against the fp64 oracle.
+
+Every test runs for both backward forms: mode 1 (default: a dK/dV pass over
+key blocks and a dQ pass over query blocks, no atomics) and mode 0 (one pass
+with dQ accumulated by fp32 atomics, then converted)."""
 import math
 
 import numpy as np
@@ -21,6 +25,14 @@ def _dev():
     yield
     fa.fa_debug_set("grid", 0)
     fa.fa_debug_set("bwd_poly8", 0)
+    fa.fa_debug_set("bwd_mode", 1)
+
+
+@pytest.fixture(params=[1, 0], ids=["two_pass", "one_pass"], autouse=True)
+def bwd_mode(request):
+    fa.fa_debug_set("bwd_mode", request.param)
+    yield request.param
+    fa.fa_debug_set("bwd_mode", 1)
 
 
 def _dims(x, cu):
@@ -100,14 +112,26 @@ def test_gqa_matches_repeated_kv():
         assert (a.float() - s).abs().max().item() <= 2e-2 * s.abs().max().item()
 
 
-def test_schedule_permutation():
+def test_schedule_permutation(bwd_mode):
     x = random_inputs(B=2, Hq=2, Hkv=2, Sq=700, Sk=700, d=128, seed=78, device="cuda")
     a = _run(x, True, 0.1)
     fa.fa_debug_set("grid", 5)
     b = _run(x, True, 0.1)
     fa.fa_debug_set("grid", 0)
     assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])     # dK, dV: no atomics
-    assert (a[0].float() - b[0].float()).abs().max().item() <= 1e-2
+    if bwd_mode == 1:
+        assert torch.equal(a[0], b[0])                              # dQ: no atomics either
+    else:
+        assert (a[0].float() - b[0].float()).abs().max().item() <= 1e-2
+
+
+def test_two_pass_is_deterministic(bwd_mode):
+    if bwd_mode != 1:
+        pytest.skip("the one-pass form adds dQ with atomics")
+    x = random_inputs(B=1, Hq=4, Hkv=2, Sq=1000, Sk=1000, d=128, seed=81, device="cuda")
+    a = _run(x, True, 0.1)
+    b = _run(x, True, 0.1)
+    assert all(torch.equal(u, v) for u, v in zip(a, b))
 
 
 @pytest.mark.parametrize("poly8", [2, 4])
@@ -118,8 +142,21 @@ def test_poly_exp_split(poly8):
     fa.fa_debug_set("bwd_poly8", 0)
 
 
-def test_head_dim_64_backward_is_reported_unsupported():
-    x = random_inputs(B=1, Hq=2, Hkv=2, Sq=128, Sk=128, d=64, seed=80, device="cuda")
-    with pytest.raises(fa.FAError) as e:
-        _run(x, False, 0.125)
-    assert e.value.status == 2
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("S", [1, 100, 128, 300])
+def test_head_dim_64(S, causal, bwd_mode):
+    x = random_inputs(B=2, Hq=4, Hkv=2, Sq=S, Sk=S, d=64, seed=80 + S, device="cuda")
+    if bwd_mode == 0:
+        with pytest.raises(fa.FAError) as e:
+            _run(x, causal, 0.125)
+        assert e.value.status == 2                                  # one-pass form: d=128 only
+    else:
+        _check(x, causal, 0.125)
+
+
+def test_head_dim_64_varlen(bwd_mode):
+    if bwd_mode == 0:
+        pytest.skip("the one-pass form supports d=128 only")
+    x = random_inputs(B=None, Hq=2, Hkv=2, Sq=None, Sk=None, d=64, seed=82,
+                      lengths=[3, 130, 257], device="cuda")
+    _check(x, True, 0.125, cu=x.cu_seqlens)
