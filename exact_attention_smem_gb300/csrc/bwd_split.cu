@@ -28,8 +28,8 @@
 //
 // Both kernels: 12 warps. Warps 0-3 and 4-7 are two compute warpgroups that
 // split the 128 columns of each score tile (64 each, one thread per TMEM lane =
-// tile row); warp 8 allocates TMEM and one of its threads issues the MMAs; warp
-// 9 is the TMA producer; warps 10-11 only complete the register split.
+// tile row); warp 8 allocates TMEM and one of its threads issues the MMAs;
+// warp 9 is the TMA producer; warps 10-11 only complete the register split.
 // A warpgroup writes its bf16 half of P^T/dS^T/dS over the first 32 of its own
 // 64 fp32 columns, so the A operand of the accumulating MMA sits in columns
 // [0,32) and [64,96) of its buffer.
@@ -65,21 +65,28 @@ struct Tile {
 };
 
 // dK/dV pass layout. Q slots are held from S^T(i) to dK(i), the longest span,
-// so Q gets three slots and dO two.
+// so Q gets three slots and dO two. The -LSE*log2(e) and -D values of a
+// step's 128 query rows (one per score column) go through a two-slot ring of
+// their own, filled by the producer and released by the compute warps. The
+// layout leaves no room for aligning the dynamic shared memory by hand: the
+// kernel requires (and checks) that it starts on a 1024-byte boundary.
 template <int D>
 struct CfgKV {
   using T = Tile<D>;
-  static constexpr int NQ = 3, NDO = 2;
+  static constexpr int NQ = 3, NDO = 2, NLD = 2;
+  static constexpr int LD_BYTES = 2 * BM * 4;          // [-LSE*log2e x128][-D x128]
   static constexpr int K_OFF = 0, V_OFF = T::BYTES, Q_OFF = 2 * T::BYTES,
-                       DO_OFF = Q_OFF + NQ * T::BYTES, BAR_OFF = DO_OFF + NDO * T::BYTES;
+                       DO_OFF = Q_OFF + NQ * T::BYTES, LD_OFF = DO_OFF + NDO * T::BYTES,
+                       BAR_OFF = LD_OFF + NLD * LD_BYTES;
   static constexpr int B_KVFULL = 0, B_KVEMPTY = 1, B_QFULL = 2, B_QEMPTY = B_QFULL + NQ,
                        B_DOFULL = B_QEMPTY + NQ, B_DOEMPTY = B_DOFULL + NDO,
-                       B_SFULL = B_DOEMPTY + NDO, B_DPFULL = B_SFULL + 1,
+                       B_LDFULL = B_DOEMPTY + NDO, B_LDEMPTY = B_LDFULL + NLD,
+                       B_SFULL = B_LDEMPTY + NLD, B_DPFULL = B_SFULL + 1,
                        B_PREADY = B_DPFULL + 1, B_DSREADY = B_PREADY + 1,
                        B_ACCFULL = B_DSREADY + 1, B_DRAIN = B_ACCFULL + 1, NBAR = B_DRAIN + 1;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int CU_OFF = MISC_OFF + 16;
-  static constexpr int SMEM_BYTES = CU_OFF + (MAX_SEQ_SMEM + 1) * 4 + 1024;
+  static constexpr int SMEM_BYTES = CU_OFF + (MAX_SEQ_SMEM + 1) * 4;
   static_assert(SMEM_BYTES <= SMEM_LIMIT, "dK/dV pass shared memory");
   // TMEM: dV [0,D), dK [D,2D), S^T/P^T [2D,2D+128), dP^T/dS^T [2D+128,2D+256)
   static constexpr uint32_t TM_DV = 0, TM_DK = D, TM_SB = 2 * D, TM_DB = 2 * D + 128;
@@ -201,6 +208,18 @@ __device__ __forceinline__ void store_acc_half(uint32_t t_acc, __nv_bfloat16* ds
   }
 }
 
+// Role timeline for tuning (CTA 0 only, when a trace buffer is armed).
+#define FA_TRACE(ev, step)                                                        \
+  do {                                                                            \
+    if (p.trace != nullptr && blockIdx.x == 0 && (step) < (uint32_t)TRACE_STEPS) \
+      p.trace[(ev) * TRACE_STEPS + (step)] = clock64();                           \
+  } while (0)
+#define FA_TRACE_VAL(ev, step, val)                                               \
+  do {                                                                            \
+    if (p.trace != nullptr && blockIdx.x == 0 && (step) < (uint32_t)TRACE_STEPS) \
+      p.trace[(ev) * TRACE_STEPS + (step)] = (val);                               \
+  } while (0)
+
 template <int D>
 __device__ __forceinline__ void zero_half(__nv_bfloat16* dst) {
 #pragma unroll
@@ -212,10 +231,16 @@ template <int D, int POLY8>
 __global__ void __launch_bounds__(NUM_THREADS, 1) dkdv_kernel(const __grid_constant__ BwdParams p) {
   using C = CfgKV<D>;
   using T = Tile<D>;
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw = smem_u32(smem_raw);
-  const uint32_t base = (raw + 1023u) & ~1023u;
-  uint8_t* smem = smem_raw + (base - raw);
+  extern __shared__ __align__(1024) uint8_t smem_al[];
+  uint32_t base;                                        // opaque to the compiler: checked, not assumed
+  asm volatile("{\n\t.reg .u64 t;\n\tcvta.to.shared.u64 t, %1;\n\tcvt.u32.u64 %0, t;\n\t}"
+               : "=r"(base)
+               : "l"(smem_al));
+  if (base & 1023u) {                                   // 128B-swizzled tiles need 1024 B
+    if (threadIdx.x == 0) atomicCAS(p.err, 0, SITE_SMEM_ALIGN);
+    return;
+  }
+  uint8_t* smem = smem_al;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t bars = base + C::BAR_OFF;
@@ -234,6 +259,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dkdv_kernel(const __grid_const
     for (int s = 0; s < C::NDO; ++s) {
       mbar_init(BAR(C::B_DOFULL + s), 1);
       mbar_init(BAR(C::B_DOEMPTY + s), 1);
+    }
+    for (int s = 0; s < C::NLD; ++s) {
+      mbar_init(BAR(C::B_LDFULL + s), 1);
+      mbar_init(BAR(C::B_LDEMPTY + s), 256);
     }
     mbar_init(BAR(C::B_SFULL), 1);
     mbar_init(BAR(C::B_DPFULL), 1);
@@ -280,7 +309,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dkdv_kernel(const __grid_const
       w.init(spec);
       int u_it = 0;
       bool ok = true;
-      uint32_t nq = 0, nd = 0;                            // Q / dO loads issued
+      uint32_t nq = 0, nd = 0, nl = 0;                    // Q / dO / row-value loads issued
       for (int k = 0; ok; ++k) {
         Unit u;
         if (!w.seek(snake_index(k, G, cta), u)) break;
@@ -331,6 +360,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dkdv_kernel(const __grid_const
             tma_load_3d(base + C::DO_OFF + sd * T::BYTES + c * T::CHUNK, &p.tm_do,
                         BAR(C::B_DOFULL + sd), c * 64, st.h, row);
           ++nd;
+          // the step's row values, released by the compute warps after dS
+          const int sl = nl % C::NLD;
+          if (nl >= (uint32_t)C::NLD) {
+            ok = mbar_wait(BAR(C::B_LDEMPTY + sl), ((nl / C::NLD) - 1) & 1, wc,
+                           SITE_DKDV_LD_EMPTY);
+            if (!ok) break;
+          }
+          const long long off = (long long)st.h * p.pad_hstride + pad_start(u.seq, u.q_start) +
+                                (long long)st.m * BM;
+          const uint32_t ld = base + C::LD_OFF + sl * C::LD_BYTES;
+          mbar_arrive_expect_tx(BAR(C::B_LDFULL + sl), C::LD_BYTES);
+          bulk_load(ld, p.lse2 + off, BM * 4, BAR(C::B_LDFULL + sl));
+          bulk_load(ld + BM * 4, p.delta + off, BM * 4, BAR(C::B_LDFULL + sl));
+          ++nl;
         }
       }
       if (!ok) {
@@ -339,6 +382,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dkdv_kernel(const __grid_const
           drain_wait(BAR(C::B_QFULL + i % C::NQ), (i / C::NQ) & 1, 100000000ull);
         for (uint32_t i = nd > (uint32_t)C::NDO ? nd - C::NDO : 0; i < nd; ++i)
           drain_wait(BAR(C::B_DOFULL + i % C::NDO), (i / C::NDO) & 1, 100000000ull);
+        for (uint32_t i = nl > (uint32_t)C::NLD ? nl - C::NLD : 0; i < nl; ++i)
+          drain_wait(BAR(C::B_LDFULL + i % C::NLD), (i / C::NLD) & 1, 100000000ull);
         if (u_it > 0) drain_wait(BAR(C::B_KVFULL), (u_it - 1) & 1, 100000000ull);
       }
     }
@@ -359,7 +404,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dkdv_kernel(const __grid_const
         if (!w.seek(snake_index(k, G, cta), u)) break;
         if (u.cost == 0) continue;
         const int n = u.cost * group;
-        // Per step two sync points, each probing everything it needs at once:
+        // Per step two sync points, each probing everything it needs at once
+        // (every memory access of this thread waits for the MMAs it has
+        // queued, so the probes of a sync point go out together):
         //   A(i): P^T(i) ready (+ Q(i+1) loaded) -> dV(i), S^T(i+1)
         //   B(i): dS^T(i) ready (+ dO(i+1) loaded) -> dK(i), dP^T(i+1)
         // S^T(i+1) reuses the S buffer right after dV(i) has read P^T(i) from
@@ -385,6 +432,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dkdv_kernel(const __grid_const
                           more ? (it1 / C::NQ) & 1 : it & 1, SITE_DKDV_Q_FULL,
                           BAR(C::B_PREADY), it & 1, SITE_DKDV_P_READY, wc);
           if (!ok) break;
+          FA_TRACE(TR_KV_A, it);
           tc_fence_after();
           mma_acc<D, C::IDESC_ACC>(tmem + C::TM_DV, tSB, dslot(it), i > 0);
           tc_commit(BAR(C::B_DOEMPTY + it % C::NDO));
@@ -398,6 +446,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dkdv_kernel(const __grid_const
                           more ? (it1 / C::NDO) & 1 : it & 1, SITE_DKDV_DO_FULL,
                           BAR(C::B_DSREADY), it & 1, SITE_DKDV_DS_READY, wc);
           if (!ok) break;
+          FA_TRACE(TR_KV_B, it);
           tc_fence_after();
           mma_acc<D, C::IDESC_ACC>(tmem + C::TM_DK, tDB, qslot(it), i > 0);
           tc_commit(BAR(C::B_QEMPTY + it % C::NQ));
@@ -453,16 +502,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dkdv_kernel(const __grid_const
       const int m_first = first_qblock(u, p.causal);
       // query q (within the sequence) sees this key iff q >= qmin
       const int qmin = p.causal ? key - (u.k_len - u.q_len) : -(1 << 30);
-      const long long pbase = pad_start(u.seq, u.q_start) + c0;
       for (int i = 0; i < n; ++i, ++it) {
         const StepInfo st = step_of(i, u.cost, m_first, g, group);
         // -LSE*log2(e) and -D of this warpgroup's 64 query rows (padding rows
-        // hold -inf and 0, so they contribute exact zeros)
-        const long long off = (long long)st.h * p.pad_hstride + pbase + (long long)st.m * BM;
-        const float4* nl4 = reinterpret_cast<const float4*>(p.lse2 + off);
-        const float4* nd4 = reinterpret_cast<const float4*>(p.delta + off);
+        // hold -inf and 0, so they contribute exact zeros), from the ring
+        const uint32_t sl = it % C::NLD;
+        const float4* nl4 =
+            reinterpret_cast<const float4*>(smem + C::LD_OFF + sl * C::LD_BYTES) + c0 / 4;
+        const float4* nd4 = nl4 + BM / 4;
+        ok = mbar_wait(BAR(C::B_LDFULL + sl), (it / C::NLD) & 1, wc, SITE_DKDV_LD_FULL);
+        if (!ok) break;
+        // -LSE*log2(e) into registers while S^T is still on its way
+        float4 l4r[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) l4r[c] = nl4[c];
         ok = mbar_wait(BAR(C::B_SFULL), it & 1, wc, SITE_DKDV_S_FULL);
         if (!ok) break;
+        if (threadIdx.x == 0) FA_TRACE(TR_KV_S, it);
         tc_fence_after();
         uint32_t sa[64];
         tmem_ld64(t_s, sa);
@@ -474,7 +530,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dkdv_kernel(const __grid_const
           const uint64_t sl2x2 = f2pack(sl2, sl2);
 #pragma unroll
           for (int c = 0; c < 64; c += 4) {
-            const float4 l4 = __ldg(nl4 + c / 4);
+            const float4 l4 = l4r[c / 4];
             float x[4];
             f2unpack(ffma2(f2pack(u2f(sa[c]), u2f(sa[c + 1])), sl2x2, f2pack(l4.x, l4.y)), x[0],
                      x[1]);
@@ -494,25 +550,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dkdv_kernel(const __grid_const
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(BAR(C::B_PREADY));
+        if (threadIdx.x == 0) FA_TRACE(TR_KV_P, it);
         ok = mbar_wait(BAR(C::B_DPFULL), it & 1, wc, SITE_DKDV_DP_FULL);
         if (!ok) break;
+        if (threadIdx.x == 0) FA_TRACE(TR_KV_DP, it);
         tc_fence_after();
         uint32_t dpa[64];
         tmem_ld64(t_dp, dpa);
         uint32_t pk[32];
 #pragma unroll
         for (int c = 0; c < 64; c += 4) {
-          const float4 d4 = __ldg(nd4 + c / 4);
+          const float4 d4 = nd4[c / 4];
           pk[c / 2] = pack2(fmul2(p2[c / 2], fadd2(f2pack(u2f(dpa[c]), u2f(dpa[c + 1])),
                                                    f2pack(d4.x, d4.y))));
           pk[c / 2 + 1] = pack2(fmul2(p2[c / 2 + 1],
                                       fadd2(f2pack(u2f(dpa[c + 2]), u2f(dpa[c + 3])),
                                             f2pack(d4.z, d4.w))));
         }
+        mbar_arrive(BAR(C::B_LDEMPTY + sl));
         tmem_st32(t_dp, pk);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(BAR(C::B_DSREADY));
+        if (threadIdx.x == 0) FA_TRACE(TR_KV_DS, it);
       }
       if (!ok) break;
       // unit epilogue: this warpgroup's half of the dV and dK rows of this key
@@ -604,6 +664,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dq_kernel(const __grid_constan
       Walker w;
       w.init(spec);
       uint32_t r = 0;                                     // K/V ring position
+      uint32_t pj = 0;                                    // steps loaded (trace index)
       int u_it = 0;
       bool ok = true;
       for (int k = 0; ok; ++k) {
@@ -632,6 +693,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dq_kernel(const __grid_constan
               ok = mbar_wait(BAR(C::B_KVEMPTY + s), ((r / C::NKV) - 1) & 1, wc, SITE_DQ_KV_EMPTY);
               if (!ok) break;
             }
+            if (which == 0) FA_TRACE(TR_Q_KLOAD, pj);
             mbar_arrive_expect_tx(BAR(C::B_KVFULL + s), T::BYTES);
             const void* tm = which ? static_cast<const void*>(&p.tm_v)
                                    : static_cast<const void*>(&p.tm_k);
@@ -639,6 +701,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dq_kernel(const __grid_constan
               tma_load_3d(base + C::KV_OFF + s * T::BYTES + c * T::CHUNK, tm,
                           BAR(C::B_KVFULL + s), c * 64, kvh, u.k_start + jb * BN);
           }
+          ++pj;
         }
       }
       if (!ok) {
@@ -697,6 +760,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dq_kernel(const __grid_constan
                           SITE_DQ_KV_FULL, more2 ? full(rk2) : BAR(C::B_DSREADY),
                           more2 ? ph(rk2) : sj & 1, SITE_DQ_KV_FULL, wc);
           if (!ok) break;
+          FA_TRACE(TR_Q_SYNC, sj);
           tc_fence_after();
           mma_acc<D, C::IDESC_DQ>(tmem + C::TM_DQ, tmem + C::TM_S + 128 * b, kv(rk), jb > 0);
           tc_commit(empty(rk));
@@ -763,6 +827,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dq_kernel(const __grid_constan
         const uint32_t b = sj & 1;
         ok = mbar_wait(BAR(C::B_SFULL + b), (sj >> 1) & 1, wc, SITE_DQ_S_FULL);
         if (!ok) break;
+        if (threadIdx.x == 0) FA_TRACE(TR_Q_S, sj);
         tc_fence_after();
         uint32_t sa[64];
         tmem_ld64(t_s + 128 * b, sa);
@@ -781,8 +846,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dq_kernel(const __grid_constan
           }
           p2[c / 2] = f2pack(e0, e1);
         }
+        if (threadIdx.x == 0) FA_TRACE(TR_Q_P, sj);
         ok = mbar_wait(BAR(C::B_DPFULL), sj & 1, wc, SITE_DQ_DP_FULL);
         if (!ok) break;
+        if (threadIdx.x == 0) FA_TRACE(TR_Q_DP, sj);
         tc_fence_after();
         uint32_t dpa[64];
         tmem_ld64(t_dp, dpa);
@@ -794,6 +861,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dq_kernel(const __grid_constan
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(BAR(C::B_DSREADY));
+        if (threadIdx.x == 0) FA_TRACE(TR_Q_DS, sj);
       }
       if (!ok) break;
       ok = mbar_wait(BAR(C::B_DQFULL), u_it & 1, wc, SITE_DQ_DQ_FULL);

@@ -19,9 +19,11 @@ enum WaitSite : int {
   SITE_BWD_DQ_EMPTY, SITE_BWD_ACC_FULL, SITE_BWD_KV_EMPTY,
   SITE_DKDV_KV_FULL = 301, SITE_DKDV_KV_EMPTY, SITE_DKDV_Q_FULL, SITE_DKDV_Q_EMPTY,
   SITE_DKDV_DO_FULL, SITE_DKDV_DO_EMPTY, SITE_DKDV_S_FULL, SITE_DKDV_DP_FULL,
-  SITE_DKDV_P_READY, SITE_DKDV_DS_READY, SITE_DKDV_ACC_FULL,
+  SITE_DKDV_P_READY, SITE_DKDV_DS_READY, SITE_DKDV_ACC_FULL, SITE_DKDV_LD_FULL,
+  SITE_DKDV_LD_EMPTY,
   SITE_DQ_Q_FULL = 401, SITE_DQ_Q_EMPTY, SITE_DQ_KV_FULL, SITE_DQ_KV_EMPTY, SITE_DQ_S_FULL,
   SITE_DQ_DP_FULL, SITE_DQ_DS_READY, SITE_DQ_DQ_FULL,
+  SITE_SMEM_ALIGN = 801,         // dynamic shared memory not on a 1024-byte boundary
   SITE_TEST = 901,
 };
 
@@ -43,6 +45,13 @@ enum TraceEvent : int {
   TR_MMA_P = 0, TR_MMA_DS, TR_MMA_QD2, TR_MMA_DQE,     // MMA thread: after each wait
   TR_PDS_S, TR_PDS_P, TR_PDS_DP, TR_PDS_DS,            // P/dS warps (thread 0)
   TR_DRN_FULL, TR_DRN_DONE,                            // dQ drain (thread 128)
+  // two-pass form, dK/dV pass
+  TR_KV_A, TR_KV_B,                                    // MMA thread after sync A / B
+  TR_KV_S, TR_KV_P, TR_KV_DP, TR_KV_DS,                // compute thread 0
+  // two-pass form, dQ pass
+  TR_Q_SYNC,                                           // MMA thread after its sync
+  TR_Q_S, TR_Q_P, TR_Q_DP, TR_Q_DS,                    // compute thread 0
+  TR_Q_KLOAD,                                          // producer: K_j load issued
   TR_NUM
 };
 Knobs knobs_snapshot();

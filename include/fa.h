@@ -155,7 +155,7 @@ FA_API int fa_debug_set_events(int which /* 0 = forward, 1 = backward */, void* 
 /*
  * Tuning hook: while armed, each fa_bwd main kernel writes a role timeline of
  * CTA 0 (clock64 after each cross-role wait, for its first 512 steps) into
- * trace_dev (device buffer of at least 10*512 int64). NULL disarms.
+ * trace_dev (device buffer of at least 22*512 int64). NULL disarms.
  */
 FA_API int fa_debug_set_trace(void* trace_dev, size_t bytes);
 
