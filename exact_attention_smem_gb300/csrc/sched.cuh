@@ -21,14 +21,26 @@
 // CTAs take the next G units, in CTA order for even r and reversed for odd r,
 // which evens out the per-CTA sums. Every role of a CTA runs its own Walker
 // over the same list, so they agree on the unit sequence without
-// communicating; seeking is amortised O(1) per unit because the list is walked
-// group by group ((cost level, sequence) groups of consecutive row blocks).
+// communicating. Dense layouts seek directly (O(log) per unit, seek_dense);
+// packed layouts walk the list group by group ((cost level, sequence) groups
+// of consecutive row blocks), one step per group passed.
 //
 // Host and device share this code; the host build backs the scheduler tests.
 #pragma once
 #include <cstdint>
 
 namespace fa {
+
+// x / d for x >= 0; a shift when d is a power of two (it always is here: 64,
+// 128 or 256 rows), so the scheduler's arithmetic stays off the divide path.
+__host__ __device__ __forceinline__ int div_nonneg(int x, int d) {
+  if ((d & (d - 1)) == 0) {
+    int sh = 0;
+    while ((1 << sh) < d) ++sh;
+    return x >> sh;
+  }
+  return x / d;
+}
 
 struct SchedSpec {
   const int* cu;   // packed boundaries (nseq + 1), nullptr for dense
@@ -57,24 +69,24 @@ struct SchedSpec {
   // Number of row blocks (units per head) of sequence i.
   __host__ __device__ __forceinline__ int nblocks(int ql, int kl) const {
     const int n = kind == 0 ? ql : kl;
-    return (n + unit_rows - 1) / unit_rows;
+    return div_nonneg(n + unit_rows - 1, unit_rows);
   }
   // Inner blocks walked by row block m.
   __host__ __device__ __forceinline__ int cost(int m, int ql, int kl) const {
     if (kind == 0) {
-      if (!causal) return (kl + inner - 1) / inner;
+      if (!causal) return div_nonneg(kl + inner - 1, inner);
       int last = m * unit_rows + unit_rows;
       last = last < ql ? last : ql;                 // one past the last query row
       int kend = last + (kl - ql);                  // keys visible to that row
       kend = kend < kl ? kend : kl;
-      return kend <= 0 ? 0 : (kend + inner - 1) / inner;
+      return kend <= 0 ? 0 : div_nonneg(kend + inner - 1, inner);
     }
-    const int nq = (ql + inner - 1) / inner;
+    const int nq = div_nonneg(ql + inner - 1, inner);
     if (!causal) return nq;
     int r0 = m * unit_rows - (kl - ql);             // first query row seeing key m*unit_rows
     r0 = r0 > 0 ? r0 : 0;
     if (r0 >= ql) return 0;
-    return nq - r0 / inner;
+    return nq - div_nonneg(r0, inner);
   }
   __host__ __device__ __forceinline__ int max_cost() const {
     int mx = 0;
@@ -167,8 +179,47 @@ struct Walker {
       if (hi > lo) return;
     }
   }
+  // Dense layouts (every sequence has the same lengths): the entry at any list
+  // index follows directly. Inside a head group the list holds, per row block
+  // in order of decreasing cost, nseq x hcount units; so the p-th block in that
+  // order (m = p for the backward, whose cost falls with m; m = nb-1-p for the
+  // forward, whose cost grows with m) fixes the cost level, and the level's
+  // block range fixes sequence, block and head. O(log nb) per call instead of
+  // a walk over every group before the target.
+  __host__ __device__ __forceinline__ bool seek_dense(long long target, Unit& u) const {
+    int qs0, ql, ks0, kl;
+    s.seq(0, qs0, ql, ks0, kl);
+    const int nb = s.nblocks(ql, kl);
+    if (nb == 0 || s.nseq <= 0 || s.heads <= 0 || target < 0) return false;
+    const long long per_head = (long long)nb * s.nseq;
+    const long long full = per_head * s.hblock;
+    const long long hg = target / full;
+    if (hg * s.hblock >= s.heads) return false;
+    const int h0g = (int)(hg * s.hblock);
+    const int hc = s.heads - h0g < s.hblock ? s.heads - h0g : s.hblock;
+    const long long o = target - hg * full;
+    if (o >= per_head * hc) return false;
+    const long long per_block = (long long)s.nseq * hc;
+    const int pos = (int)(o / per_block);
+    const int mp = s.kind == 0 ? nb - 1 - pos : pos;
+    const int c = s.cost(mp, ql, kl);
+    int rlo, rhi;
+    s.range(c, ql, kl, rlo, rhi);
+    const long long r = o - (long long)(s.kind == 0 ? nb - rhi : rlo) * per_block;
+    const long long per_seq = (long long)(rhi - rlo) * hc;
+    const int sq = (int)(r / per_seq);
+    const long long rem = r - (long long)sq * per_seq;
+    u.seq = sq;
+    u.m = rlo + (int)(rem / hc);
+    u.head = h0g + (int)(rem % hc);
+    u.cost = c;
+    s.seq(sq, u.q_start, u.q_len, u.k_start, u.k_len);
+    return true;
+  }
+
   // Position on list entry `target` (targets must not decrease between calls).
   __host__ __device__ __forceinline__ bool seek(long long target, Unit& u) {
+    if (s.cu == nullptr) return seek_dense(target, u);
     while (!done && target >= gstart + (long long)(hi - lo) * hcount) advance_group();
     if (done) return false;
     const long long off = target - gstart;

@@ -21,29 +21,34 @@ def _visible(i, j, ql, kl, causal):
     return j < kl and i < ql and (not causal or j <= i + kl - ql)
 
 
+# kind -> (query-unit rows or key-unit rows, inner block rows, units over queries?)
+_KINDS = {0: (256, 128, True), 1: (128, 64, False), 2: (128, 128, False), 3: (128, 128, True)}
+
+
 def _brute_units(kind, B, cu, Sq, Sk, heads, causal):
+    U, I, over_queries = _KINDS[kind]
     units = {}
     for s, (ql, kl) in enumerate(_seqs(B, cu, Sq, Sk)):
-        if kind == 0:
-            for m in range((ql + 255) // 256):
-                rows = range(m * 256, min(ql, m * 256 + 256))
+        if over_queries:
+            for m in range((ql + U - 1) // U):
+                rows = range(m * U, min(ql, m * U + U))
                 # KV blocks walked: from block 0 up to the last block with a visible key
                 last = -1
-                for jb in range((kl + 127) // 128):
+                for jb in range((kl + I - 1) // I):
                     if any(_visible(i, j, ql, kl, causal) for i in (rows[-1],)
-                           for j in range(jb * 128, min(kl, jb * 128 + 128))):
+                           for j in range(jb * I, min(kl, jb * I + I))):
                         last = jb
                 for h in range(heads):
                     units[(s, m, h)] = last + 1
         else:
-            for n in range((kl + 127) // 128):
-                keys = range(n * 128, min(kl, n * 128 + 128))
+            for n in range((kl + U - 1) // U):
+                keys = range(n * U, min(kl, n * U + U))
                 first = None
-                for ib in range((ql + 63) // 64):
-                    if any(_visible(i, keys[0], ql, kl, causal) for i in range(ib * 64, min(ql, ib * 64 + 64))):
+                for ib in range((ql + I - 1) // I):
+                    if any(_visible(i, keys[0], ql, kl, causal) for i in range(ib * I, min(ql, ib * I + I))):
                         first = ib
                         break
-                c = 0 if first is None else (ql + 63) // 64 - first
+                c = 0 if first is None else (ql + I - 1) // I - first
                 for h in range(heads):
                     units[(s, n, h)] = c
     return units
@@ -55,6 +60,10 @@ CASES = [
     (0, 4, [0, 1, 1, 700, 3000], 3000, 3000, 2, True), (0, 3, [0, 129, 385, 1000], 1000, 1000, 4, False),
     (1, 2, None, 600, 600, 3, True), (1, 2, None, 600, 600, 3, False), (1, 1, None, 300, 1000, 2, True),
     (1, 1, None, 1000, 300, 2, True), (1, 4, [0, 1, 1, 700, 3000], 3000, 3000, 2, True),
+    (2, 2, None, 600, 600, 3, True), (2, 2, None, 600, 600, 3, False), (2, 1, None, 300, 1000, 2, True),
+    (2, 1, None, 1000, 300, 2, True), (2, 4, [0, 1, 1, 700, 3000], 3000, 3000, 2, True),
+    (3, 2, None, 600, 600, 3, True), (3, 2, None, 600, 600, 3, False), (3, 1, None, 300, 1000, 2, True),
+    (3, 1, None, 1000, 300, 2, True), (3, 3, [0, 129, 385, 1000], 1000, 1000, 4, True),
 ]
 
 
@@ -109,7 +118,8 @@ def test_auto_group_covers_the_grid():
 def test_causal_balance_near_lpt_bound():
     """Long causal batch: per-CTA total cost within a few percent of the mean."""
     G = 152
-    for kind, hpg in ((0, 32), (1, 0)):     # the kernels' choices: fwd one group, bwd auto
+    # the kernels' choices: forward and dQ pass one group, dK/dV pass and one-pass auto
+    for kind, hpg in ((0, 32), (1, 0), (2, 0), (3, 32)):
         loads = [sum(u[3] for u in fa_sched_list(kind, 1, None, 32768, 32768, 32, True, G, b, hpg))
                  for b in range(G)]
         mean = sum(loads) / G
