@@ -318,7 +318,12 @@ extern "C" int fa_bwd(const void* q, const void* k, const void* v, const void* o
   int grid = kn.grid_override > 0 ? kn.grid_override : di->sms;
   const long long kv_units_per_head =
       sh.packed ? (sh.Tk + 127) / 128 + B : (long long)B * ((Sk + 127) / 128);
-  p.hblock = pick_hblock(kv_units_per_head, Hkv, grid);
+  // Head groups keep the data concurrently running units share in L2. Packed
+  // layouts use one group in the two-pass form: their scheduler walks the
+  // list one (cost level, sequence) group at a time, so head groups of one
+  // head would multiply that walk by the head count (dense layouts seek
+  // directly and keep the L2-sized groups).
+  p.hblock = (mode != 0 && sh.packed) ? Hkv : pick_hblock(kv_units_per_head, Hkv, grid);
   // dQ units (128 query rows of one head) walk K/V like the forward: one LPT group.
   const long long q_units_per_head =
       sh.packed ? (sh.Tq + 127) / 128 + B : (long long)B * ((Sq + 127) / 128);
