@@ -324,10 +324,15 @@ extern "C" int fa_bwd(const void* q, const void* k, const void* v, const void* o
   // head would multiply that walk by the head count (dense layouts seek
   // directly and keep the L2-sized groups).
   p.hblock = (mode != 0 && sh.packed) ? Hkv : pick_hblock(kv_units_per_head, Hkv, grid);
-  // dQ units (128 query rows of one head) walk K/V like the forward: one LPT group.
+  // dQ units (128 query rows of one head) stream the K/V of their head. When
+  // the K/V of all heads would not stay in L2 (GB300: 129 MB) a dense layout
+  // takes the fewest heads whose units cover the grid twice (one group over
+  // 32 heads of S=32768 re-read K/V from DRAM about 14 times); otherwise, and
+  // for packed layouts (see above), one group balances best.
   const long long q_units_per_head =
       sh.packed ? (sh.Tq + 127) / 128 + B : (long long)B * ((Sq + 127) / 128);
-  p.hblock_q = Hq;
+  const double kv_bytes = (double)sh.Tk * Hkv * d * 4.0;
+  p.hblock_q = (sh.packed || kv_bytes <= 96e6) ? Hq : pick_hblock(q_units_per_head, Hq, 2 * grid);
   int grid_q = kn.grid_override > 0 ? kn.grid_override : di->sms;
   if (mode != 0) {
     const long long kv_units = kv_units_per_head * Hkv, q_units = q_units_per_head * Hq;
