@@ -21,6 +21,8 @@ cudaError_t launch_mma_probe(const __nv_bfloat16* A, const __nv_bfloat16* B, flo
                              int N, cudaStream_t st);
 cudaError_t launch_wait_timeout_probe(int* status, unsigned long long timeout_ns,
                                       cudaStream_t st);
+cudaError_t launch_mma_pair_probe(const __nv_bfloat16* A, const __nv_bfloat16* B, float* C,
+                                  int* flags, int mode, int N, cudaStream_t st);
 cudaError_t launch_micro(int kind, int iters, double* out, int ctas, cudaStream_t st);
 
 __device__ int g_error_word;  // first expired bounded wait (site code), per device
@@ -452,6 +454,19 @@ extern "C" int fa_test_mma(const void* A, const void* B, float* C, int mode, int
   cudaError_t e = launch_mma_probe(static_cast<const __nv_bfloat16*>(A),
                                    static_cast<const __nv_bfloat16*>(B), C, mode, N,
                                    static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : fail(FA_ERR_CUDA, "%s", cudaGetErrorString(e));
+}
+
+extern "C" int fa_test_mma_pair(const void* A, const void* B, float* C, int* flags, int mode,
+                                int N, void* stream) {
+  if (!A || !B || !C || !flags || (mode != 0 && mode != 1) || N != 128)
+    return fail(FA_ERR_INVALID_ARG, "fa_test_mma_pair arguments");
+  DevInfo* di = nullptr;
+  int st = device_info(&di);
+  if (st != FA_OK) return st;
+  cudaError_t e = launch_mma_pair_probe(static_cast<const __nv_bfloat16*>(A),
+                                        static_cast<const __nv_bfloat16*>(B), C, flags, mode, N,
+                                        static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : fail(FA_ERR_CUDA, "%s", cudaGetErrorString(e));
 }
 

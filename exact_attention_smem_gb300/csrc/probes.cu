@@ -143,6 +143,122 @@ cudaError_t launch_mma_probe(const __nv_bfloat16* A, const __nv_bfloat16* B, flo
   return cudaGetLastError();
 }
 
+// CTA-pair (cta_group::2) MMA probe: a cluster of two CTAs computes
+//   mode 0: C[256][N] = A[256][128] * B[N][128]^T   (A, B K-major in shared memory)
+//   mode 1: C[256][N] = A[256][128] * B[128][N]     (A from TMEM, B MN-major)
+// with M=256 MMAs issued by CTA 0. CTA r holds A rows [128r, 128r+128) and B's
+// N columns [r*N/2, (r+1)*N/2); its TMEM receives C rows [128r, 128r+128).
+// flags[r] = 1 if CTA r saw its MMAs complete; flags[2 + r] = its TMEM base.
+// TMEM (256 columns): A in [0, 64) for mode 1, C in [128, 128 + N), N = 128.
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(128, 1)
+    mma_pair_probe_kernel(const __nv_bfloat16* A, const __nv_bfloat16* B, float* C, int* flags,
+                          int mode, int N, int* err) {
+  extern __shared__ __align__(1024) uint8_t smem_pp[];
+  const uint32_t base = smem_u32(smem_pp);
+  uint8_t* smem = smem_pp;
+  const uint32_t a_s = base, b_s = base + 32768;
+  const uint32_t bar = base + 65536;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + 65536 + 64);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 65536 + 72);
+  const int warp = threadIdx.x >> 5, tid = threadIdx.x;
+  const int rank = (int)cluster_ctarank();
+  const int nh = N / 2;
+  for (int i = tid; i < 128 * 128; i += 128) {
+    const int r = i >> 7, c = i & 127;
+    *reinterpret_cast<__nv_bfloat16*>(smem + sw128_offset(r, c, 128)) = A[(rank * 128 + r) * 128 + c];
+  }
+  if (mode == 0) {
+    for (int i = tid; i < nh * 128; i += 128) {                 // B rows [rank*nh, +nh), K-major
+      const int r = i >> 7, c = i & 127;
+      *reinterpret_cast<__nv_bfloat16*>(smem + 32768 + sw128_offset(r, c, nh)) =
+          B[(rank * nh + r) * 128 + c];
+    }
+  } else {
+    for (int i = tid; i < 128 * nh; i += 128) {                 // B columns [rank*nh, +nh), MN-major
+      const int r = i / nh, c = i % nh;
+      *reinterpret_cast<__nv_bfloat16*>(smem + 32768 + sw128_offset(r, c, 128)) =
+          B[r * N + rank * nh + c];
+    }
+  }
+  if (tid == 0) {
+    mbar_init(bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc_pair(smem_u32(tmem_slot), 256);
+    tmem_relinquish_pair();
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+  if (mode == 1) {                                              // A rows into TMEM columns [0, 64)
+    uint32_t pk[32];
+    for (int half = 0; half < 2; ++half) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const int c = half * 64 + 2 * j;
+        const int row = rank * 128 + tid;
+        pk[j] = pack_bf16x2(__bfloat162float(A[row * 128 + c]), __bfloat162float(A[row * 128 + c + 1]));
+      }
+      tmem_st32(tmem + lane_off + half * 32, pk);
+    }
+    tmem_st_wait();
+  }
+  tc_fence_before();
+  cluster_sync_all();                                           // both CTAs' operands in place
+  tc_fence_after();
+  const uint32_t d_tm = tmem + 128;
+  if (rank == 0 && tid == 0) {
+    for (int kk = 0; kk < 8; ++kk) {
+      if (mode == 0) {
+        const uint32_t off = (kk >> 2) * (128 * 128) + (kk & 3) * 32;
+        const uint32_t boff = (kk >> 2) * (nh * 128) + (kk & 3) * 32;
+        mma_ss_pair(d_tm, sdesc_sw128(a_s + off, 128 * 128, 1024),
+                    sdesc_sw128(b_s + boff, nh * 128, 1024), idesc_bf16(256, N, false, false),
+                    kk > 0);
+      } else {
+        mma_ts_pair(d_tm, tmem + kk * 8, sdesc_sw128(b_s + kk * 2048, 128 * 128, 1024),
+                    idesc_bf16(256, N, false, true), kk > 0);
+      }
+    }
+    tc_commit_pair(bar, 0x3);
+  }
+  const WaitCtl wc{err, abort_flag, 1000000000ull};
+  const bool ok = mbar_wait(bar, 0, wc, SITE_TEST);
+  tc_fence_after();
+  if (ok) {
+    for (int c = 0; c < N; c += 32) {
+      uint32_t v[32];
+      tmem_ld32(tmem + lane_off + 128 + c, v);
+      for (int i = 0; i < 32; ++i) C[(rank * 128 + tid) * N + c + i] = __uint_as_float(v[i]);
+    }
+  }
+  if (tid == 0) {
+    flags[rank] = ok ? 1 : 0;
+    flags[2 + rank] = (int)tmem;
+  }
+  tc_fence_before();
+  cluster_sync_all();                                           // no CTA frees TMEM its peer still uses
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, 256);
+  }
+}
+
+cudaError_t launch_mma_pair_probe(const __nv_bfloat16* A, const __nv_bfloat16* B, float* C,
+                                  int* flags, int mode, int N, cudaStream_t st) {
+  const int smem = 65536 + 128;
+  cudaError_t e = cudaFuncSetAttribute(mma_pair_probe_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  mma_pair_probe_kernel<<<2, 128, smem, st>>>(A, B, C, flags, mode, N, device_error_word());
+  return cudaGetLastError();
+}
+
 // A wait on a barrier that nothing ever arrives on: must return through the
 // timeout path, recording SITE_TEST in the error word and `status[0] = 1`.
 __global__ void wait_timeout_probe_kernel(int* status, int* err, unsigned long long timeout_ns) {

@@ -203,6 +203,17 @@ FA_API float fa_exp2_poly_host(float x);
 FA_API int fa_test_mma(const void* A, const void* B, float* C, int mode, int N, void* stream);
 
 /*
+ * CTA-pair (cta_group::2) tcgen05 MMA probe: a cluster of two CTAs computes
+ * C[256][N] (fp32), N = 128, with M=256 MMAs issued by CTA 0; CTA r
+ * holds A rows [128r, 128r+128) and B's N columns [r*N/2, (r+1)*N/2).
+ *   mode 0: C = A[256][128] * B[N][128]^T   mode 1: C = A * B[128][N] (A via TMEM)
+ * flags (device, 4 ints): [r] = 1 if CTA r saw the MMAs complete, [2+r] = its
+ * TMEM base address (equal in both CTAs).
+ */
+FA_API int fa_test_mma_pair(const void* A, const void* B, float* C, int* flags, int mode, int N,
+                            void* stream);
+
+/*
  * Runs a kernel whose bounded wait can never complete; *status_dev (device
  * int) becomes 1 when the wait timed out as designed. Leaves the site code in
  * the device error word (clear it with fa_get_device_error(&c, 1)).

@@ -61,6 +61,26 @@ def test_mma_probe(mode, N):
     assert np.abs(got - want).max() <= 1e-3 * max(1.0, np.abs(want).max())
 
 
+@pytest.mark.parametrize("N", [128])
+@pytest.mark.parametrize("mode", [0, 1])
+def test_mma_pair_probe(mode, N):
+    """cta_group::2: one M=256 MMA chain over a cluster of two CTAs."""
+    g = torch.Generator().manual_seed(200 + mode * 7 + N)
+    A = torch.randn(256, 128, generator=g).to(torch.bfloat16)
+    B = torch.randn(*((N, 128) if mode == 0 else (128, N)), generator=g).to(torch.bfloat16)
+    C = torch.full((256, N), float("nan"), device="cuda")
+    flags = torch.zeros(4, dtype=torch.int32, device="cuda")
+    fa.fa_test_mma_pair(A.cuda(), B.cuda(), C, flags, mode, N)
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_error(clear=True) == 0
+    f = flags.cpu().tolist()
+    assert f[0] == 1 and f[1] == 1 and f[2] == f[3], f
+    a, b = A.double().numpy(), B.double().numpy()
+    want = a @ b.T if mode == 0 else a @ b
+    got = C.cpu().double().numpy()
+    assert np.abs(got - want).max() <= 1e-3 * max(1.0, np.abs(want).max())
+
+
 def test_bounded_wait_times_out_instead_of_hanging():
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     fa.fa_test_wait_timeout(status, 50.0)
