@@ -266,7 +266,7 @@ extern "C" int fa_bwd(const void* q, const void* k, const void* v, const void* o
   if ((st = device_info(&di)) != FA_OK) return st;
   const Knobs kn = knobs_snapshot();
 
-  const int mode = kn.bwd_mode;
+  const int mode = (kn.bwd_mode == 2 && d != 128) ? 1 : kn.bwd_mode;
   if (mode == 0 && d != 128)
     return fail(FA_ERR_UNSUPPORTED, "the one-pass backward supports head dim 128 only");
   BwdParams p;
@@ -285,6 +285,14 @@ extern "C" int fa_bwd(const void* q, const void* k, const void* v, const void* o
   if ((st = encode_rows(&p.tm_v, sh.Tk > 0 ? v : q, sh.Tk > 0 ? Tk : Tq, sh.Tk > 0 ? Hkv : Hq,
                         d)) != FA_OK)
     return st;
+  if (mode == 2) {
+    if ((st = encode_rows(&p.tm_q2, sh.Tq > 0 ? q : k, sh.Tq > 0 ? Tq : Tk, sh.Tq > 0 ? Hq : Hkv,
+                          d, 64)) != FA_OK)
+      return st;
+    if ((st = encode_rows(&p.tm_do2, sh.Tq > 0 ? dout : k, sh.Tq > 0 ? Tq : Tk,
+                          sh.Tq > 0 ? Hq : Hkv, d, 64)) != FA_OK)
+      return st;
+  }
   auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
   char* ws = static_cast<char*>(workspace);
   const size_t T = (size_t)sh.Tq;
@@ -341,6 +349,21 @@ extern "C" int fa_bwd(const void* q, const void* k, const void* v, const void* o
     if (kv_units < grid) grid = (int)(kv_units > 0 ? kv_units : 1);
     if (q_units < grid_q) grid_q = (int)(q_units > 0 ? q_units : 1);
   }
+  if (mode == 2) {
+    // dK/dV units of 256 keys on CTA pairs: a grid of pairs that can all be
+    // resident at once (a persistent grid must never wait for a pair slot)
+    const long long pair_units_per_head =
+        sh.packed ? (sh.Tk + 255) / 256 + B : (long long)B * ((Sk + 255) / 256);
+    int pairs = (kn.grid_override > 0 ? kn.grid_override : di->sms) / 2;
+    const int maxc = dkdv_pair_max_clusters();
+    if (maxc <= 0) return fail(FA_ERR_CUDA, "no CTA pair of the dK/dV kernel fits on this GPU");
+    if (pairs > maxc) pairs = maxc;
+    const long long pair_units = pair_units_per_head * Hkv;
+    if (pair_units < pairs) pairs = (int)(pair_units > 0 ? pair_units : 1);
+    if (pairs < 1) pairs = 1;
+    grid = 2 * pairs;
+    p.hblock = sh.packed ? Hkv : pick_hblock(pair_units_per_head, Hkv, pairs);
+  }
   cudaError_t e = launch_bwd(p, aux, d, grid, grid_q, static_cast<cudaStream_t>(stream),
                              kn.bwd_poly8, mode);
   if (e == cudaErrorNotSupported)
@@ -390,7 +413,8 @@ extern "C" int fa_debug_set(const char* key, double value) {
     if (v != 0 && v != 2 && v != 4) return fail(FA_ERR_INVALID_ARG, "poly8 in {0, 2, 4}");
     (key[0] == 'p' ? g_knobs.poly8 : g_knobs.bwd_poly8) = v;
   } else if (!strcmp(key, "bwd_mode")) {
-    if (value != 0.0 && value != 1.0) return fail(FA_ERR_INVALID_ARG, "bwd_mode in {0, 1}");
+    if (value != 0.0 && value != 1.0 && value != 2.0)
+      return fail(FA_ERR_INVALID_ARG, "bwd_mode in {0, 1, 2}");
     g_knobs.bwd_mode = (int)value;
   } else if (!strcmp(key, "timeout_ms")) {
     if (!(value >= 1.0 && value <= 60000.0)) return fail(FA_ERR_INVALID_ARG, "timeout_ms");
@@ -484,12 +508,12 @@ extern "C" int fa_test_wait_timeout(int* status_dev, double timeout_ms, void* st
 extern "C" int fa_sched_list(int kind, int B, const int* cu_seqlens_host, int Sq, int Sk,
                              int heads, int causal, int grid, int cta, int heads_per_group,
                              int* out, int max_units) {
-  if (kind < 0 || kind > 3 || B < 0 || Sq < 0 || Sk < 0 || heads <= 0 || grid <= 0 ||
+  if (kind < 0 || kind > 4 || B < 0 || Sq < 0 || Sk < 0 || heads <= 0 || grid <= 0 ||
       cta < 0 || cta >= grid || heads_per_group < 0 || max_units < 0 || (max_units > 0 && !out))
     return -1;
-  // kind: 0 forward, 1 one-pass backward, 2 dK/dV pass, 3 dQ pass
-  static const int kUnit[4] = {256, 128, 128, 128}, kInner[4] = {128, 64, 128, 128},
-                   kList[4] = {0, 1, 1, 0};
+  // kind: 0 forward, 1 one-pass backward, 2 dK/dV pass, 3 dQ pass, 4 dK/dV pass on CTA pairs
+  static const int kUnit[5] = {256, 128, 128, 128, 256}, kInner[5] = {128, 64, 128, 128, 128},
+                   kList[5] = {0, 1, 1, 0, 1};
   SchedSpec s{cu_seqlens_host, B, Sq, Sk, heads, causal ? 1 : 0, kUnit[kind], kInner[kind],
               kList[kind], heads_per_group};
   if (heads_per_group == 0) {

@@ -717,8 +717,11 @@ cudaError_t launch_bwd(const BwdParams& p, const BwdAux& aux, int d, int grid, i
     cudaEvent_t ev0, ev1;
     take_events(1, &ev0, &ev1);
     if (ev0) cudaEventRecord(ev0, stream);
-    const cudaError_t e = launch_bwd_split(p, d, p.total_k > 0 ? grid : 0,
-                                           p.total_q > 0 ? grid_q : 0, stream, poly8);
+    const cudaError_t e =
+        mode == 2 ? launch_bwd_pair(p, p.total_k > 0 ? grid : 0, p.total_q > 0 ? grid_q : 0,
+                                    stream, poly8)
+                  : launch_bwd_split(p, d, p.total_k > 0 ? grid : 0, p.total_q > 0 ? grid_q : 0,
+                                     stream, poly8);
     if (ev1) cudaEventRecord(ev1, stream);
     return e;
   }

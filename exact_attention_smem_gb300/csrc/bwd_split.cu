@@ -596,6 +596,460 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dkdv_kernel(const __grid_const
 #undef BAR
 }
 
+// ============================================================== dK/dV pass, CTA pairs
+// The same pass with each unit's MMAs issued over a cluster of two CTAs
+// (cta_group::2, M = 256). A unit is 256 keys; CTA r of the pair owns keys
+// [128r, 128r+128): its K/V tiles, its TMEM accumulators and its P^T/dS^T
+// columns. The step's Q and dO tiles are split the way each M=256 MMA takes
+// its B operand: S^T and dP^T read query rows [64r, 64r+64) (all head-dim
+// columns, K-major) from CTA r, dV and dK read head-dim columns [64r, 64r+64)
+// of all 128 query rows (MN-major) from CTA r. Each CTA thus reads half of
+// every B operand from its own shared memory, the traffic that bounds the
+// one-CTA form. CTA 0 issues every MMA; CTA 1's TMA completions (forwarded
+// by its warp 10) and its P^T/dS^T readiness reach CTA 0's barriers as remote
+// arrivals, and CTA 0's commits are multicast to both CTAs.
+// A Q/dO slot holds [rows half: two 64-row x 128-byte chunks][columns half:
+// one 128-row x 128-byte chunk], 32 KB, the same size as in the one-CTA form.
+constexpr int PAIR_BN = 256;     // keys per unit (two CTAs)
+
+// X (TMEM, 256 keys x 128 q over the pair) = K/V tile (this CTA's 128 rows,
+// K-major) * (64 rows of this CTA's half of B, K-major)^T
+template <uint32_t IDESC>
+__device__ __forceinline__ void mma_abt_pair(uint32_t tm, uint32_t a, uint32_t b) {
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) {
+    const uint32_t a_off = (kk >> 2) * (128 * 128) + (kk & 3) * 32;
+    const uint32_t b_off = (kk >> 2) * (64 * 128) + (kk & 3) * 32;
+    mma_ss_pair(tm, sdesc_sw128(a + a_off, 128 * 128, 1024), sdesc_sw128(b + b_off, 64 * 128, 1024),
+                IDESC, kk > 0 ? 1u : 0u);
+  }
+}
+// Acc (TMEM, 256 keys x 128 over the pair) (+)= X (TMEM bf16, columns [0,32)
+// and [64,96)) * Y (128 q rows x this CTA's 64 head-dim columns, MN-major)
+template <uint32_t IDESC>
+__device__ __forceinline__ void mma_acc_pair(uint32_t tm_acc, uint32_t tm_x, uint32_t y, bool acc) {
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) {
+    const uint32_t ta = tm_x + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8);
+    mma_ts_pair(tm_acc, ta, sdesc_sw128(y + kk * 2048, 128 * 128, 1024), IDESC,
+                (acc || kk > 0) ? 1u : 0u);
+  }
+}
+
+__device__ __forceinline__ int first_qblock_pair(const Unit& u, int causal) {
+  if (!causal) return 0;
+  int r0 = u.m * PAIR_BN - (u.k_len - u.q_len);
+  r0 = r0 > 0 ? r0 : 0;
+  return r0 / BM;
+}
+
+template <int POLY8>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
+    dkdv_pair_kernel(const __grid_constant__ BwdParams p) {
+  constexpr int D = 128;
+  using C = CfgKV<D>;
+  using T = Tile<D>;
+  constexpr uint32_t IDESC_S2 = idesc_bf16(256, 128, false, false);   // S^T, dP^T
+  constexpr uint32_t IDESC_ACC2 = idesc_bf16(256, D, false, true);    // dV, dK
+  constexpr uint32_t ROWS_HALF = 0, COLS_HALF = 2 * 64 * 128;         // offsets inside a slot
+  extern __shared__ __align__(1024) uint8_t smem_al[];
+  uint32_t base;                                        // opaque to the compiler: checked, not assumed
+  asm volatile("{\n\t.reg .u64 t;\n\tcvta.to.shared.u64 t, %1;\n\tcvt.u32.u64 %0, t;\n\t}"
+               : "=r"(base)
+               : "l"(smem_al));
+  if (base & 1023u) {                                   // same in both CTAs of the pair
+    if (threadIdx.x == 0) atomicCAS(p.err, 0, SITE_SMEM_ALIGN);
+    return;
+  }
+  uint8_t* smem = smem_al;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const uint32_t bars = base + C::BAR_OFF;
+#define BAR(i) (bars + 8u * (uint32_t)(i))
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::MISC_OFF);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
+  int* cu_s = reinterpret_cast<int*>(smem + C::CU_OFF);
+
+  if (threadIdx.x == 0) {
+    // CTA 0's full barriers also count CTA 1's forwarded completion
+    const uint32_t fulls = leader ? 2 : 1;
+    mbar_init(BAR(C::B_KVFULL), fulls);
+    mbar_init(BAR(C::B_KVEMPTY), 1);
+    for (int s = 0; s < C::NQ; ++s) {
+      mbar_init(BAR(C::B_QFULL + s), fulls);
+      mbar_init(BAR(C::B_QEMPTY + s), 1);
+    }
+    for (int s = 0; s < C::NDO; ++s) {
+      mbar_init(BAR(C::B_DOFULL + s), fulls);
+      mbar_init(BAR(C::B_DOEMPTY + s), 1);
+    }
+    for (int s = 0; s < C::NLD; ++s) {
+      mbar_init(BAR(C::B_LDFULL + s), 1);
+      mbar_init(BAR(C::B_LDEMPTY + s), 256);
+    }
+    mbar_init(BAR(C::B_SFULL), 1);
+    mbar_init(BAR(C::B_DPFULL), 1);
+    mbar_init(BAR(C::B_PREADY), 512);                  // 16 warps of the pair, 32 each
+    mbar_init(BAR(C::B_DSREADY), 512);
+    mbar_init(BAR(C::B_ACCFULL), 1);
+    mbar_init(BAR(C::B_DRAIN), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == TMA_WARP && lane == 0) {
+    tma_prefetch_desc(&p.tm_q);
+    tma_prefetch_desc(&p.tm_q2);
+    tma_prefetch_desc(&p.tm_do);
+    tma_prefetch_desc(&p.tm_do2);
+    tma_prefetch_desc(&p.tm_k);
+    tma_prefetch_desc(&p.tm_v);
+  }
+  if (warp == MMA_WARP) {
+    tmem_alloc_pair(smem_u32(tmem_slot), 512);
+    tmem_relinquish_pair();
+  }
+  const bool cu_in_smem = p.cu != nullptr && p.nseq <= MAX_SEQ_SMEM;
+  if (cu_in_smem)
+    for (int i = threadIdx.x; i <= p.nseq; i += NUM_THREADS) cu_s[i] = p.cu[i];
+  tc_fence_before();
+  cluster_sync_all();                                   // both CTAs' barriers exist before any remote arrival
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  const SchedSpec spec{cu_in_smem ? cu_s : p.cu, p.nseq, p.Sq, p.Sk, p.Hkv, p.causal, PAIR_BN, BM,
+                       1, p.hblock};
+  const WaitCtl wc{p.err, abort_flag, p.timeout_ns};
+  const int G = gridDim.x / 2;                          // pairs
+  const int cta = blockIdx.x / 2;                       // this pair
+  const int group = p.Hq / p.Hkv;
+
+  if (warp >= 8) {
+    regs_dec<REGS_CONTROL>();
+  if (warp == 11) {
+    // spare warp of the control warpgroup
+  } else if (warp == 10) {
+    // ------------------------------------------------------------ forwarder
+    // CTA 1: each of its K/V, Q and dO copies, once landed, counts on CTA 0's
+    // barrier of the same slot (same order as the producer issues them).
+    if (!leader && lane == 0) {
+      Walker w;
+      w.init(spec);
+      int u_it = 0;
+      bool ok = true;
+      uint32_t nq = 0, nd = 0;
+      for (int k = 0; ok; ++k) {
+        Unit u;
+        if (!w.seek(snake_index(k, G, cta), u)) break;
+        if (u.cost == 0) continue;
+        const int n = u.cost * group;
+        const int lead = n < 2 ? n : 2;
+        for (int i = 0; i <= n; ++i) {
+          if (i == lead) {
+            ok = mbar_wait(BAR(C::B_KVFULL), u_it & 1, wc, SITE_DKDV_KV_FULL);
+            if (!ok) break;
+            mbar_arrive_cluster(BAR(C::B_KVFULL), 0, 1);
+            ++u_it;
+          }
+          if (i == n) break;
+          ok = mbar_wait(BAR(C::B_QFULL + nq % C::NQ), (nq / C::NQ) & 1, wc, SITE_DKDV_Q_FULL);
+          if (!ok) break;
+          mbar_arrive_cluster(BAR(C::B_QFULL + nq % C::NQ), 0, 1);
+          ++nq;
+          ok = mbar_wait(BAR(C::B_DOFULL + nd % C::NDO), (nd / C::NDO) & 1, wc, SITE_DKDV_DO_FULL);
+          if (!ok) break;
+          mbar_arrive_cluster(BAR(C::B_DOFULL + nd % C::NDO), 0, 1);
+          ++nd;
+        }
+      }
+    }
+  } else if (warp == TMA_WARP) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      Walker w;
+      w.init(spec);
+      int u_it = 0;
+      bool ok = true;
+      uint32_t nq = 0, nd = 0, nl = 0;                    // Q / dO / row-value loads issued
+      for (int k = 0; ok; ++k) {
+        Unit u;
+        if (!w.seek(snake_index(k, G, cta), u)) break;
+        if (u.cost == 0) continue;
+        const int n = u.cost * group;
+        const int m_first = first_qblock_pair(u, p.causal);
+        const int lead = n < 2 ? n : 2;
+        for (int i = 0; i <= n; ++i) {
+          if (i == lead) {
+            if (u_it > 0) {
+              ok = mbar_wait_cl(BAR(C::B_KVEMPTY), (u_it - 1) & 1, wc, SITE_DKDV_KV_EMPTY);
+              if (!ok) break;
+            }
+            mbar_arrive_expect_tx(BAR(C::B_KVFULL), 2 * T::BYTES);
+            const int krow = u.k_start + u.m * PAIR_BN + 128 * (int)rank;
+            for (int c = 0; c < T::CHUNKS; ++c) {
+              tma_load_3d(base + C::K_OFF + c * T::CHUNK, &p.tm_k, BAR(C::B_KVFULL), c * 64,
+                          u.head, krow);
+              tma_load_3d(base + C::V_OFF + c * T::CHUNK, &p.tm_v, BAR(C::B_KVFULL), c * 64,
+                          u.head, krow);
+            }
+            ++u_it;
+          }
+          if (i == n) break;
+          const StepInfo st = step_of(i, u.cost, m_first, u.head, group);
+          const int row = u.q_start + st.m * BM;
+          const int sq = nq % C::NQ, sd = nd % C::NDO;
+          if (nq >= (uint32_t)C::NQ) {
+            ok = mbar_wait_cl(BAR(C::B_QEMPTY + sq), ((nq / C::NQ) - 1) & 1, wc, SITE_DKDV_Q_EMPTY);
+            if (!ok) break;
+          }
+          {
+            const uint32_t slot = base + C::Q_OFF + sq * T::BYTES, bq = BAR(C::B_QFULL + sq);
+            mbar_arrive_expect_tx(bq, T::BYTES);
+            for (int c = 0; c < 2; ++c)                   // rows [64r, 64r+64), all columns
+              tma_load_3d(slot + ROWS_HALF + c * (64 * 128), &p.tm_q2, bq, c * 64, st.h,
+                          row + 64 * (int)rank);
+            tma_load_3d(slot + COLS_HALF, &p.tm_q, bq, 64 * (int)rank, st.h, row);  // columns half
+          }
+          ++nq;
+          if (nd >= (uint32_t)C::NDO) {
+            ok = mbar_wait_cl(BAR(C::B_DOEMPTY + sd), ((nd / C::NDO) - 1) & 1, wc,
+                              SITE_DKDV_DO_EMPTY);
+            if (!ok) break;
+          }
+          {
+            const uint32_t slot = base + C::DO_OFF + sd * T::BYTES, bd = BAR(C::B_DOFULL + sd);
+            mbar_arrive_expect_tx(bd, T::BYTES);
+            for (int c = 0; c < 2; ++c)
+              tma_load_3d(slot + ROWS_HALF + c * (64 * 128), &p.tm_do2, bd, c * 64, st.h,
+                          row + 64 * (int)rank);
+            tma_load_3d(slot + COLS_HALF, &p.tm_do, bd, 64 * (int)rank, st.h, row);
+          }
+          ++nd;
+          const int sl = nl % C::NLD;
+          if (nl >= (uint32_t)C::NLD) {
+            ok = mbar_wait(BAR(C::B_LDEMPTY + sl), ((nl / C::NLD) - 1) & 1, wc,
+                           SITE_DKDV_LD_EMPTY);
+            if (!ok) break;
+          }
+          const long long off = (long long)st.h * p.pad_hstride + pad_start(u.seq, u.q_start) +
+                                (long long)st.m * BM;
+          const uint32_t ld = base + C::LD_OFF + sl * C::LD_BYTES;
+          mbar_arrive_expect_tx(BAR(C::B_LDFULL + sl), C::LD_BYTES);
+          bulk_load(ld, p.lse2 + off, BM * 4, BAR(C::B_LDFULL + sl));
+          bulk_load(ld + BM * 4, p.delta + off, BM * 4, BAR(C::B_LDFULL + sl));
+          ++nl;
+        }
+      }
+      if (!ok) {
+        for (uint32_t i = nq > (uint32_t)C::NQ ? nq - C::NQ : 0; i < nq; ++i)
+          drain_wait(BAR(C::B_QFULL + i % C::NQ), (i / C::NQ) & 1, 100000000ull);
+        for (uint32_t i = nd > (uint32_t)C::NDO ? nd - C::NDO : 0; i < nd; ++i)
+          drain_wait(BAR(C::B_DOFULL + i % C::NDO), (i / C::NDO) & 1, 100000000ull);
+        for (uint32_t i = nl > (uint32_t)C::NLD ? nl - C::NLD : 0; i < nl; ++i)
+          drain_wait(BAR(C::B_LDFULL + i % C::NLD), (i / C::NLD) & 1, 100000000ull);
+        if (u_it > 0) drain_wait(BAR(C::B_KVFULL), (u_it - 1) & 1, 100000000ull);
+      }
+    }
+  } else if (warp == MMA_WARP) {
+    // ------------------------------------------------------------ MMA issue (CTA 0)
+    if (leader && lane == 0) {
+      Walker w;
+      w.init(spec);
+      uint32_t it = 0;
+      int u_it = 0;
+      bool ok = true;
+      const uint32_t kt = base + C::K_OFF, vt = base + C::V_OFF;
+      const uint32_t tSB = tmem + C::TM_SB, tDB = tmem + C::TM_DB;
+      auto qslot = [&](uint32_t s) { return base + C::Q_OFF + (s % C::NQ) * T::BYTES; };
+      auto dslot = [&](uint32_t s) { return base + C::DO_OFF + (s % C::NDO) * T::BYTES; };
+      for (int k = 0; ok; ++k) {
+        Unit u;
+        if (!w.seek(snake_index(k, G, cta), u)) break;
+        if (u.cost == 0) continue;
+        const int n = u.cost * group;
+        // Same schedule as the one-CTA form (sync points A and B per step),
+        // with pair MMAs and commits multicast to both CTAs.
+        ok = mbar_wait3_cl(BAR(C::B_KVFULL), u_it & 1, SITE_DKDV_KV_FULL,
+                           BAR(C::B_QFULL + it % C::NQ), (it / C::NQ) & 1, SITE_DKDV_Q_FULL,
+                           BAR(C::B_DOFULL + it % C::NDO), (it / C::NDO) & 1, SITE_DKDV_DO_FULL,
+                           wc);
+        if (!ok) break;
+        tc_fence_after();
+        mma_abt_pair<IDESC_S2>(tSB, kt, qslot(it) + ROWS_HALF);
+        tc_commit_pair(BAR(C::B_SFULL), 0x3);
+        mma_abt_pair<IDESC_S2>(tDB, vt, dslot(it) + ROWS_HALF);
+        tc_commit_pair(BAR(C::B_DPFULL), 0x3);
+        for (int i = 0; i < n && ok; ++i, ++it) {
+          const bool more = i + 1 < n;
+          const uint32_t it1 = it + 1;
+          ok = mbar_wait3_cl(BAR(C::B_PREADY), it & 1, SITE_DKDV_P_READY,
+                             more ? BAR(C::B_QFULL + it1 % C::NQ) : BAR(C::B_PREADY),
+                             more ? (it1 / C::NQ) & 1 : it & 1, SITE_DKDV_Q_FULL,
+                             BAR(C::B_PREADY), it & 1, SITE_DKDV_P_READY, wc);
+          if (!ok) break;
+          FA_TRACE(TR_KV_A, it);
+          tc_fence_after();
+          mma_acc_pair<IDESC_ACC2>(tmem + C::TM_DV, tSB, dslot(it) + COLS_HALF, i > 0);
+          tc_commit_pair(BAR(C::B_DOEMPTY + it % C::NDO), 0x3);
+          if (more) {
+            mma_abt_pair<IDESC_S2>(tSB, kt, qslot(it1) + ROWS_HALF);
+            tc_commit_pair(BAR(C::B_SFULL), 0x3);
+          }
+          ok = mbar_wait3_cl(BAR(C::B_DSREADY), it & 1, SITE_DKDV_DS_READY,
+                             more ? BAR(C::B_DOFULL + it1 % C::NDO) : BAR(C::B_DSREADY),
+                             more ? (it1 / C::NDO) & 1 : it & 1, SITE_DKDV_DO_FULL,
+                             BAR(C::B_DSREADY), it & 1, SITE_DKDV_DS_READY, wc);
+          if (!ok) break;
+          FA_TRACE(TR_KV_B, it);
+          tc_fence_after();
+          mma_acc_pair<IDESC_ACC2>(tmem + C::TM_DK, tDB, qslot(it) + COLS_HALF, i > 0);
+          tc_commit_pair(BAR(C::B_QEMPTY + it % C::NQ), 0x3);
+          if (more) {
+            mma_abt_pair<IDESC_S2>(tDB, vt, dslot(it1) + ROWS_HALF);
+            tc_commit_pair(BAR(C::B_DPFULL), 0x3);
+          } else {
+            tc_commit_pair(BAR(C::B_ACCFULL), 0x3);
+            tc_commit_pair(BAR(C::B_KVEMPTY), 0x3);
+          }
+        }
+        ++u_it;
+      }
+      // every MMA of this CTA pair has landed before either CTA tears down
+      tc_commit_pair(BAR(C::B_DRAIN), 0x3);
+      drain_wait(BAR(C::B_DRAIN), 0, 100000000ull);
+    }
+  }
+  } else {
+    regs_inc<REGS_COMPUTE>();
+    // ------------------------------------------------------------ P^T / dS^T
+    const int wg = warp >> 2;                             // query-column half
+    const int lg = warp & 3;
+    const int j = lg * 32 + lane;                         // key row within this CTA's 128
+    const uint32_t lane_off = (uint32_t)(lg * 32) << 16;
+    const int c0 = wg * 64;
+    const uint32_t t_s = tmem + lane_off + C::TM_SB + c0;
+    const uint32_t t_dp = tmem + lane_off + C::TM_DB + c0;
+    const float sl2 = p.scale_log2;
+    Walker w;
+    w.init(spec);
+    uint32_t it = 0;
+    int u_it = 0;
+    bool ok = true;
+    // a warp's 32 threads count once (32) on CTA 0's barrier
+    auto ready = [&](uint32_t bar) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(bar, 0, 32);
+    };
+    for (int k = 0; ok; ++k) {
+      Unit u;
+      if (!w.seek(snake_index(k, G, cta), u)) break;
+      const int g = u.head;
+      const int key = u.m * PAIR_BN + 128 * (int)rank + j;   // key index within the sequence
+      const bool key_ok = key < u.k_len;
+      const long long krow = ((long long)u.k_start + key) * p.Hkv + g;
+      __nv_bfloat16* dk_row = p.dk + krow * D + wg * (D / 2);
+      __nv_bfloat16* dv_row = p.dv + krow * D + wg * (D / 2);
+      if (u.cost == 0) {
+        if (key_ok) {
+          zero_half<D>(dk_row);
+          zero_half<D>(dv_row);
+        }
+        continue;
+      }
+      const int n = u.cost * group;
+      const int m_first = first_qblock_pair(u, p.causal);
+      const int qmin = p.causal ? key - (u.k_len - u.q_len) : -(1 << 30);
+      for (int i = 0; i < n; ++i, ++it) {
+        const StepInfo st = step_of(i, u.cost, m_first, g, group);
+        const uint32_t sl = it % C::NLD;
+        const float4* nl4 =
+            reinterpret_cast<const float4*>(smem + C::LD_OFF + sl * C::LD_BYTES) + c0 / 4;
+        const float4* nd4 = nl4 + BM / 4;
+        ok = mbar_wait(BAR(C::B_LDFULL + sl), (it / C::NLD) & 1, wc, SITE_DKDV_LD_FULL);
+        if (!ok) break;
+        float4 l4r[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) l4r[c] = nl4[c];
+        ok = mbar_wait_cl(BAR(C::B_SFULL), it & 1, wc, SITE_DKDV_S_FULL);
+        if (!ok) break;
+        if (threadIdx.x == 0) FA_TRACE(TR_KV_S, it);
+        tc_fence_after();
+        uint32_t sa[64];
+        tmem_ld64(t_s, sa);
+        const int cmin = key_ok ? qmin - (st.m * BM + c0) : 64;
+        const bool mask = __any_sync(0xffffffffu, cmin > 0);
+        uint64_t p2[32];
+        {
+          const uint64_t sl2x2 = f2pack(sl2, sl2);
+#pragma unroll
+          for (int c = 0; c < 64; c += 4) {
+            const float4 l4 = l4r[c / 4];
+            float x[4];
+            f2unpack(ffma2(f2pack(u2f(sa[c]), u2f(sa[c + 1])), sl2x2, f2pack(l4.x, l4.y)), x[0],
+                     x[1]);
+            f2unpack(ffma2(f2pack(u2f(sa[c + 2]), u2f(sa[c + 3])), sl2x2, f2pack(l4.z, l4.w)),
+                     x[2], x[3]);
+            float pe[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              pe[e] = ((c + e) & 7) < POLY8 ? exp2_poly(x[e]) : ex2_mufu(x[e]);
+              if (mask) pe[e] = (c + e) < cmin ? 0.f : pe[e];
+            }
+            p2[c / 2] = f2pack(pe[0], pe[1]);
+            p2[c / 2 + 1] = f2pack(pe[2], pe[3]);
+          }
+        }
+        store_bf16_half(t_s, p2);
+        tmem_st_wait();
+        tc_fence_before();
+        ready(BAR(C::B_PREADY));
+        if (threadIdx.x == 0) FA_TRACE(TR_KV_P, it);
+        ok = mbar_wait_cl(BAR(C::B_DPFULL), it & 1, wc, SITE_DKDV_DP_FULL);
+        if (!ok) break;
+        if (threadIdx.x == 0) FA_TRACE(TR_KV_DP, it);
+        tc_fence_after();
+        uint32_t dpa[64];
+        tmem_ld64(t_dp, dpa);
+        uint32_t pk[32];
+#pragma unroll
+        for (int c = 0; c < 64; c += 4) {
+          const float4 d4 = nd4[c / 4];
+          pk[c / 2] = pack2(fmul2(p2[c / 2], fadd2(f2pack(u2f(dpa[c]), u2f(dpa[c + 1])),
+                                                   f2pack(d4.x, d4.y))));
+          pk[c / 2 + 1] = pack2(fmul2(p2[c / 2 + 1],
+                                      fadd2(f2pack(u2f(dpa[c + 2]), u2f(dpa[c + 3])),
+                                            f2pack(d4.z, d4.w))));
+        }
+        mbar_arrive(BAR(C::B_LDEMPTY + sl));
+        tmem_st32(t_dp, pk);
+        tmem_st_wait();
+        tc_fence_before();
+        ready(BAR(C::B_DSREADY));
+        if (threadIdx.x == 0) FA_TRACE(TR_KV_DS, it);
+      }
+      if (!ok) break;
+      ok = mbar_wait_cl(BAR(C::B_ACCFULL), u_it & 1, wc, SITE_DKDV_ACC_FULL);
+      if (!ok) break;
+      tc_fence_after();
+      ++u_it;
+      store_acc_half<D>(tmem + lane_off + C::TM_DV + wg * (D / 2), dv_row, 1.0f, key_ok);
+      store_acc_half<D>(tmem + lane_off + C::TM_DK + wg * (D / 2), dk_row, p.scale, key_ok);
+      tc_fence_before();
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();                                   // the peer no longer signals or reads this CTA
+  if (warp == MMA_WARP) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, 512);
+  }
+#undef BAR
+}
+
 // ============================================================== dQ pass
 template <int D, int POLY8>
 __global__ void __launch_bounds__(NUM_THREADS, 1) dq_kernel(const __grid_constant__ BwdParams p) {
@@ -905,6 +1359,55 @@ static cudaError_t launch_split_pair(const BwdParams& p, int grid_kv, int grid_q
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   return cudaSuccess;
+}
+
+// Most CTA pairs of the dK/dV pair kernel that can be resident at once (0 on error).
+int dkdv_pair_max_clusters() {
+  auto kern = bsplit::dkdv_pair_kernel<0>;
+  const int smem = bsplit::CfgKV<128>::SMEM_BYTES;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(bsplit::NUM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, (void*)kern, &cfg) != cudaSuccess) return 0;
+  return n;
+}
+
+template <int POLY8>
+static cudaError_t launch_pair_then_dq(const BwdParams& p, int grid_pair, int grid_q,
+                                       cudaStream_t stream) {
+  auto kkv = bsplit::dkdv_pair_kernel<POLY8>;
+  auto kq = bsplit::dq_kernel<128, POLY8>;
+  const int s_kv = bsplit::CfgKV<128>::SMEM_BYTES, s_q = bsplit::CfgQ<128>::SMEM_BYTES;
+  cudaError_t e = cudaFuncSetAttribute(kkv, cudaFuncAttributeMaxDynamicSharedMemorySize, s_kv);
+  if (e != cudaSuccess) return e;
+  if ((e = cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, s_q)) !=
+      cudaSuccess)
+    return e;
+  if (grid_pair > 0) {
+    kkv<<<grid_pair, bsplit::NUM_THREADS, s_kv, stream>>>(p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  if (grid_q > 0) {
+    kq<<<grid_q, bsplit::NUM_THREADS, s_q, stream>>>(p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+// The two-pass backward with the dK/dV pass on CTA pairs (head dim 128);
+// grid_pair is even.
+cudaError_t launch_bwd_pair(const BwdParams& p, int grid_pair, int grid_q, cudaStream_t stream,
+                            int poly8) {
+  switch (poly8) {
+    case 0: return launch_pair_then_dq<0>(p, grid_pair, grid_q, stream);
+    case 2: return launch_pair_then_dq<2>(p, grid_pair, grid_q, stream);
+    case 4: return launch_pair_then_dq<4>(p, grid_pair, grid_q, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 // The two passes of the split backward (after the preprocess pass of bwd.cu).

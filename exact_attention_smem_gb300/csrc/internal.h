@@ -32,8 +32,9 @@ struct Knobs {
   float tau_log2 = 0.0f;         // rescale threshold, base-2 units
   int poly8 = 0;                 // eighths of the exponentials done by the polynomial (fwd)
   int bwd_poly8 = 0;             // same for the backward
-  int bwd_mode = 1;              // 1: two-pass backward (dK/dV pass + dQ pass); 0: one pass
-                                 // with dQ by fp32 atomics and a convert pass
+  int bwd_mode = 1;              // 1: two-pass backward (dK/dV pass + dQ pass); 2: the same
+                                 // with the dK/dV pass on CTA pairs (d = 128; d = 64 runs
+                                 // mode 1); 0: one pass with dQ by fp32 atomics + convert
   long long timeout_ns = 2000000000LL;
   int grid_override = 0;         // >0: persistent grid size (schedule permutation tests)
   cudaEvent_t ev[2][2] = {{nullptr, nullptr}, {nullptr, nullptr}};  // [fwd|bwd][start|stop]
@@ -78,6 +79,7 @@ struct BwdParams {
   CUtensorMap tm_q, tm_do;       // [T, Hq, d] views, 64-column boxes of 64 rows (one-pass
                                  // kernel) or 128 rows (two-pass kernels), 128B swizzle
   CUtensorMap tm_k, tm_v;        // [T, Hkv, d] views, 64-column x 128-row boxes
+  CUtensorMap tm_q2, tm_do2;     // 64-column x 64-row boxes (CTA-pair dK/dV pass only)
   __nv_bfloat16 *dk, *dv;
   __nv_bfloat16* dq;             // bf16 [Tq, Hq, d] (written directly by the dQ pass)
   float* dq_acc;                 // fp32 [Tq, Hq, d] (one-pass kernel only; else nullptr)
@@ -122,6 +124,9 @@ cudaError_t launch_bwd(const BwdParams& p, const BwdAux& aux, int d, int grid, i
                        cudaStream_t stream, int poly8, int mode);
 cudaError_t launch_bwd_split(const BwdParams& p, int d, int grid_kv, int grid_q,
                              cudaStream_t stream, int poly8);
+cudaError_t launch_bwd_pair(const BwdParams& p, int grid_pair, int grid_q, cudaStream_t stream,
+                            int poly8);
+int dkdv_pair_max_clusters();
 
 int num_sms();
 int* device_error_word();

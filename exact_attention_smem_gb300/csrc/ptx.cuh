@@ -238,6 +238,68 @@ __device__ __forceinline__ void mma_ts_pair(uint32_t d_tmem, uint32_t a_tmem, ui
       : "memory");
 }
 
+// Arrive `count` times on the barrier at the same shared-memory offset in CTA
+// `cta` of the cluster (release at cluster scope).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar, uint32_t cta, uint32_t count) {
+  asm volatile(
+      "{\n\t.reg .b32 ra;\n\t"
+      "mapa.shared::cluster.u32 ra, %0, %1;\n\t"
+      "mbarrier.arrive.release.cluster.shared::cluster.b64 _, [ra], %2;\n\t}" ::"r"(bar),
+      "r"(cta), "r"(count)
+      : "memory");
+}
+// Probes with acquire at cluster scope, for barriers that also receive
+// arrivals from the peer CTA.
+__device__ __forceinline__ bool mbar_try_wait_cl(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_test3_cl(uint32_t b0, uint32_t p0, uint32_t b1, uint32_t p1,
+                                              uint32_t b2, uint32_t p2) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred q0, q1, q2;\n\t"
+      "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 q0, [%1], %2;\n\t"
+      "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 q1, [%3], %4;\n\t"
+      "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 q2, [%5], %6;\n\t"
+      "and.pred q0, q0, q1;\n\t"
+      "and.pred q0, q0, q2;\n\t"
+      "selp.u32 %0, 1, 0, q0;\n\t}"
+      : "=r"(ok)
+      : "r"(b0), "r"(p0), "r"(b1), "r"(p1), "r"(b2), "r"(p2)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_cl(uint32_t bar, uint32_t parity, const WaitCtl& w,
+                                             int site) {
+  if (mbar_try_wait_cl(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_try_wait_cl(bar, parity)) return true;
+    if ((it & 15u) == 15u) {
+      if (*w.abort) return false;
+      if (globaltimer_ns() - t0 > w.timeout_ns) {
+        atomicCAS(w.err, 0, site);
+        *w.abort = 1;
+        return false;
+      }
+    }
+  }
+}
+__device__ __forceinline__ bool mbar_wait3_cl(uint32_t b0, uint32_t p0, int s0, uint32_t b1,
+                                              uint32_t p1, int s1, uint32_t b2, uint32_t p2,
+                                              int s2, const WaitCtl& w) {
+  if (mbar_test3_cl(b0, p0, b1, p1, b2, p2)) return true;
+  return mbar_wait_cl(b0, p0, w, s0) && mbar_wait_cl(b1, p1, w, s1) && mbar_wait_cl(b2, p2, w, s2);
+}
+
 // D (TMEM) (+)= A (smem) * B (smem)
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                        uint32_t idesc, uint32_t accumulate) {

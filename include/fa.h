@@ -230,7 +230,8 @@ FA_API int fa_test_wait_timeout(int* status_dev, double timeout_ms, void* stream
  * = one-pass backward (units of 128 keys, cost = query blocks of 64), kind 2 =
  * dK/dV pass of the two-pass backward (units of 128 keys, cost = query blocks
  * of 128), kind 3 = its dQ pass (units of 128 query rows, cost = KV blocks of
- * 128). cu_seqlens_host
+ * 128), kind 4 = the dK/dV pass on CTA pairs (units of 256 keys, cost =
+ * query blocks of 128). cu_seqlens_host
  * is a HOST array (or NULL for dense B x Sq/Sk). Returns the number of units
  * (may exceed max_units; only max_units are written), or -1 on bad arguments.
  */

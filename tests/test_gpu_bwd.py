@@ -1,8 +1,9 @@
 """Backward parity: dQ, dK, dV from the CUDA path against the fp64 oracle.
 
-Every test runs for both backward forms: mode 1 (default: a dK/dV pass over
-key blocks and a dQ pass over query blocks, no atomics) and mode 0 (one pass
-with dQ accumulated by fp32 atomics, then converted)."""
+Every test runs for each backward form: mode 1 (a dK/dV pass over key blocks
+and a dQ pass over query blocks, no atomics), mode 2 (the same with the dK/dV
+pass on CTA pairs; head dim 64 runs mode 1) and mode 0 (one pass with dQ
+accumulated by fp32 atomics, then converted)."""
 import math
 
 import numpy as np
@@ -28,7 +29,7 @@ def _dev():
     fa.fa_debug_set("bwd_mode", 1)
 
 
-@pytest.fixture(params=[1, 0], ids=["two_pass", "one_pass"], autouse=True)
+@pytest.fixture(params=[1, 2, 0], ids=["two_pass", "two_pass_pairs", "one_pass"], autouse=True)
 def bwd_mode(request):
     fa.fa_debug_set("bwd_mode", request.param)
     yield request.param
@@ -119,14 +120,14 @@ def test_schedule_permutation(bwd_mode):
     b = _run(x, True, 0.1)
     fa.fa_debug_set("grid", 0)
     assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])     # dK, dV: no atomics
-    if bwd_mode == 1:
+    if bwd_mode != 0:
         assert torch.equal(a[0], b[0])                              # dQ: no atomics either
     else:
         assert (a[0].float() - b[0].float()).abs().max().item() <= 1e-2
 
 
 def test_two_pass_is_deterministic(bwd_mode):
-    if bwd_mode != 1:
+    if bwd_mode == 0:
         pytest.skip("the one-pass form adds dQ with atomics")
     x = random_inputs(B=1, Hq=4, Hkv=2, Sq=1000, Sk=1000, d=128, seed=81, device="cuda")
     a = _run(x, True, 0.1)

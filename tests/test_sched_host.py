@@ -22,7 +22,8 @@ def _visible(i, j, ql, kl, causal):
 
 
 # kind -> (query-unit rows or key-unit rows, inner block rows, units over queries?)
-_KINDS = {0: (256, 128, True), 1: (128, 64, False), 2: (128, 128, False), 3: (128, 128, True)}
+_KINDS = {0: (256, 128, True), 1: (128, 64, False), 2: (128, 128, False), 3: (128, 128, True),
+          4: (256, 128, False)}
 
 
 def _brute_units(kind, B, cu, Sq, Sk, heads, causal):
@@ -64,6 +65,8 @@ CASES = [
     (2, 1, None, 1000, 300, 2, True), (2, 4, [0, 1, 1, 700, 3000], 3000, 3000, 2, True),
     (3, 2, None, 600, 600, 3, True), (3, 2, None, 600, 600, 3, False), (3, 1, None, 300, 1000, 2, True),
     (3, 1, None, 1000, 300, 2, True), (3, 3, [0, 129, 385, 1000], 1000, 1000, 4, True),
+    (4, 2, None, 600, 600, 3, True), (4, 1, None, 300, 1000, 2, True), (4, 1, None, 1000, 300, 2, True),
+    (4, 4, [0, 1, 1, 700, 3000], 3000, 3000, 2, True),
 ]
 
 
@@ -119,8 +122,9 @@ def test_causal_balance_near_lpt_bound():
     """Long causal batch: per-CTA total cost within a few percent of the mean."""
     G = 152
     # the kernels' choices: forward and dQ pass one group, dK/dV pass and one-pass auto
-    for kind, hpg in ((0, 32), (1, 0), (2, 0), (3, 32)):
-        loads = [sum(u[3] for u in fa_sched_list(kind, 1, None, 32768, 32768, 32, True, G, b, hpg))
-                 for b in range(G)]
-        mean = sum(loads) / G
+    for kind, hpg in ((0, 32), (1, 0), (2, 0), (3, 32), (4, 0)):
+        g = G // 2 if kind == 4 else G           # the pair kernel's grid counts CTA pairs
+        loads = [sum(u[3] for u in fa_sched_list(kind, 1, None, 32768, 32768, 32, True, g, b, hpg))
+                 for b in range(g)]
+        mean = sum(loads) / g
         assert max(loads) <= 1.03 * mean, (kind, max(loads) / mean)
