@@ -48,9 +48,11 @@ def _dist():
 
 
 class Clocks:
-    """Samples nvidia-smi SM clocks and throttle reasons during the timed region."""
+    """Samples nvidia-smi SM clocks and throttle reasons every 50 ms. Started
+    before the warm-up (nvidia-smi needs a moment for its first sample); the
+    summary keeps the samples stamped inside the timed region."""
 
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -64,7 +66,7 @@ class Clocks:
             os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=self.fh, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
@@ -79,14 +81,25 @@ class Clocks:
                 self.proc.kill()
             self.fh.close()
 
-    def summary(self):
+    def summary(self, t0=None, t1=None):
+        """Median SM clock, max clock and throttle reasons of the samples taken
+        between wall-clock times t0 and t1 (all samples when not given)."""
+        import datetime
         if self.proc is None or not os.path.exists(self.path):
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
         rows = []
         for line in open(self.path):
             parts = [x.strip() for x in line.split(",")]
-            if len(parts) >= 9:
-                rows.append(parts)
+            if len(parts) < 10:
+                continue
+            if t0 is not None:
+                try:
+                    ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                except ValueError:
+                    continue
+                if not (t0 <= ts <= t1):
+                    continue
+            rows.append(parts[1:])
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
         sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
@@ -177,6 +190,7 @@ def run_ours(args):
         fa.fa_bwd(x.q, x.k, x.v, o, lse, x.do, dq, dk, dv, B, Hq, Hkv, S, S, d, True, scale, None,
                   wsbuf, nbytes, stream)
 
+    clk = Clocks(local).__enter__()
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
@@ -187,12 +201,14 @@ def run_ours(args):
     if ws > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    with Clocks(local) as clk:
-        t0.record(stream)
-        for i in range(args.steps):
-            step(evs[i])
-        t1.record(stream)
-        torch.cuda.synchronize()
+    wall0 = time.time()
+    t0.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    wall1 = time.time()
+    clk.__exit__(None, None, None)
     if ws > 1:
         dist.barrier()
     assert fa.fa_get_device_error() == 0
@@ -236,7 +252,7 @@ def run_ours(args):
                                                          f"fwd_kernel_{WORKLOAD}.md")}},
         "e2e": e2e,
         "gpu_launches": 5 * args.steps,
-        "clocks": clk.summary(),
+        "clocks": clk.summary(wall0, wall1),
         "cpu_baseline": cpu,
     }
     print(json.dumps(out))
@@ -245,44 +261,72 @@ def run_ours(args):
 
 
 def run_e2e(fa, w, x, args, stream):
-    """Same step with inputs in pinned host memory: H2D copies, fwd, bwd, D2H of results."""
+    """The step through the C ABI with inputs and results in pinned host memory.
+
+    Every step copies its inputs host->device and its results (O, LSE, dQ, dK,
+    dV) device->host inside the timed region. The copies run on their own
+    streams and device buffers are double-buffered, so step k's input copy and
+    step k-1's result copy overlap step k-1's / k's kernels (a buffer set is
+    reused only after the step that last used it has finished with it)."""
     import torch
     hq, hk, hv, hdo = (t.cpu().pin_memory() for t in (x.q, x.k, x.v, x.do))
     B, Hq, Hkv, S, d = w.B, w.Hq, w.Hkv, w.Sq, w.d
-    dq_, dk_, dv_ = (torch.empty_like(t) for t in (x.q, x.k, x.v))
-    q_, k_, v_, do_ = (torch.empty_like(t) for t in (x.q, x.k, x.v, x.do))
-    o_ = torch.empty_like(x.q)
-    lse_ = torch.empty(B, Hq, S, dtype=torch.float32, device="cuda")
     ho, hlse = torch.empty_like(hq).pin_memory(), torch.empty(B, Hq, S).pin_memory()
     hdq, hdk, hdv = (torch.empty_like(t).pin_memory() for t in (hq, hk, hv))
     nbytes = fa.fa_bwd_workspace_bytes(B, Hq, S, d, 0)
     wsbuf = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
-
-    def step():
-        for dst, src in ((q_, hq), (k_, hk), (v_, hv), (do_, hdo)):
-            dst.copy_(src, non_blocking=True)
-        fa.fa_fwd(q_, k_, v_, o_, lse_, B, Hq, Hkv, S, S, d, True, w.scale, None, stream)
-        fa.fa_bwd(q_, k_, v_, o_, lse_, do_, dq_, dk_, dv_, B, Hq, Hkv, S, S, d, True, w.scale,
-                  None, wsbuf, nbytes, stream)
-        for dst, src in ((ho, o_), (hlse, lse_), (hdq, dq_), (hdk, dk_), (hdv, dv_)):
-            dst.copy_(src, non_blocking=True)
-
+    sets = []
     for _ in range(2):
-        step()
+        q_, k_, v_, do_ = (torch.empty_like(t) for t in (x.q, x.k, x.v, x.do))
+        sets.append({"in": (q_, k_, v_, do_),
+                     "out": (torch.empty_like(x.q), torch.empty(B, Hq, S, dtype=torch.float32,
+                                                                 device="cuda"),
+                             torch.empty_like(x.q), torch.empty_like(x.k), torch.empty_like(x.v))})
+    comp, h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(2)]      # inputs of the set copied
+    ev_used = [torch.cuda.Event() for _ in range(2)]    # kernels done with the set
+    ev_out = [torch.cuda.Event() for _ in range(2)]     # results of the set copied out
+    for e in ev_used + ev_out:
+        e.record(comp)
+
+    def step(i):
+        st = sets[i % 2]
+        q_, k_, v_, do_ = st["in"]
+        o_, lse_, dq_, dk_, dv_ = st["out"]
+        h2d.wait_event(ev_used[i % 2])
+        with torch.cuda.stream(h2d):
+            for dst, src in ((q_, hq), (k_, hk), (v_, hv), (do_, hdo)):
+                dst.copy_(src, non_blocking=True)
+        ev_in[i % 2].record(h2d)
+        comp.wait_event(ev_in[i % 2])
+        comp.wait_event(ev_out[i % 2])
+        fa.fa_fwd(q_, k_, v_, o_, lse_, B, Hq, Hkv, S, S, d, True, w.scale, None, comp)
+        fa.fa_bwd(q_, k_, v_, o_, lse_, do_, dq_, dk_, dv_, B, Hq, Hkv, S, S, d, True, w.scale,
+                  None, wsbuf, nbytes, comp)
+        ev_used[i % 2].record(comp)
+        d2h.wait_event(ev_used[i % 2])
+        with torch.cuda.stream(d2h):
+            for dst, src in ((ho, o_), (hlse, lse_), (hdq, dq_), (hdk, dk_), (hdv, dv_)):
+                dst.copy_(src, non_blocking=True)
+        ev_out[i % 2].record(d2h)
+
+    for i in range(2):
+        step(i)
     torch.cuda.synchronize()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    n = max(1, min(args.steps, 5))
-    t0.record(stream)
-    for _ in range(n):
-        step()
-    t1.record(stream)
+    n = max(1, min(args.steps, 10))
+    t0.record(h2d)
+    for i in range(n):
+        step(i)
+    t1.record(d2h)                                      # after the last result copy
     torch.cuda.synchronize()
     ms = t0.elapsed_time(t1) / n
     f_fwd, f_bwd = flops(w)
-    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
-    d2h = sum(t.numel() * t.element_size() for t in (ho, hlse, hdq, hdk, hdv))
+    h2d_b = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
+    d2h_b = sum(t.numel() * t.element_size() for t in (ho, hlse, hdq, hdk, hdv))
     return {"value": round((f_fwd + f_bwd) / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
-            "ms_per_step": round(ms, 3), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+            "ms_per_step": round(ms, 3), "h2d_bytes_per_step": h2d_b, "d2h_bytes_per_step": d2h_b,
+            "steps": n, "overlap": "copies on their own streams, device buffers double-buffered"}
 
 
 def _oracle_sample(w, x_cpu):

@@ -423,6 +423,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dkdv_kernel(const __grid_const
         tc_commit(BAR(C::B_SFULL));
         mma_abt<D, C::IDESC_S>(tDB, vt, dslot(it));
         tc_commit(BAR(C::B_DPFULL));
+        // K and V feed only S^T and dP^T: they are released once the unit's
+        // last dP^T is issued, so the next unit's copy overlaps this one's tail
+        if (n == 1) tc_commit(BAR(C::B_KVEMPTY));
         for (int i = 0; i < n && ok; ++i, ++it) {
           const bool more = i + 1 < n;
           const uint32_t it1 = it + 1;
@@ -453,9 +456,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dkdv_kernel(const __grid_const
           if (more) {
             mma_abt<D, C::IDESC_S>(tDB, vt, dslot(it1));
             tc_commit(BAR(C::B_DPFULL));
+            if (i + 2 == n) tc_commit(BAR(C::B_KVEMPTY));
           } else {
             tc_commit(BAR(C::B_ACCFULL));
-            tc_commit(BAR(C::B_KVEMPTY));
           }
         }
         ++u_it;
@@ -880,6 +883,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         tc_commit_pair(BAR(C::B_SFULL), 0x3);
         mma_abt_pair<IDESC_S2>(tDB, vt, dslot(it) + ROWS_HALF);
         tc_commit_pair(BAR(C::B_DPFULL), 0x3);
+        if (n == 1) tc_commit_pair(BAR(C::B_KVEMPTY), 0x3);   // K/V: see the one-CTA form
         for (int i = 0; i < n && ok; ++i, ++it) {
           const bool more = i + 1 < n;
           const uint32_t it1 = it + 1;
@@ -908,9 +912,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           if (more) {
             mma_abt_pair<IDESC_S2>(tDB, vt, dslot(it1) + ROWS_HALF);
             tc_commit_pair(BAR(C::B_DPFULL), 0x3);
+            if (i + 2 == n) tc_commit_pair(BAR(C::B_KVEMPTY), 0x3);
           } else {
             tc_commit_pair(BAR(C::B_ACCFULL), 0x3);
-            tc_commit_pair(BAR(C::B_KVEMPTY), 0x3);
           }
         }
         ++u_it;
