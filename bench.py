@@ -329,13 +329,16 @@ def run_e2e(fa, w, x, args, stream):
             "steps": n, "overlap": "copies on their own streams, device buffers double-buffered"}
 
 
-def _oracle_sample(w, x_cpu):
-    """fp64 oracle forward + backward of query head 0 (one of Hq heads) of the workload."""
+def _oracle_sample(w, x_cpu, rows=None):
+    """fp64 oracle forward + backward of query head 0 of the workload, on its
+    first `rows` query rows (all when None; causal rows [0, n) see only keys
+    [0, n), so that prefix is itself an exact causal problem)."""
     import oracle
-    q = x_cpu.q[0, :, 0]
-    k = x_cpu.k[0, :, 0]
-    v = x_cpu.v[0, :, 0]
-    do = x_cpu.do[0, :, 0]
+    n = x_cpu.q.shape[1] if rows is None else rows
+    q = x_cpu.q[0, :n, 0]
+    k = x_cpu.k[0, :n, 0]
+    v = x_cpu.v[0, :n, 0]
+    do = x_cpu.do[0, :n, 0]
     oracle.attend_head_backward(q, k, v, do, w.scale, w.causal)   # runs the forward inside
 
 
@@ -369,13 +372,16 @@ def run_reference(args):
     w = WORKLOADS[WORKLOAD]
     x = make_inputs(w, "cpu")
     f_fwd, f_bwd = flops(w)
-    sample_flops = (f_fwd + f_bwd) / w.Hq
-    for _ in range(args.warmup and 1):
-        pass
+    # each step: the first half of head 0's query rows (a quarter of the head's
+    # causal FLOPs), so that --steps 10 --warmup 3 stays near a minute of CPU time
+    rows = w.Sq // 2
+    sample_flops = (f_fwd + f_bwd) / w.Hq * (rows / w.Sq) ** 2
+    for _ in range(args.warmup):
+        _oracle_sample(w, x, rows)
     times = []
     for _ in range(args.steps):
         t = time.perf_counter()
-        _oracle_sample(w, x)
+        _oracle_sample(w, x, rows)
         times.append(time.perf_counter() - t)
     dt = statistics.mean(times)
     value = sample_flops / dt / 1e12
@@ -384,10 +390,12 @@ def run_reference(args):
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
            "data": "synthetic (seeded N(0,1) bf16, upcast to fp64)", "impl": "reference",
            "config": {"workload": WORKLOAD, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "S": w.Sq,
-                      "d": w.d, "causal": True, "step": "fwd+bwd (one head per step)"},
+                      "d": w.d, "causal": True,
+                      "step": "fwd+bwd of query rows [0, S/2) of head 0 per step"},
            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": os.cpu_count(),
                             "kind": "oracle",
-                            "sample": f"query head 0 of {WORKLOAD} per step (1/{w.Hq} of the "
+                            "sample": f"query rows [0, {rows}) of head 0 of {WORKLOAD} per step "
+                                      f"(causal: {sample_flops / (f_fwd + f_bwd):.5f} of the "
                                       "workload's FLOPs), fp64 numpy fwd+bwd"},
            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                    "d2h_bytes_per_step": 0}}
