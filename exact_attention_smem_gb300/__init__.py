@@ -11,7 +11,7 @@ import math
 
 from ._lib import (FAError, fa_bwd, fa_bwd_noalloc, fa_bwd_workspace_bytes, fa_debug_set,  # noqa: F401
                    fa_debug_set_events, fa_debug_set_trace,
-                   fa_exp2_poly_host, fa_fwd, fa_micro, fa_get_device_error, fa_sched_list, fa_test_exp2,
+                   fa_exp2_poly_host, fa_fwd, fa_merge, fa_micro, fa_get_device_error, fa_sched_list, fa_test_exp2,
                    fa_test_mma, fa_test_mma_pair, fa_test_wait_timeout, load)
 
 

@@ -45,6 +45,7 @@ _SIGS = {
     "fa_exp2_poly_host": (_F, [_F]),
     "fa_micro": (_I, [_I, _I, _P, _I, _P]),
     "fa_test_mma": (_I, [_P, _P, _P, _I, _I, _P]),
+    "fa_merge": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P]),
     "fa_test_mma_pair": (_I, [_P, _P, _P, _P, _I, _I, _P]),
     "fa_test_wait_timeout": (_I, [_P, ctypes.c_double, _P]),
     "fa_sched_list": (_I, [_I, _I, _P, _I, _I, _I, _I, _I, _I, _I, _P, _I]),
@@ -166,6 +167,11 @@ def fa_exp2_poly_host(x: float) -> float:
 
 def fa_test_mma(A, B, C, mode, N, stream=None):
     _check(load().fa_test_mma(_ptr(A), _ptr(B), _ptr(C), mode, N, _stream(stream)), "fa_test_mma")
+
+
+def fa_merge(o_parts, lse_parts, P, B, Hq, S, d, packed, o, lse, stream=None):
+    _check(load().fa_merge(_ptr(o_parts), _ptr(lse_parts), P, B, Hq, S, d, int(packed), _ptr(o),
+                           _ptr(lse), _stream(stream)), "fa_merge")
 
 
 def fa_test_mma_pair(A, B, C, flags, mode, N, stream=None):

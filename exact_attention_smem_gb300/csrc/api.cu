@@ -372,6 +372,28 @@ extern "C" int fa_bwd(const void* q, const void* k, const void* v, const void* o
   return FA_OK;
 }
 
+extern "C" int fa_merge(const void* o_parts, const float* lse_parts, int P, int B, int Hq, int S,
+                        int d, int packed, void* o, float* lse, void* stream) {
+  t_last_error.clear();
+  const void* ptrs[4] = {o_parts, lse_parts, o, lse};
+  for (int i = 0; i < 4; ++i)
+    if (!ptrs[i]) return fail(FA_ERR_INVALID_ARG, "pointer %d is NULL", i);
+  if (P < 1 || P > 64) return fail(FA_ERR_INVALID_ARG, "parts P=%d (1..64)", P);
+  if (B < 0 || Hq <= 0 || S < 0) return fail(FA_ERR_INVALID_ARG, "bad sizes B=%d Hq=%d S=%d", B, Hq, S);
+  if (d != 64 && d != 128) return fail(FA_ERR_UNSUPPORTED, "head dim %d (supported: 64, 128)", d);
+  const long long rows = packed ? (long long)S : (long long)B * S;
+  if (rows == 0) return FA_OK;
+  DevInfo* di = nullptr;
+  int st = device_info(&di);
+  if (st != FA_OK) return st;
+  cudaError_t e = launch_merge(static_cast<const __nv_bfloat16*>(o_parts), lse_parts, P, rows, Hq,
+                               packed ? (int)rows : S, d, packed ? 1 : 0,
+                               static_cast<__nv_bfloat16*>(o), lse,
+                               static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(FA_ERR_CUDA, "merge launch: %s", cudaGetErrorString(e));
+  return FA_OK;
+}
+
 extern "C" const char* fa_status_string(int status) {
   switch (status) {
     case FA_OK: return "ok";

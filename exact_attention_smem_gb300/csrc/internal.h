@@ -127,6 +127,9 @@ cudaError_t launch_bwd_split(const BwdParams& p, int d, int grid_kv, int grid_q,
 cudaError_t launch_bwd_pair(const BwdParams& p, int grid_pair, int grid_q, cudaStream_t stream,
                             int poly8);
 int dkdv_pair_max_clusters();
+cudaError_t launch_merge(const __nv_bfloat16* o_parts, const float* lse_parts, int P,
+                         long long rows, int Hq, int S, int d, int packed, __nv_bfloat16* o,
+                         float* lse, cudaStream_t stream);
 
 int num_sms();
 int* device_error_word();

@@ -114,6 +114,29 @@ FA_API int fa_bwd_noalloc(const void* q, const void* k, const void* v, const voi
                           int Hq, int Hkv, int Sq, int Sk, int d, int causal, float scale,
                           const int* cu_seqlens, void* stream);
 
+/*
+ * Combine step of context parallelism (K/V split into disjoint shards, each
+ * shard's forward run separately): given, for the same queries, part p's O_p
+ * and LSE_p from fa_fwd over key set p, writes the attention over the union
+ * of the key sets,
+ *     LSE = log sum_p exp(LSE_p),   O = sum_p exp(LSE_p - LSE) O_p
+ * (the online-softmax rescale applied across parts: "FlashAttention-4
+ * Conquers Asymmetric GPU Hardware Scaling", episode description, tiling with
+ * an online softmax; its source list names Ring Attention, blockwise
+ * attention across devices). A row that saw no key in a part (LSE = +inf,
+ * O = 0, the forward's convention) counts zero; a row with no key in any part
+ * gets O = 0, LSE = +inf.
+ *   o_parts   device bf16, P consecutive arrays in fa_fwd's O layout
+ *             ([B,S,Hq,d] dense, [S,Hq,d] packed with S = T)
+ *   lse_parts device fp32, P consecutive arrays in fa_fwd's LSE layout
+ *             ([B,Hq,S] dense, [Hq,T] packed)
+ *   packed    0 dense, 1 packed (B is then unused)
+ *   o, lse    outputs in the same layouts (must not alias the parts)
+ * 1 <= P <= 64, d in {64, 128}. Asynchronous on `stream`; allocates nothing.
+ */
+FA_API int fa_merge(const void* o_parts, const float* lse_parts, int P, int B, int Hq, int S,
+                    int d, int packed, void* o, float* lse, void* stream);
+
 /* Static text for a status code. */
 FA_API const char* fa_status_string(int status);
 
