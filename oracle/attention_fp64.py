@@ -28,8 +28,11 @@ The query rows are processed in chunks (``row_chunk``) only to bound memory;
 each row still gets the full two-pass softmax over all of its keys.
 
 Layouts: dense ``[B, S, H, d]``; packed variable-length ``[T, H, d]`` with
-``cu_seqlens`` (one boundary list for queries and keys). LSE is ``[B, Hq, Sq]``
-dense or ``[Hq, T]`` packed.
+``cu_seqlens`` (one boundary list for queries and keys, or, with
+``cu_seqlens_k``, separate lists: sequence i's queries are rows
+[cu_seqlens[i], cu_seqlens[i+1]) of q and its keys rows
+[cu_seqlens_k[i], cu_seqlens_k[i+1]) of k and v, causal bottom-right aligned
+per sequence). LSE is ``[B, Hq, Sq]`` dense or ``[Hq, Tq]`` packed.
 """
 from __future__ import annotations
 
@@ -64,7 +67,7 @@ def attend_head(q, k, v, scale: float, causal: bool, row_chunk: int = 1024):
         s = scale * (q[r0:r1] @ k.T)
         vis = _visible(nq, nk, causal, r0, r1 - r0)
         s = np.where(vis, s, -np.inf)
-        m = s.max(axis=1)
+        m = s.max(axis=1, initial=-np.inf)        # -inf also for a sequence with no keys
         has = np.isfinite(m)
         m_safe = np.where(has, m, 0.0)
         p = np.exp(s - m_safe[:, None])
@@ -101,20 +104,24 @@ def attend_head_backward(q, k, v, do, scale: float, causal: bool, row_chunk: int
     return dq, dk, dv
 
 
-def _segments(q, cu_seqlens, Sq_dense):
+def _bounds(cu):
+    return [int(x) for x in (cu.tolist() if hasattr(cu, "tolist") else cu)]
+
+
+def _segments(q, cu_seqlens, cu_seqlens_k=None):
     """Yield (seq index, q row slice, k row slice) for dense or packed layouts."""
     if cu_seqlens is None:
         for b in range(q.shape[0]):
             yield b, (b, slice(None)), (b, slice(None))
     else:
-        cu = [int(x) for x in (cu_seqlens.tolist() if hasattr(cu_seqlens, "tolist") else cu_seqlens)]
+        cu = _bounds(cu_seqlens)
+        ck = cu if cu_seqlens_k is None else _bounds(cu_seqlens_k)
         for i in range(len(cu) - 1):
-            sl = slice(cu[i], cu[i + 1])
-            yield i, (sl,), (sl,)
+            yield i, (slice(cu[i], cu[i + 1]),), (slice(ck[i], ck[i + 1]),)
 
 
 def forward(q, k, v, scale: float, causal: bool, cu_seqlens=None, heads=None, seqs=None,
-            row_chunk: int = 1024):
+            row_chunk: int = 1024, cu_seqlens_k=None):
     """Forward over a whole batch (or a subset of query heads / sequences).
 
     Returns (o, lse) as float64 arrays in the caller's layout; entries of heads or
@@ -129,7 +136,7 @@ def forward(q, k, v, scale: float, causal: bool, cu_seqlens=None, heads=None, se
     else:
         lse = np.full((hq, q.shape[0]), np.nan)
     heads = range(hq) if heads is None else heads
-    for si, qi, ki in _segments(q, cu_seqlens, None):
+    for si, qi, ki in _segments(q, cu_seqlens, cu_seqlens_k):
         if seqs is not None and si not in seqs:
             continue
         for h in heads:
@@ -145,7 +152,7 @@ def forward(q, k, v, scale: float, causal: bool, cu_seqlens=None, heads=None, se
 
 
 def backward(q, k, v, do, scale: float, causal: bool, cu_seqlens=None, kv_heads=None,
-             seqs=None, row_chunk: int = 1024):
+             seqs=None, row_chunk: int = 1024, cu_seqlens_k=None):
     """Backward over a whole batch (or a subset of KV heads / sequences).
 
     For each selected KV head g, all query heads of its group contribute to dK_g
@@ -158,7 +165,7 @@ def backward(q, k, v, do, scale: float, causal: bool, cu_seqlens=None, kv_heads=
     dk = np.full(k.shape, np.nan)
     dv = np.full(v.shape, np.nan)
     kv_heads = range(hkv) if kv_heads is None else kv_heads
-    for si, qi, ki in _segments(q, cu_seqlens, None):
+    for si, qi, ki in _segments(q, cu_seqlens, cu_seqlens_k):
         if seqs is not None and si not in seqs:
             continue
         for g in kv_heads:

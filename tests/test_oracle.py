@@ -186,6 +186,53 @@ def test_backward_finite_differences_gqa_varlen():
             assert g[idx] == pytest.approx((lp - lm) / (2 * h), rel=1e-6, abs=1e-8)
 
 
+def test_separate_key_boundaries_uniform_scores():
+    """Packed layout with separate query/key boundaries, scale 0: every visible
+    key gets the same weight, so row i of a sequence with q_len queries and
+    k_len keys is the plain mean of V over its first i + k_len - q_len + 1 keys
+    (bottom-right causal) or over all keys, and LSE = ln(number of keys)."""
+    cu_q, cu_k = np.array([0, 3, 4, 9]), np.array([0, 5, 5, 8])   # k_len 5, 0, 3
+    hq, hkv, d = 2, 1, 3
+    q, k, v = _rand((9, hq, d), 60), _rand((8, hkv, d), 61), _rand((8, hkv, d), 62)
+    for causal in (False, True):
+        o, lse = oracle.forward(q, k, v, 0.0, causal, cu_seqlens=cu_q, cu_seqlens_k=cu_k)
+        for s in range(3):
+            ql, kl = cu_q[s + 1] - cu_q[s], cu_k[s + 1] - cu_k[s]
+            for i in range(ql):
+                n = kl if not causal else max(0, min(kl, i + kl - ql + 1))
+                row = cu_q[s] + i
+                for h in range(hq):
+                    if n == 0:
+                        assert np.all(o[row, h] == 0) and lse[h, row] == np.inf
+                    else:
+                        want = v[cu_k[s]:cu_k[s] + n, 0].mean(axis=0)
+                        np.testing.assert_allclose(o[row, h], want, atol=1e-14)
+                        assert lse[h, row] == pytest.approx(np.log(n), abs=1e-14)
+
+
+def test_separate_key_boundaries_finite_differences():
+    """Backward with separate boundaries (prefill over cached keys: more keys than
+    queries, and one sequence with fewer), against central finite differences."""
+    cu_q, cu_k = np.array([0, 2, 5]), np.array([0, 4, 6])
+    hq, hkv, d, scale, h = 2, 1, 3, 0.5, 1e-6
+    q, k, v, do = _rand((5, hq, d), 70), _rand((6, hkv, d), 71), _rand((6, hkv, d), 72), _rand((5, hq, d), 73)
+    dq, dk, dv = oracle.backward(q, k, v, do, scale, True, cu_seqlens=cu_q, cu_seqlens_k=cu_k)
+
+    def loss():
+        o, _ = oracle.forward(q, k, v, scale, True, cu_seqlens=cu_q, cu_seqlens_k=cu_k)
+        return float((o * do).sum())
+
+    for x, g in ((q, dq), (k, dk), (v, dv)):
+        for idx in np.ndindex(*x.shape):
+            old = x[idx]
+            x[idx] = old + h
+            lp = loss()
+            x[idx] = old - h
+            lm = loss()
+            x[idx] = old
+            assert g[idx] == pytest.approx((lp - lm) / (2 * h), rel=1e-6, abs=1e-8)
+
+
 def test_gqa_equals_mha_with_repeated_kv():
     B, S, hq, hkv, d = 2, 19, 6, 2, 5
     q, k, v, do = _rand((B, S, hq, d), 50), _rand((B, S, hkv, d), 51), _rand((B, S, hkv, d), 52), _rand((B, S, hq, d), 53)
