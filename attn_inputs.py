@@ -81,6 +81,7 @@ class Inputs:
     cu_seqlens: torch.Tensor | None
     lengths: list[int] | None
     kv_factors: list[float] | None
+    cu_seqlens_k: torch.Tensor | None = None   # key boundaries, when they differ from cu_seqlens
 
 
 def make_inputs(w: Workload, device: str | torch.device = "cpu") -> Inputs:
@@ -112,13 +113,21 @@ def make_inputs(w: Workload, device: str | torch.device = "cpu") -> Inputs:
     return Inputs(*out, cu_seqlens=cu, lengths=lengths, kv_factors=factors)
 
 
-def random_inputs(B, Hq, Hkv, Sq, Sk, d, seed, lengths=None, device="cpu", std=1.0):
-    """Small ad-hoc cases for tests (same draw order as the workloads)."""
+def random_inputs(B, Hq, Hkv, Sq, Sk, d, seed, lengths=None, device="cpu", std=1.0,
+                  lengths_k=None):
+    """Small ad-hoc cases for tests (same draw order as the workloads).
+
+    lengths_k (packed only): per-sequence key counts, giving k/v their own
+    rows [Tk, Hkv, d] and boundary list (cu_seqlens_k)."""
     gen = torch.Generator(device="cpu").manual_seed(seed)
+    cu_k = None
     if lengths is not None:
         T = sum(lengths)
-        qs, ks = (T, Hq, d), (T, Hkv, d)
+        Tk = T if lengths_k is None else sum(lengths_k)
+        qs, ks = (T, Hq, d), (Tk, Hkv, d)
         cu = torch.tensor([0] + list(_cumsum(lengths)), dtype=torch.int32)
+        if lengths_k is not None:
+            cu_k = torch.tensor([0] + list(_cumsum(lengths_k)), dtype=torch.int32)
     else:
         qs, ks = (B, Sq, Hq, d), (B, Sk, Hkv, d)
         cu = None
@@ -129,7 +138,9 @@ def random_inputs(B, Hq, Hkv, Sq, Sk, d, seed, lengths=None, device="cpu", std=1
     out = [t.to(torch.bfloat16).to(device) for t in (q, k, v, do)]
     if cu is not None:
         cu = cu.to(device)
-    return Inputs(*out, cu_seqlens=cu, lengths=lengths, kv_factors=None)
+    if cu_k is not None:
+        cu_k = cu_k.to(device)
+    return Inputs(*out, cu_seqlens=cu, lengths=lengths, kv_factors=None, cu_seqlens_k=cu_k)
 
 
 def _cumsum(xs):

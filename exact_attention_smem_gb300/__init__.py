@@ -9,7 +9,8 @@ from __future__ import annotations
 
 import math
 
-from ._lib import (FAError, fa_bwd, fa_bwd_noalloc, fa_bwd_workspace_bytes, fa_debug_set,  # noqa: F401
+from ._lib import (FAError, fa_bwd, fa_bwd_noalloc, fa_bwd_varlen, fa_bwd_workspace_bytes,  # noqa: F401
+                   fa_debug_set, fa_fwd_varlen,
                    fa_debug_set_events, fa_debug_set_trace,
                    fa_exp2_poly_host, fa_fwd, fa_merge, fa_micro, fa_get_device_error, fa_sched_list, fa_test_exp2,
                    fa_test_mma, fa_test_mma_pair, fa_test_wait_timeout, load)
@@ -23,8 +24,10 @@ def _dims(q, k, cu_seqlens):
     return B, Hq, k.shape[2], Sq, k.shape[1], d
 
 
-def forward(q, k, v, causal=False, scale=None, cu_seqlens=None, out=None, lse=None, stream=None):
-    """O, LSE for bf16 q/k/v ([B,S,H,d] dense or [T,H,d] packed with int32 cu_seqlens)."""
+def forward(q, k, v, causal=False, scale=None, cu_seqlens=None, out=None, lse=None, stream=None,
+            cu_seqlens_k=None):
+    """O, LSE for bf16 q/k/v ([B,S,H,d] dense or [T,H,d] packed with int32 cu_seqlens;
+    cu_seqlens_k gives the keys their own boundaries, k/v then [Tk,Hkv,d])."""
     import torch
     B, Hq, Hkv, Sq, Sk, d = _dims(q, k, cu_seqlens)
     scale = 1.0 / math.sqrt(d) if scale is None else scale
@@ -33,12 +36,16 @@ def forward(q, k, v, causal=False, scale=None, cu_seqlens=None, out=None, lse=No
     if lse is None:
         shape = (Hq, Sq) if cu_seqlens is not None else (B, Hq, Sq)
         lse = torch.empty(shape, dtype=torch.float32, device=q.device)
-    fa_fwd(q, k, v, out, lse, B, Hq, Hkv, Sq, Sk, d, causal, scale, cu_seqlens, stream)
+    if cu_seqlens_k is not None:
+        fa_fwd_varlen(q, k, v, out, lse, B, Hq, Hkv, Sq, Sk, d, causal, scale, cu_seqlens,
+                      cu_seqlens_k, stream)
+    else:
+        fa_fwd(q, k, v, out, lse, B, Hq, Hkv, Sq, Sk, d, causal, scale, cu_seqlens, stream)
     return out, lse
 
 
 def backward(q, k, v, o, lse, dout, causal=False, scale=None, cu_seqlens=None, workspace=None,
-             stream=None):
+             stream=None, cu_seqlens_k=None):
     """dQ, dK, dV (bf16) for the forward above."""
     import torch
     B, Hq, Hkv, Sq, Sk, d = _dims(q, k, cu_seqlens)
@@ -47,6 +54,10 @@ def backward(q, k, v, o, lse, dout, causal=False, scale=None, cu_seqlens=None, w
     if workspace is None or workspace.numel() < nbytes:
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, Sq, Sk, d, causal, scale, cu_seqlens,
-           workspace, nbytes, stream)
+    if cu_seqlens_k is not None:
+        fa_bwd_varlen(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, Sq, Sk, d, causal, scale,
+                      cu_seqlens, cu_seqlens_k, workspace, nbytes, stream)
+    else:
+        fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, Sq, Sk, d, causal, scale,
+               cu_seqlens, workspace, nbytes, stream)
     return dq, dk, dv

@@ -35,6 +35,9 @@ _SIGS = {
                     ctypes.c_size_t, _P]),
     "fa_bwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F,
                             _P, _P]),
+    "fa_fwd_varlen": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _P, _P, _P]),
+    "fa_bwd_varlen": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F,
+                           _P, _P, _P, ctypes.c_size_t, _P]),
     "fa_status_string": (ctypes.c_char_p, [_I]),
     "fa_last_error": (ctypes.c_char_p, []),
     "fa_get_device_error": (_I, [ctypes.POINTER(_I), _I]),
@@ -102,6 +105,22 @@ def _check(status, where):
 def fa_fwd(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, d, causal, scale, cu_seqlens=None, stream=None):
     _check(load().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Sq, Sk, d,
                          int(causal), float(scale), _ptr(cu_seqlens), _stream(stream)), "fa_fwd")
+
+
+def fa_fwd_varlen(q, k, v, o, lse, nseq, Hq, Hkv, Tq, Tk, d, causal, scale, cu_q, cu_k,
+                  stream=None):
+    _check(load().fa_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), nseq, Hq, Hkv, Tq,
+                                Tk, d, int(causal), float(scale), _ptr(cu_q), _ptr(cu_k),
+                                _stream(stream)), "fa_fwd_varlen")
+
+
+def fa_bwd_varlen(q, k, v, o, lse, dout, dq, dk, dv, nseq, Hq, Hkv, Tq, Tk, d, causal, scale,
+                  cu_q, cu_k, workspace, workspace_bytes, stream=None):
+    _check(load().fa_bwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout),
+                                _ptr(dq), _ptr(dk), _ptr(dv), nseq, Hq, Hkv, Tq, Tk, d,
+                                int(causal), float(scale), _ptr(cu_q), _ptr(cu_k),
+                                _ptr(workspace), int(workspace_bytes), _stream(stream)),
+           "fa_bwd_varlen")
 
 
 def fa_bwd_workspace_bytes(B, Hq, Sq, d, total_q=0):

@@ -113,8 +113,11 @@ struct Shape {
   bool packed;
 };
 
+// Packed layouts: cu alone gives the boundaries of queries and keys (then
+// Sq == Sk == T); with cu_k the keys have their own boundaries and Sq / Sk are
+// the query / key row counts.
 int validate_common(const void* const* ptrs, int nptrs, int B, int Hq, int Hkv, int Sq, int Sk,
-                    int d, float scale, const int* cu, Shape* sh) {
+                    int d, float scale, const int* cu, Shape* sh, const int* cu_k = nullptr) {
   for (int i = 0; i < nptrs; ++i) {
     if (!ptrs[i]) return fail(FA_ERR_INVALID_ARG, "tensor pointer %d is NULL", i);
     if (!aligned16(ptrs[i]))
@@ -126,11 +129,13 @@ int validate_common(const void* const* ptrs, int nptrs, int B, int Hq, int Hkv, 
   if (d != 64 && d != 128) return fail(FA_ERR_UNSUPPORTED, "head dim %d (supported: 64, 128)", d);
   if (!std::isfinite(scale) || !(scale > 0.f))
     return fail(FA_ERR_INVALID_ARG, "scale must be finite and > 0");
+  if (cu_k && !cu) return fail(FA_ERR_INVALID_ARG, "key boundaries without query boundaries");
   if (cu) {
-    if (Sq != Sk)
+    if (!cu_k && Sq != Sk)
       return fail(FA_ERR_INVALID_ARG, "packed layout: Sq and Sk must both equal the packed "
                   "row count T (got %d, %d)", Sq, Sk);
-    sh->Tq = sh->Tk = Sq;
+    sh->Tq = Sq;
+    sh->Tk = Sk;
     sh->packed = true;
   } else {
     sh->Tq = (long long)B * Sq;
@@ -180,13 +185,14 @@ int* device_error_word() {
 
 using namespace fa;
 
-extern "C" int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
-                      int Hq, int Hkv, int Sq, int Sk, int d, int causal, float scale,
-                      const int* cu_seqlens, void* stream) {
+namespace {
+int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+             int Hkv, int Sq, int Sk, int d, int causal, float scale, const int* cu_seqlens,
+             const int* cu_seqlens_k, void* stream) {
   t_last_error.clear();
   const void* ptrs[5] = {q, k, v, o, lse};
   Shape sh;
-  int st = validate_common(ptrs, 5, B, Hq, Hkv, Sq, Sk, d, scale, cu_seqlens, &sh);
+  int st = validate_common(ptrs, 5, B, Hq, Hkv, Sq, Sk, d, scale, cu_seqlens, &sh, cu_seqlens_k);
   if (st != FA_OK) return st;
   if (B == 0 || sh.Tq == 0) return FA_OK;
   DevInfo* di = nullptr;
@@ -207,6 +213,7 @@ extern "C" int fa_fwd(const void* q, const void* k, const void* v, void* o, floa
   p.o = static_cast<__nv_bfloat16*>(o);
   p.lse = lse;
   p.cu = cu_seqlens;
+  p.cu_k = cu_seqlens_k;
   p.nseq = B;
   p.Hq = Hq;
   p.Hkv = Hkv;
@@ -240,6 +247,27 @@ extern "C" int fa_fwd(const void* q, const void* k, const void* v, void* o, floa
   return FA_OK;
 }
 
+}  // namespace
+
+extern "C" int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                      int Hq, int Hkv, int Sq, int Sk, int d, int causal, float scale,
+                      const int* cu_seqlens, void* stream) {
+  return fwd_impl(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, d, causal, scale, cu_seqlens, nullptr,
+                  stream);
+}
+
+extern "C" int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                             int nseq, int Hq, int Hkv, int Tq, int Tk, int d, int causal,
+                             float scale, const int* cu_seqlens_q, const int* cu_seqlens_k,
+                             void* stream) {
+  if (!cu_seqlens_q || !cu_seqlens_k) {
+    t_last_error = "fa_fwd_varlen needs both boundary lists";
+    return FA_ERR_INVALID_ARG;
+  }
+  return fwd_impl(q, k, v, o, lse, nseq, Hq, Hkv, Tq, Tk, d, causal, scale, cu_seqlens_q,
+                  cu_seqlens_k, stream);
+}
+
 extern "C" size_t fa_bwd_workspace_bytes(int B, int Hq, int Sq, int d, int total_q) {
   if (B < 0 || Hq <= 0 || Sq < 0 || d <= 0 || total_q < 0) return 0;
   const size_t T = total_q > 0 ? (size_t)total_q : (size_t)B * (size_t)Sq;
@@ -248,15 +276,15 @@ extern "C" size_t fa_bwd_workspace_bytes(int B, int Hq, int Sq, int d, int total
   return up(T * Hq * d * sizeof(float)) + 2 * up(P * Hq * sizeof(float));
 }
 
-extern "C" int fa_bwd(const void* q, const void* k, const void* v, const void* o,
-                      const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
-                      int Hq, int Hkv, int Sq, int Sk, int d, int causal, float scale,
-                      const int* cu_seqlens, void* workspace, size_t workspace_bytes,
-                      void* stream) {
+namespace {
+int bwd_impl(const void* q, const void* k, const void* v, const void* o, const float* lse,
+             const void* dout, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Sq,
+             int Sk, int d, int causal, float scale, const int* cu_seqlens,
+             const int* cu_seqlens_k, void* workspace, size_t workspace_bytes, void* stream) {
   t_last_error.clear();
   const void* ptrs[9] = {q, k, v, o, lse, dout, dq, dk, dv};
   Shape sh;
-  int st = validate_common(ptrs, 9, B, Hq, Hkv, Sq, Sk, d, scale, cu_seqlens, &sh);
+  int st = validate_common(ptrs, 9, B, Hq, Hkv, Sq, Sk, d, scale, cu_seqlens, &sh, cu_seqlens_k);
   if (st != FA_OK) return st;
   if (B == 0 || (sh.Tq == 0 && sh.Tk == 0)) return FA_OK;
   const size_t need = fa_bwd_workspace_bytes(B, Hq, Sq, d, sh.packed ? (int)sh.Tq : 0);
@@ -305,6 +333,7 @@ extern "C" int fa_bwd(const void* q, const void* k, const void* v, const void* o
   p.dk = static_cast<__nv_bfloat16*>(dk);
   p.dv = static_cast<__nv_bfloat16*>(dv);
   p.cu = cu_seqlens;
+  p.cu_k = cu_seqlens_k;
   p.nseq = B;
   p.Hq = Hq;
   p.Hkv = Hkv;
@@ -370,6 +399,30 @@ extern "C" int fa_bwd(const void* q, const void* k, const void* v, const void* o
     return fail(FA_ERR_UNSUPPORTED, "backward head dim %d unsupported", d);
   if (e != cudaSuccess) return fail(FA_ERR_CUDA, "backward launch: %s", cudaGetErrorString(e));
   return FA_OK;
+}
+
+}  // namespace
+
+extern "C" int fa_bwd(const void* q, const void* k, const void* v, const void* o,
+                      const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
+                      int Hq, int Hkv, int Sq, int Sk, int d, int causal, float scale,
+                      const int* cu_seqlens, void* workspace, size_t workspace_bytes,
+                      void* stream) {
+  return bwd_impl(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, Sq, Sk, d, causal, scale,
+                  cu_seqlens, nullptr, workspace, workspace_bytes, stream);
+}
+
+extern "C" int fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o,
+                             const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                             int nseq, int Hq, int Hkv, int Tq, int Tk, int d, int causal,
+                             float scale, const int* cu_seqlens_q, const int* cu_seqlens_k,
+                             void* workspace, size_t workspace_bytes, void* stream) {
+  if (!cu_seqlens_q || !cu_seqlens_k) {
+    t_last_error = "fa_bwd_varlen needs both boundary lists";
+    return FA_ERR_INVALID_ARG;
+  }
+  return bwd_impl(q, k, v, o, lse, dout, dq, dk, dv, nseq, Hq, Hkv, Tq, Tk, d, causal, scale,
+                  cu_seqlens_q, cu_seqlens_k, workspace, workspace_bytes, stream);
 }
 
 extern "C" int fa_merge(const void* o_parts, const float* lse_parts, int P, int B, int Hq, int S,

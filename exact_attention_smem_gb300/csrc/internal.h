@@ -63,6 +63,7 @@ struct FwdParams {
   __nv_bfloat16* o;
   float* lse;
   const int* cu;                 // packed boundaries or nullptr
+  const int* cu_k;               // packed key boundaries when they differ from cu, else nullptr
   int nseq, Hq, Hkv, Sq, Sk;     // dense per-sequence lengths (ignored when packed)
   int total_q;                   // rows of the packed/flattened query tensor
   int causal;
@@ -86,7 +87,8 @@ struct BwdParams {
   const float* lse2;             // fp32 [Hq][pad_hstride] padded per sequence: -LSE * log2(e)
   const float* delta;            // fp32 [Hq][pad_hstride] padded: -D_i = -sum_c dO_ic O_ic
   long long pad_hstride;         // floats per head in the padded row arrays
-  const int* cu;
+  const int* cu;                 // packed (query) boundaries or nullptr
+  const int* cu_k;               // packed key boundaries when they differ from cu, else nullptr
   int nseq, Hq, Hkv, Sq, Sk, total_q, total_k, causal;
   float scale_log2, scale;
   int hblock;                    // KV heads per scheduler group (dK/dV units)

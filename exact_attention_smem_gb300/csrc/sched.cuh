@@ -52,13 +52,19 @@ struct SchedSpec {
   int inner;       // rows per inner block: fwd keys per KV block, bwd query rows per block
   int kind;        // 0 forward, 1 backward
   int hblock;      // heads per group (>= 1)
+  const int* cu_k = nullptr;  // packed key boundaries when they differ from cu
 
   __host__ __device__ __forceinline__ void seq(int i, int& qs, int& ql, int& ks, int& kl) const {
     if (cu) {
       qs = cu[i];
       ql = cu[i + 1] - cu[i];
-      ks = qs;
-      kl = ql;
+      if (cu_k) {
+        ks = cu_k[i];
+        kl = cu_k[i + 1] - cu_k[i];
+      } else {
+        ks = qs;
+        kl = ql;
+      }
     } else {
       qs = i * Sq;
       ql = Sq;

@@ -115,6 +115,29 @@ FA_API int fa_bwd_noalloc(const void* q, const void* k, const void* v, const voi
                           const int* cu_seqlens, void* stream);
 
 /*
+ * Packed variable-length attention with separate query and key boundaries
+ * (e.g. prefill over cached keys: a sequence may have more keys than
+ * queries, or fewer). Sequence i's queries are rows [cu_seqlens_q[i],
+ * cu_seqlens_q[i+1]) of q/o/dout/dq ([Tq,Hq,d]) and its keys rows
+ * [cu_seqlens_k[i], cu_seqlens_k[i+1]) of k/v/dk/dv ([Tk,Hkv,d]); causal masking
+ * is bottom-right aligned per sequence (key j visible to query i iff
+ * j <= i + k_len - q_len), as in the dense Sq != Sk case. LSE is [Hq,Tq]. Both
+ * lists are device int32 arrays of nseq+1 non-decreasing entries from 0 to
+ * Tq / Tk. Same method and errors as fa_fwd / fa_bwd (the pages' "variable
+ * sequence lengths": "FlashAttention-4: Algorithm and Kernel Pipelining
+ * Co-Design for Asymmetric Hardware Scaling", Summary); fa_bwd_varlen's
+ * workspace is fa_bwd_workspace_bytes(nseq, Hq, Tq, d, Tq) bytes.
+ */
+FA_API int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                         int nseq, int Hq, int Hkv, int Tq, int Tk, int d, int causal, float scale,
+                         const int* cu_seqlens_q, const int* cu_seqlens_k, void* stream);
+FA_API int fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o,
+                         const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                         int nseq, int Hq, int Hkv, int Tq, int Tk, int d, int causal, float scale,
+                         const int* cu_seqlens_q, const int* cu_seqlens_k, void* workspace,
+                         size_t workspace_bytes, void* stream);
+
+/*
  * Combine step of context parallelism (K/V split into disjoint shards, each
  * shard's forward run separately): given, for the same queries, part p's O_p
  * and LSE_p from fa_fwd over key set p, writes the attention over the union

@@ -36,7 +36,8 @@ def max_abs(got, ref):
     sel = ~np.isnan(ref)
     g, r = g[sel], ref[sel]
     same_inf = np.isinf(g) & np.isinf(r) & (np.sign(g) == np.sign(r))
-    d = np.where(same_inf, 0.0, np.abs(g - r))
+    with np.errstate(invalid="ignore"):                  # inf - inf where both are +inf
+        d = np.where(same_inf, 0.0, np.abs(g - r))
     d = np.where(np.isnan(d), np.inf, d)
     return float(d.max()) if d.size else 0.0
 
