@@ -237,7 +237,7 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   if (grid < 1) grid = 1;
   // The forward keeps one group (pure LPT): its K/V traffic is far from the
   // DRAM roof, and static snake rounds balance best over a single LPT list.
-  p.hblock = Hq;
+  p.hblock = kn.fwd_hblock > 0 && kn.fwd_hblock < Hq ? kn.fwd_hblock : Hq;
   cudaEvent_t ev0, ev1;
   take_events(0, &ev0, &ev1);
   if (ev0) cudaEventRecord(ev0, static_cast<cudaStream_t>(stream));
@@ -491,6 +491,9 @@ extern "C" int fa_debug_set(const char* key, double value) {
     if (value != 0.0 && value != 1.0 && value != 2.0)
       return fail(FA_ERR_INVALID_ARG, "bwd_mode in {0, 1, 2}");
     g_knobs.bwd_mode = (int)value;
+  } else if (!strcmp(key, "fwd_hblock")) {
+    if (!(value >= 0.0 && value <= 65536.0)) return fail(FA_ERR_INVALID_ARG, "fwd_hblock");
+    g_knobs.fwd_hblock = (int)value;
   } else if (!strcmp(key, "timeout_ms")) {
     if (!(value >= 1.0 && value <= 60000.0)) return fail(FA_ERR_INVALID_ARG, "timeout_ms");
     g_knobs.timeout_ns = (long long)(value * 1e6);
