@@ -59,7 +59,9 @@ class Clocks:
     def __init__(self, gpu_index):
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        import tempfile
+        fd, self.path = tempfile.mkstemp(prefix="fa_clocks_", suffix=".csv")
+        os.close(fd)
 
     def __enter__(self):
         try:

@@ -1,8 +1,8 @@
 """Microbenchmarks that size the exponential split and the tensor-core
 denominator on the GPU at hand: MUFU ex2 vs the FMA-pipe polynomial
 (exponentials per clock per SM) and tcgen05 bf16 MMA throughput (FLOP per clock
-per SM). Results are printed and, when a ``gpurun_out/`` folder exists, saved
-as JSON for the profile summaries."""
+per SM). Results are printed and, when the environment variable FA_MICRO_OUT
+names a directory, saved there as micro.json for the profile summaries."""
 import json
 import os
 
@@ -53,9 +53,9 @@ def test_microbenchmarks():
            "mma_bf16_flop_per_clk_per_sm": mma,
            "mma_flop_per_clk_per_sm_by_shape": dict(ss_n256=mma, **shapes)}
     print(json.dumps(res))
-    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-    if os.path.isdir(os.path.join(root, "gpurun_out")):
-        with open(os.path.join(root, "gpurun_out", "micro.json"), "w") as f:
+    out_dir = os.environ.get("FA_MICRO_OUT")
+    if out_dir and os.path.isdir(out_dir):
+        with open(os.path.join(out_dir, "micro.json"), "w") as f:
             json.dump(res, f)
     assert 1 <= mufu <= 256 and 1 <= poly <= 256
     assert 1000 <= mma <= 65536
