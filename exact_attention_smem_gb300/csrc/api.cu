@@ -126,7 +126,8 @@ int validate_common(const void* const* ptrs, int nptrs, int B, int Hq, int Hkv, 
   if (B < 0 || Hq <= 0 || Hkv <= 0 || Sq < 0 || Sk < 0)
     return fail(FA_ERR_INVALID_ARG, "bad sizes B=%d Hq=%d Hkv=%d Sq=%d Sk=%d", B, Hq, Hkv, Sq, Sk);
   if (Hq % Hkv != 0) return fail(FA_ERR_INVALID_ARG, "Hq (%d) %% Hkv (%d) != 0", Hq, Hkv);
-  if (d != 64 && d != 128) return fail(FA_ERR_UNSUPPORTED, "head dim %d (supported: 64, 128)", d);
+  if (d != 64 && d != 128 && d != 192 && d != 256)
+    return fail(FA_ERR_UNSUPPORTED, "head dim %d (supported: 64, 128; forward also 192, 256)", d);
   if (!std::isfinite(scale) || !(scale > 0.f))
     return fail(FA_ERR_INVALID_ARG, "scale must be finite and > 0");
   if (cu_k && !cu) return fail(FA_ERR_INVALID_ARG, "key boundaries without query boundaries");
@@ -202,9 +203,10 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   FwdParams p;
   memset(&p, 0, sizeof(p));
   if ((st = encode_rows(&p.tm_q, q, sh.Tq, Hq, d)) != FA_OK) return st;
+  const int kv_box = d > 128 ? 64 : 128;             // keys per K/V block of the kernel
   if (sh.Tk > 0) {
-    if ((st = encode_rows(&p.tm_k, k, sh.Tk, Hkv, d)) != FA_OK) return st;
-    if ((st = encode_rows(&p.tm_v, v, sh.Tk, Hkv, d)) != FA_OK) return st;
+    if ((st = encode_rows(&p.tm_k, k, sh.Tk, Hkv, d, kv_box)) != FA_OK) return st;
+    if ((st = encode_rows(&p.tm_v, v, sh.Tk, Hkv, d, kv_box)) != FA_OK) return st;
   } else {
     // no keys at all: every row is fully masked; maps are never used by the TMA
     if ((st = encode_rows(&p.tm_k, q, sh.Tq, Hq, d)) != FA_OK) return st;
@@ -229,8 +231,10 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   p.timeout_ns = (unsigned long long)kn.timeout_ns;
 
   // persistent grid: one CTA per SM, capped by an upper bound on the unit count
+  const int unit_rows = d > 128 ? 128 : 256;         // query rows per unit of the kernel
   const long long units_per_head =
-      sh.packed ? (sh.Tq + 255) / 256 + B : (long long)B * ((Sq + 255) / 256);
+      sh.packed ? (sh.Tq + unit_rows - 1) / unit_rows + B
+                : (long long)B * ((Sq + unit_rows - 1) / unit_rows);
   const long long units = units_per_head * Hq;
   int grid = kn.grid_override > 0 ? kn.grid_override : di->sms;
   if (units < grid) grid = (int)units;
@@ -241,7 +245,8 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
   cudaEvent_t ev0, ev1;
   take_events(0, &ev0, &ev1);
   if (ev0) cudaEventRecord(ev0, static_cast<cudaStream_t>(stream));
-  cudaError_t e = launch_fwd(p, d, grid, static_cast<cudaStream_t>(stream), kn.poly8);
+  cudaError_t e = d > 128 ? launch_fwd_big(p, d, grid, static_cast<cudaStream_t>(stream), kn.poly8)
+                          : launch_fwd(p, d, grid, static_cast<cudaStream_t>(stream), kn.poly8);
   if (ev1) cudaEventRecord(ev1, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(FA_ERR_CUDA, "forward launch: %s", cudaGetErrorString(e));
   return FA_OK;
@@ -286,6 +291,7 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const f
   Shape sh;
   int st = validate_common(ptrs, 9, B, Hq, Hkv, Sq, Sk, d, scale, cu_seqlens, &sh, cu_seqlens_k);
   if (st != FA_OK) return st;
+  if (d > 128) return fail(FA_ERR_UNSUPPORTED, "backward head dim %d (supported: 64, 128)", d);
   if (B == 0 || (sh.Tq == 0 && sh.Tk == 0)) return FA_OK;
   const size_t need = fa_bwd_workspace_bytes(B, Hq, Sq, d, sh.packed ? (int)sh.Tq : 0);
   if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
@@ -433,7 +439,8 @@ extern "C" int fa_merge(const void* o_parts, const float* lse_parts, int P, int 
     if (!ptrs[i]) return fail(FA_ERR_INVALID_ARG, "pointer %d is NULL", i);
   if (P < 1 || P > 64) return fail(FA_ERR_INVALID_ARG, "parts P=%d (1..64)", P);
   if (B < 0 || Hq <= 0 || S < 0) return fail(FA_ERR_INVALID_ARG, "bad sizes B=%d Hq=%d S=%d", B, Hq, S);
-  if (d != 64 && d != 128) return fail(FA_ERR_UNSUPPORTED, "head dim %d (supported: 64, 128)", d);
+  if (d != 64 && d != 128 && d != 192 && d != 256)
+    return fail(FA_ERR_UNSUPPORTED, "head dim %d (supported: 64, 128, 192, 256)", d);
   const long long rows = packed ? (long long)S : (long long)B * S;
   if (rows == 0) return FA_OK;
   DevInfo* di = nullptr;

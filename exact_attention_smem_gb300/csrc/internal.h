@@ -112,6 +112,7 @@ __host__ __device__ __forceinline__ long long pad_hstride(long long T, int nseq)
 
 // Launchers (fwd.cu / bwd.cu). Return a cudaError_t.
 cudaError_t launch_fwd(const FwdParams& p, int d, int grid, cudaStream_t stream, int poly8);
+cudaError_t launch_fwd_big(const FwdParams& p, int d, int grid, cudaStream_t stream, int poly8);
 int fwd_units_total(const FwdParams& p);
 struct BwdAux {                  // inputs of the preprocess / convert passes
   const __nv_bfloat16* o;

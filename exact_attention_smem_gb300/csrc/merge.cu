@@ -51,7 +51,7 @@ __global__ void merge_kernel(const __nv_bfloat16* __restrict__ o_parts,
       continue;
     }
     float wsum = 0.f;
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};                // columns lane, lane+32, ... (d <= 128)
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // columns lane + 32e (d <= 256)
     for (int q = 0; q < P; ++q) {
       const float l = lse_parts[q * part_l + li];
       if (l == INFINITY) continue;
@@ -59,14 +59,14 @@ __global__ void merge_kernel(const __nv_bfloat16* __restrict__ o_parts,
       wsum += wq;
       const __nv_bfloat16* prow = o_parts + q * part_o + rh * d;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
+      for (int e = 0; e < 8; ++e) {
         const int c = lane + 32 * e;
         if (c < d) acc[e] = fmaf(wq, __bfloat162float(prow[c]), acc[e]);
       }
     }
     const float inv = 1.0f / wsum;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
+    for (int e = 0; e < 8; ++e) {
       const int c = lane + 32 * e;
       if (c < d) orow[c] = __float2bfloat16(acc[e] * inv);
     }

@@ -26,7 +26,8 @@
  *     [T][Hkv][d]; lse is fp32 [Hq][T]. Sequence i owns rows
  *     [cu_seqlens[i], cu_seqlens[i+1]) of every tensor (self-attention: one
  *     boundary list for queries and keys).
- *   - d (head dimension) is 64 or 128; scale must be finite and > 0.
+ *   - d (head dimension) is 64 or 128 (the forward and fa_merge also take 192
+ *     and 256); scale must be finite and > 0.
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
  *     stream). FA_OK means "validated and enqueued". The library allocates no
  *     memory on any call and keeps no per-call state; the caller owns all
@@ -54,7 +55,7 @@ extern "C" {
 typedef enum {
   FA_OK = 0,
   FA_ERR_INVALID_ARG = 1,  /* bad pointer, size, alignment or layout */
-  FA_ERR_UNSUPPORTED = 2,  /* valid but not supported (e.g. d not in {64,128}) */
+  FA_ERR_UNSUPPORTED = 2,  /* valid but not supported (e.g. a head dim not listed) */
   FA_ERR_ARCH = 3,         /* current device is not compute capability 10.3 */
   FA_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed; see fa_last_error() */
   FA_ERR_WORKSPACE = 5,    /* backward workspace missing or too small */
@@ -155,7 +156,8 @@ FA_API int fa_bwd_varlen(const void* q, const void* k, const void* v, const void
  *             ([B,Hq,S] dense, [Hq,T] packed)
  *   packed    0 dense, 1 packed (B is then unused)
  *   o, lse    outputs in the same layouts (must not alias the parts)
- * 1 <= P <= 64, d in {64, 128}. Asynchronous on `stream`; allocates nothing.
+ * 1 <= P <= 64, d in {64, 128, 192, 256}. Asynchronous on `stream`; allocates
+ * nothing.
  */
 FA_API int fa_merge(const void* o_parts, const float* lse_parts, int P, int B, int Hq, int S,
                     int d, int packed, void* o, float* lse, void* stream);

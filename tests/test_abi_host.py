@@ -49,7 +49,7 @@ def _fwd(lib, **kw):
 
 @pytest.mark.parametrize("kw,status", [
     (dict(q=None), 1), (dict(lse=None), 1), (dict(v=FAKE + 8), 1), (dict(d=96), 2),
-    (dict(d=256), 2), (dict(Hq=3, Hkv=2), 1), (dict(Hkv=0), 1), (dict(scale=float("nan")), 1),
+    (dict(d=320), 2), (dict(Hq=3, Hkv=2), 1), (dict(Hkv=0), 1), (dict(scale=float("nan")), 1),
     (dict(scale=-1.0), 1), (dict(scale=float("inf")), 1), (dict(Sq=-1), 1),
     (dict(cu=FAKE, Sq=16, Sk=8), 1),
 ])
@@ -74,6 +74,9 @@ def test_backward_validation_and_workspace(lib):
     assert lib.fa_bwd(*args, FAKE, need - 1, None) == 5
     assert lib.fa_bwd(*args, FAKE + 16, need, None) == 5      # workspace must be 256-aligned
     assert lib.fa_bwd(*args, None, need, None) == 5
+    # head dims 192 and 256 have a forward only
+    big = [FAKE] * 9 + [2, 4, 4, 100, 100, 256, 1, 0.1, None]
+    assert lib.fa_bwd(*big, FAKE, 1 << 30, None) == 2
     bad = [FAKE] * 8 + [None] + [2, 4, 4, 100, 100, 128, 1, 0.1, None]
     assert lib.fa_bwd(*bad, FAKE, need, None) == 1
 
