@@ -23,7 +23,9 @@
 // over the same list, so they agree on the unit sequence without
 // communicating. Dense layouts seek directly (O(log) per unit, seek_dense);
 // packed layouts walk the list group by group ((cost level, sequence) groups
-// of consecutive row blocks), one step per group passed.
+// of consecutive row blocks): every CTA passes every (level, sequence) pair
+// once, at two cost evaluations for a pair outside the sequence's cost range
+// (a few hundred sequences cost well under a millisecond).
 //
 // Host and device share this code; the host build backs the scheduler tests.
 #pragma once
@@ -180,7 +182,12 @@ struct Walker {
         }
       }
       s.seq(seq_i, qs, ql, ks, kl);
-      if (s.nblocks(ql, kl) == 0) continue;
+      const int nb = s.nblocks(ql, kl);
+      if (nb == 0) continue;
+      // costs are monotone in the block index: the end blocks bound this
+      // sequence's levels, so most (level, sequence) pairs skip the searches
+      const int c0 = s.cost(0, ql, kl), c1 = s.cost(nb - 1, ql, kl);
+      if (level < (c0 < c1 ? c0 : c1) || level > (c0 < c1 ? c1 : c0)) continue;
       s.range(level, ql, kl, lo, hi);
       if (hi > lo) return;
     }
