@@ -278,7 +278,9 @@ extern "C" size_t fa_bwd_workspace_bytes(int B, int Hq, int Sq, int d, int total
   const size_t T = total_q > 0 ? (size_t)total_q : (size_t)B * (size_t)Sq;
   auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
   const size_t P = (size_t)pad_hstride((long long)T, B);
-  return up(T * Hq * d * sizeof(float)) + 2 * up(P * Hq * sizeof(float));
+  // + the query and key boundary lists back to back (separate key boundaries)
+  return up(T * Hq * d * sizeof(float)) + 2 * up(P * Hq * sizeof(float)) +
+         up(2 * ((size_t)B + 1) * sizeof(int));
 }
 
 namespace {
@@ -339,7 +341,21 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const f
   p.dk = static_cast<__nv_bfloat16*>(dk);
   p.dv = static_cast<__nv_bfloat16*>(dv);
   p.cu = cu_seqlens;
-  p.cu_k = cu_seqlens_k;
+  p.k_off = 0;
+  if (cu_seqlens_k) {
+    // The kernels take one list: the query boundaries, then the key boundaries
+    // (a single pointer keeps the scheduler's registers as in the one-list case).
+    int* both = reinterpret_cast<int*>(ws + up(T * Hq * d * sizeof(float)) +
+                                       2 * up(P * Hq * sizeof(float)));
+    const size_t nb = ((size_t)B + 1) * sizeof(int);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t ce = cudaMemcpyAsync(both, cu_seqlens, nb, cudaMemcpyDeviceToDevice, s);
+    if (ce == cudaSuccess)
+      ce = cudaMemcpyAsync(both + B + 1, cu_seqlens_k, nb, cudaMemcpyDeviceToDevice, s);
+    if (ce != cudaSuccess) return fail(FA_ERR_CUDA, "boundary copy: %s", cudaGetErrorString(ce));
+    p.cu = both;
+    p.k_off = B + 1;
+  }
   p.nseq = B;
   p.Hq = Hq;
   p.Hkv = Hkv;

@@ -212,20 +212,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_kernel(const __grid_consta
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
   }
-  // packed boundaries in shared memory when they fit (query list, then key list)
-  const int ncu = p.cu_k ? 2 * (p.nseq + 1) : p.nseq + 1;
+  // packed boundaries in shared memory when they fit (query list, then the key
+  // list when it differs; the host stores the two back to back)
+  const int ncu = p.k_off ? 2 * (p.nseq + 1) : p.nseq + 1;
   const bool cu_in_smem = p.cu != nullptr && ncu <= MAX_SEQ_SMEM + 1;
   if (cu_in_smem)
-    for (int i = threadIdx.x; i < ncu; i += NUM_THREADS)
-      cu_s[i] = i <= p.nseq ? p.cu[i] : p.cu_k[i - p.nseq - 1];
-  const int* cu_k_spec = p.cu_k ? (cu_in_smem ? cu_s + p.nseq + 1 : p.cu_k) : nullptr;
+    for (int i = threadIdx.x; i < ncu; i += NUM_THREADS) cu_s[i] = p.cu[i];
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
   const SchedSpec spec{cu_in_smem ? cu_s : p.cu, p.nseq, p.Sq, p.Sk, p.Hkv, p.causal, BN, BMQ, 1,
-                       p.hblock, cu_k_spec};
+                       p.hblock, nullptr, p.k_off};
   const WaitCtl wc{p.err, abort_flag, p.timeout_ns};
   const int G = gridDim.x;
   const int cta = blockIdx.x;

@@ -88,8 +88,8 @@ struct BwdParams {
   const float* lse2;             // fp32 [Hq][pad_hstride] padded per sequence: -LSE * log2(e)
   const float* delta;            // fp32 [Hq][pad_hstride] padded: -D_i = -sum_c dO_ic O_ic
   long long pad_hstride;         // floats per head in the padded row arrays
-  const int* cu;                 // packed (query) boundaries or nullptr
-  const int* cu_k;               // packed key boundaries when they differ from cu, else nullptr
+  const int* cu;                 // packed boundaries or nullptr: the query list, then (k_off > 0)
+  int k_off;                     // the key list at cu[k_off..]; 0 when keys share the query list
   int nseq, Hq, Hkv, Sq, Sk, total_q, total_k, causal;
   float scale_log2, scale;
   int hblock;                    // KV heads per scheduler group (dK/dV units)

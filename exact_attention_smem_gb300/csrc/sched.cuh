@@ -54,7 +54,8 @@ struct SchedSpec {
   int inner;       // rows per inner block: fwd keys per KV block, bwd query rows per block
   int kind;        // 0 forward, 1 backward
   int hblock;      // heads per group (>= 1)
-  const int* cu_k = nullptr;  // packed key boundaries when they differ from cu
+  const int* cu_k = nullptr;  // packed key boundaries when they differ from cu, or
+  int k_off = 0;              // else at cu[k_off + i] (0: the query boundaries)
 
   __host__ __device__ __forceinline__ void seq(int i, int& qs, int& ql, int& ks, int& kl) const {
     if (cu) {
@@ -64,8 +65,8 @@ struct SchedSpec {
         ks = cu_k[i];
         kl = cu_k[i + 1] - cu_k[i];
       } else {
-        ks = qs;
-        kl = ql;
+        ks = cu[k_off + i];
+        kl = cu[k_off + i + 1] - ks;
       }
     } else {
       qs = i * Sq;

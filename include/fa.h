@@ -74,21 +74,27 @@ FA_API int fa_fwd(const void* q, const void* k, const void* v, void* o, float* l
            void* stream);
 
 /*
- * Bytes of device workspace fa_bwd needs: fp32 dQ accumulator [T][Hq][d], the
- * fp32 row terms D_i = sum_c dO_ic O_ic and LSE*log2(e) ([Hq][T] each), with
- * T = B*Sq (dense) or total_q (packed, pass the packed row count; 0 = dense).
+ * Bytes of device workspace fa_bwd / fa_bwd_varlen need: an fp32 dQ
+ * accumulator [T][Hq][d] (used by the one-pass form only), the fp32 row terms
+ * -D_i = -sum_c dO_ic O_ic and -LSE*log2(e) ([Hq][P] each, P = T padded per
+ * sequence), and room for two boundary lists of B+1 ints (fa_bwd_varlen copies
+ * its query and key boundaries there, back to back), each region rounded up to
+ * 256 bytes; T = B*Sq (dense) or total_q (packed, pass the packed row count;
+ * 0 = dense).
  */
 FA_API size_t fa_bwd_workspace_bytes(int B, int Hq, int Sq, int d, int total_q);
 
 /*
  * Backward: dq, dk, dv (bf16) from q, k, v, o, lse (as written by fa_fwd) and
  * dout. dk/dv of a KV head are summed over the query heads of its group.
- * Runs three kernels on `stream`: a preprocess (D, LSE*log2e, zeroed dQ
- * accumulator), the main kernel (dK, dV and fp32 dQ partial sums added
- * atomically), and a convert pass dQ = bf16(scale * accumulator). `workspace`
- * (device, 256-byte aligned, >= fa_bwd_workspace_bytes) is scratch owned by
- * the caller; its contents on entry do not matter. dQ accumulation order is
- * not fixed, so dq may differ in the last bits between runs.
+ * Runs three kernels on `stream`: a preprocess (the row terms -D and
+ * -LSE*log2e), a dK/dV pass over key blocks and a dQ pass over query blocks.
+ * Every output element is written by one CTA with a fixed summation order (no
+ * atomics), so results are bitwise reproducible. `workspace` (device, 256-byte
+ * aligned, >= fa_bwd_workspace_bytes) is scratch owned by the caller; its
+ * contents on entry do not matter. (The one-pass form selectable with
+ * fa_debug_set("bwd_mode", 0) accumulates dQ with fp32 atomics instead, so its
+ * dq may differ in the last bits between runs.)
  */
 FA_API int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
            const void* dout, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Sq,
@@ -185,6 +191,10 @@ FA_API int fa_get_device_error(int* code, int clear);
  *   "bwd_poly8"  the same for the backward
  *   "timeout_ms" bounded-wait deadline in milliseconds (default 2000)
  *   "grid"       persistent grid size override (0 = one CTA per SM)
+ *   "bwd_mode"   backward form: 1 two passes (default), 2 the same with the
+ *                dK/dV pass on CTA pairs (cta_group::2, head dim 128), 0 one
+ *                pass with fp32 dQ atomics and a convert pass (head dim 128)
+ *   "fwd_hblock" forward heads per scheduler group (0 = all heads, default)
  * Returns FA_OK or FA_ERR_INVALID_ARG. Process-wide; not thread-safe with
  * concurrent launches.
  */

@@ -68,8 +68,8 @@ def test_backward_validation_and_workspace(lib):
     # fp32 row arrays [Hq][P], P = round_up(T, 128) + 256 * (nseq + 1), each
     # part rounded up to 256 bytes
     need = lib.fa_bwd_workspace_bytes(2, 4, 100, 128, 0)
-    assert need == 200 * 4 * 128 * 4 + 2 * (1024 * 4 * 4)
-    assert lib.fa_bwd_workspace_bytes(1, 4, 300, 64, 512) == 512 * 4 * 64 * 4 + 2 * (1024 * 4 * 4)
+    assert need == 200 * 4 * 128 * 4 + 2 * (1024 * 4 * 4) + 256   # + boundary lists (3 ints each)
+    assert lib.fa_bwd_workspace_bytes(1, 4, 300, 64, 512) == 512 * 4 * 64 * 4 + 2 * (1024 * 4 * 4) + 256
     args = [FAKE] * 9 + [2, 4, 4, 100, 100, 128, 1, 0.1, None]
     assert lib.fa_bwd(*args, FAKE, need - 1, None) == 5
     assert lib.fa_bwd(*args, FAKE + 16, need, None) == 5      # workspace must be 256-aligned
