@@ -9,3 +9,4 @@ differences, a library special case and hand-derived golden values).
 from .attention_fp64 import (attend_head, attend_head_backward, backward, forward)  # noqa: F401
 from .online_softmax import online_attend_head  # noqa: F401
 from .exp2_method import exp2_exact, exp2_range_reduced, fit_exp2_poly  # noqa: F401
+from . import fp8_e4m3  # noqa: F401
