@@ -10,10 +10,10 @@ from __future__ import annotations
 import math
 
 from ._lib import (FAError, fa_bwd, fa_bwd_noalloc, fa_bwd_varlen, fa_bwd_workspace_bytes,  # noqa: F401
-                   fa_debug_set, fa_fwd_varlen,
+                   fa_debug_set, fa_fwd_varlen, fa_fwd_fp8, fa_quantize_fp8,
                    fa_debug_set_events, fa_debug_set_trace,
                    fa_exp2_poly_host, fa_fwd, fa_merge, fa_micro, fa_get_device_error, fa_sched_list, fa_test_exp2,
-                   fa_test_mma, fa_test_mma_pair, fa_test_wait_timeout, load)
+                   fa_test_mma, fa_test_mma_fp8, fa_test_mma_pair, fa_test_wait_timeout, load)
 
 
 def _dims(q, k, cu_seqlens):
@@ -61,3 +61,35 @@ def backward(q, k, v, o, lse, dout, causal=False, scale=None, cu_seqlens=None, w
         fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, Sq, Sk, d, causal, scale,
                cu_seqlens, workspace, nbytes, stream)
     return dq, dk, dv
+
+
+def quantize_fp8(x, layout):
+    """e4m3 codes and scales of a bf16 [B,S,H,d] tensor: layout 0 (Q, K) gives
+    codes [B,S,H,d] and scales [B,H,ceil(S/128)]; layout 1 (V) gives codes
+    [B,H,d,S_pad] (keys contiguous, S_pad = S rounded up to 16) and scales [B,H]."""
+    import torch
+    B, S, H, d = x.shape
+    if layout == 0:
+        codes = torch.empty((B, S, H, d), dtype=torch.uint8, device=x.device)
+        scales = torch.empty((B, H, (S + 127) // 128), dtype=torch.float32, device=x.device)
+    else:
+        codes = torch.empty((B, H, d, (S + 15) // 16 * 16), dtype=torch.uint8, device=x.device)
+        scales = torch.empty((B, H), dtype=torch.float32, device=x.device)
+    fa_quantize_fp8(x, B, S, H, d, layout, codes, scales)
+    return codes, scales
+
+
+def forward_fp8(q8, q_scale, k8, k_scale, vt8, v_scale, causal=False, scale=None, out=None,
+                lse=None, stream=None):
+    """O (bf16), LSE for e4m3 inputs from quantize_fp8 (dense layouts, d = 128)."""
+    import torch
+    B, Sq, Hq, d = q8.shape
+    Sk, Hkv = k8.shape[1], k8.shape[2]
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    if out is None:
+        out = torch.empty((B, Sq, Hq, d), dtype=torch.bfloat16, device=q8.device)
+    if lse is None:
+        lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q8.device)
+    fa_fwd_fp8(q8, k8, vt8, q_scale, k_scale, v_scale, out, lse, B, Hq, Hkv, Sq, Sk, d, causal,
+               scale, stream)
+    return out, lse

@@ -50,6 +50,10 @@ _SIGS = {
     "fa_test_mma": (_I, [_P, _P, _P, _I, _I, _P]),
     "fa_merge": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P]),
     "fa_test_mma_pair": (_I, [_P, _P, _P, _P, _I, _I, _P]),
+    "fa_test_mma_fp8": (_I, [_P, _P, _P, _I, _I, _P]),
+    "fa_quantize_fp8": (_I, [_P, _I, _I, _I, _I, _I, _P, _P, _P]),
+    "fa_fwd_fp8": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, ctypes.c_float,
+                        _P]),
     "fa_test_wait_timeout": (_I, [_P, ctypes.c_double, _P]),
     "fa_sched_list": (_I, [_I, _I, _P, _I, _I, _I, _I, _I, _I, _I, _P, _I]),
 }
@@ -196,6 +200,23 @@ def fa_merge(o_parts, lse_parts, P, B, Hq, S, d, packed, o, lse, stream=None):
 def fa_test_mma_pair(A, B, C, flags, mode, N, stream=None):
     _check(load().fa_test_mma_pair(_ptr(A), _ptr(B), _ptr(C), _ptr(flags), mode, N,
                                    _stream(stream)), "fa_test_mma_pair")
+
+
+def fa_quantize_fp8(x, B, S, H, d, layout, codes, scales, stream=None):
+    _check(load().fa_quantize_fp8(_ptr(x), B, S, H, d, layout, _ptr(codes), _ptr(scales),
+                                  _stream(stream)), "fa_quantize_fp8")
+
+
+def fa_fwd_fp8(q8, k8, vt8, q_scale, k_scale, v_scale, o, lse, B, Hq, Hkv, Sq, Sk, d, causal,
+               scale, stream=None):
+    _check(load().fa_fwd_fp8(_ptr(q8), _ptr(k8), _ptr(vt8), _ptr(q_scale), _ptr(k_scale),
+                             _ptr(v_scale), _ptr(o), _ptr(lse), B, Hq, Hkv, Sq, Sk, d,
+                             int(causal), float(scale), _stream(stream)), "fa_fwd_fp8")
+
+
+def fa_test_mma_fp8(A, B, C, mode, N, stream=None):
+    _check(load().fa_test_mma_fp8(_ptr(A), _ptr(B), _ptr(C), mode, N, _stream(stream)),
+           "fa_test_mma_fp8")
 
 
 def fa_test_wait_timeout(status_dev, timeout_ms, stream=None):

@@ -9,6 +9,7 @@
 
 #include <cmath>
 #include <cstdarg>
+#include <cstdint>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -24,6 +25,8 @@ cudaError_t launch_wait_timeout_probe(int* status, unsigned long long timeout_ns
 cudaError_t launch_mma_pair_probe(const __nv_bfloat16* A, const __nv_bfloat16* B, float* C,
                                   int* flags, int mode, int N, cudaStream_t st);
 cudaError_t launch_micro(int kind, int iters, double* out, int ctas, cudaStream_t st);
+cudaError_t launch_mma_fp8_probe(const uint8_t* A, const uint8_t* B, float* C, int mode, int N,
+                                 cudaStream_t st);
 
 __device__ int g_error_word;  // first expired bounded wait (site code), per device
 
@@ -101,6 +104,18 @@ int encode_rows(CUtensorMap* tm, const void* ptr, long long rows, int heads, int
   cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = g_encode(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return FA_OK;
+}
+
+// e4m3 codes: a 3-D view (innermost first) with 128-byte rows of 128 codes.
+int encode_u8(CUtensorMap* tm, const void* ptr, const cuuint64_t (&dims)[3],
+              const cuuint64_t (&strides)[2], const cuuint32_t (&box)[3]) {
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr), dims,
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -271,6 +286,107 @@ extern "C" int fa_fwd_varlen(const void* q, const void* k, const void* v, void* 
   }
   return fwd_impl(q, k, v, o, lse, nseq, Hq, Hkv, Tq, Tk, d, causal, scale, cu_seqlens_q,
                   cu_seqlens_k, stream);
+}
+
+extern "C" int fa_quantize_fp8(const void* x, int B, int S, int H, int d, int layout, void* codes,
+                               float* scales, void* stream) {
+  t_last_error.clear();
+  if (!x || !codes || !scales) return fail(FA_ERR_INVALID_ARG, "NULL pointer");
+  if (!aligned16(x) || !aligned16(codes))
+    return fail(FA_ERR_INVALID_ARG, "x and codes must be 16-byte aligned");
+  if (B < 0 || S < 0 || H <= 0) return fail(FA_ERR_INVALID_ARG, "bad sizes B=%d S=%d H=%d", B, S, H);
+  if (layout != 0 && layout != 1) return fail(FA_ERR_INVALID_ARG, "layout must be 0 or 1");
+  if (d != 64 && d != 128) return fail(FA_ERR_UNSUPPORTED, "head dim %d (supported: 64, 128)", d);
+  if ((long long)B * H > (1LL << 30) || (long long)S * H * d > (1LL << 40))
+    return fail(FA_ERR_INVALID_ARG, "sizes too large");
+  DevInfo* di = nullptr;
+  int st = device_info(&di);
+  if (st != FA_OK) return st;
+  cudaError_t e = launch_quantize_fp8(static_cast<const __nv_bfloat16*>(x), B, S, H, d, layout,
+                                      static_cast<uint8_t*>(codes), scales,
+                                      static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : fail(FA_ERR_CUDA, "quantize launch: %s", cudaGetErrorString(e));
+}
+
+extern "C" int fa_fwd_fp8(const void* q8, const void* k8, const void* vt8, const float* q_scale,
+                          const float* k_scale, const float* v_scale, void* o, float* lse, int B,
+                          int Hq, int Hkv, int Sq, int Sk, int d, int causal, float scale,
+                          void* stream) {
+  t_last_error.clear();
+  const void* ptrs[8] = {q8, k8, vt8, q_scale, k_scale, v_scale, o, lse};
+  for (int i = 0; i < 8; ++i)
+    if (!ptrs[i]) return fail(FA_ERR_INVALID_ARG, "tensor pointer %d is NULL", i);
+  if (!aligned16(q8) || !aligned16(k8) || !aligned16(vt8) || !aligned16(o))
+    return fail(FA_ERR_INVALID_ARG, "q8, k8, vt8 and o must be 16-byte aligned");
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || Sq < 0 || Sk < 0)
+    return fail(FA_ERR_INVALID_ARG, "bad sizes B=%d Hq=%d Hkv=%d Sq=%d Sk=%d", B, Hq, Hkv, Sq, Sk);
+  if (Hq % Hkv != 0) return fail(FA_ERR_INVALID_ARG, "Hq (%d) %% Hkv (%d) != 0", Hq, Hkv);
+  if (d != 128) return fail(FA_ERR_UNSUPPORTED, "FP8 forward head dim %d (supported: 128)", d);
+  if (!std::isfinite(scale) || !(scale > 0.f))
+    return fail(FA_ERR_INVALID_ARG, "scale must be finite and > 0");
+  if ((long long)B * Sq > INT32_MAX / 2 || (long long)B * Sk > INT32_MAX / 2)
+    return fail(FA_ERR_INVALID_ARG, "sizes too large");
+  if (B == 0 || Sq == 0) return FA_OK;
+  DevInfo* di = nullptr;
+  int st = device_info(&di);
+  if (st != FA_OK) return st;
+  const Knobs kn = knobs_snapshot();
+
+  FwdParams p;
+  memset(&p, 0, sizeof(p));
+  const long long Tq = (long long)B * Sq;
+  const long long S_pad = ((long long)Sk + 15) / 16 * 16;
+  {
+    const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)Hq, (cuuint64_t)Tq};
+    const cuuint64_t strides[2] = {(cuuint64_t)d, (cuuint64_t)Hq * d};
+    const cuuint32_t box[3] = {128, 1, 128};
+    if ((st = encode_u8(&p.tm_q, q8, dims, strides, box)) != FA_OK) return st;
+  }
+  if (Sk > 0) {
+    const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)Hkv, (cuuint64_t)B * Sk};
+    const cuuint64_t strides[2] = {(cuuint64_t)d, (cuuint64_t)Hkv * d};
+    const cuuint32_t box[3] = {128, 1, 128};
+    if ((st = encode_u8(&p.tm_k, k8, dims, strides, box)) != FA_OK) return st;
+    const cuuint64_t vdims[3] = {(cuuint64_t)S_pad, (cuuint64_t)d, (cuuint64_t)B * Hkv};
+    const cuuint64_t vstrides[2] = {(cuuint64_t)S_pad, (cuuint64_t)S_pad * d};
+    const cuuint32_t vbox[3] = {128, 128, 1};
+    if ((st = encode_u8(&p.tm_v, vt8, vdims, vstrides, vbox)) != FA_OK) return st;
+  } else {
+    // no keys: every row is fully masked and the maps are never used
+    p.tm_k = p.tm_q;
+    p.tm_v = p.tm_q;
+  }
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.lse = lse;
+  p.nseq = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.Sq = Sq;
+  p.Sk = Sk;
+  p.total_q = (int)Tq;
+  p.causal = causal ? 1 : 0;
+  p.lse_hstride = Sq;
+  p.lse_seqstride = (long long)Hq * Sq;
+  p.scale_log2 = (float)((double)scale * 1.4426950408889634);
+  p.err = di->err_word;
+  p.timeout_ns = (unsigned long long)kn.timeout_ns;
+  p.q_scale = q_scale;
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
+  p.nqb = (Sq + 127) / 128;
+  p.nkb = (Sk + 127) / 128;
+  const long long units = (long long)B * ((Sq + 255) / 256) * Hq;
+  int grid = kn.grid_override > 0 ? kn.grid_override : di->sms;
+  if (units < grid) grid = (int)units;
+  if (grid < 1) grid = 1;
+  p.hblock = Hq;
+  cudaEvent_t ev0, ev1;
+  take_events(0, &ev0, &ev1);
+  if (ev0) cudaEventRecord(ev0, static_cast<cudaStream_t>(stream));
+  cudaError_t e = launch_fwd_fp8(p, grid, static_cast<cudaStream_t>(stream));
+  if (ev1) cudaEventRecord(ev1, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(FA_ERR_CUDA, "FP8 forward launch: %s", cudaGetErrorString(e));
+  return FA_OK;
 }
 
 extern "C" size_t fa_bwd_workspace_bytes(int B, int Hq, int Sq, int d, int total_q) {
@@ -592,6 +708,19 @@ extern "C" int fa_test_mma_pair(const void* A, const void* B, float* C, int* fla
   cudaError_t e = launch_mma_pair_probe(static_cast<const __nv_bfloat16*>(A),
                                         static_cast<const __nv_bfloat16*>(B), C, flags, mode, N,
                                         static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : fail(FA_ERR_CUDA, "%s", cudaGetErrorString(e));
+}
+
+extern "C" int fa_test_mma_fp8(const void* A, const void* B, float* C, int mode, int N,
+                               void* stream) {
+  if (!A || !B || !C || (mode != 0 && mode != 1) || (N != 64 && N != 128))
+    return fail(FA_ERR_INVALID_ARG, "fa_test_mma_fp8 arguments");
+  DevInfo* di = nullptr;
+  int st = device_info(&di);
+  if (st != FA_OK) return st;
+  cudaError_t e = launch_mma_fp8_probe(static_cast<const uint8_t*>(A),
+                                       static_cast<const uint8_t*>(B), C, mode, N,
+                                       static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : fail(FA_ERR_CUDA, "%s", cudaGetErrorString(e));
 }
 

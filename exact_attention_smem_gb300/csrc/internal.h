@@ -75,6 +75,11 @@ struct FwdParams {
   int hblock;                    // heads per scheduler group
   int* err;
   unsigned long long timeout_ns;
+  // FP8 forward only (else unused): e4m3 inputs with per-block scales
+  const float* q_scale;          // [B, Hq, nqb]: per 128 query rows
+  const float* k_scale;          // [B, Hkv, nkb]: per 128 keys
+  const float* v_scale;          // [B, Hkv]
+  int nqb, nkb;
 };
 
 struct BwdParams {
@@ -113,6 +118,9 @@ __host__ __device__ __forceinline__ long long pad_hstride(long long T, int nseq)
 // Launchers (fwd.cu / bwd.cu). Return a cudaError_t.
 cudaError_t launch_fwd(const FwdParams& p, int d, int grid, cudaStream_t stream, int poly8);
 cudaError_t launch_fwd_big(const FwdParams& p, int d, int grid, cudaStream_t stream, int poly8);
+cudaError_t launch_fwd_fp8(const FwdParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_quantize_fp8(const __nv_bfloat16* x, int B, int S, int H, int d, int layout,
+                                uint8_t* codes, float* scales, cudaStream_t st);
 int fwd_units_total(const FwdParams& p);
 struct BwdAux {                  // inputs of the preprocess / convert passes
   const __nv_bfloat16* o;

@@ -143,6 +143,97 @@ cudaError_t launch_mma_probe(const __nv_bfloat16* A, const __nv_bfloat16* B, flo
   return cudaGetLastError();
 }
 
+// 8-bit operands, K-major, 128-byte swizzle: rows of 128 one-byte elements.
+__device__ __forceinline__ uint32_t sw128_offset8(int r, int c) {
+  return r * 128 + ((((uint32_t)c >> 4) ^ (uint32_t)(r & 7)) << 4) + (c & 15);
+}
+
+// e4m3 (kind::f8f6f4) probe: C[128][N] = A[128][128] * B[N][128]^T, fp32.
+// mode 0: A and B in shared memory; mode 1: A from TMEM (four codes per
+// column), B in shared memory. A and B are row-major e4m3 codes.
+__global__ void __launch_bounds__(128, 1)
+    mma_fp8_probe_kernel(const uint8_t* A, const uint8_t* B, float* C, int mode, int N,
+                         int* err) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (base - raw);
+  const uint32_t a_s = base, b_s = base + 16384;
+  const uint32_t bar = base + 32768;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + 32768 + 64);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 32768 + 72);
+  const int warp = threadIdx.x >> 5;
+  const int tid = threadIdx.x;
+  for (int i = tid; i < 128 * 128; i += 128) smem[sw128_offset8(i >> 7, i & 127)] = A[i];
+  for (int i = tid; i < N * 128; i += 128) smem[16384 + sw128_offset8(i >> 7, i & 127)] = B[i];
+  if (tid == 0) {
+    mbar_init(bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+  if (mode == 1) {
+    uint32_t pk[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const uint8_t* a = A + tid * 128 + 4 * j;
+      pk[j] = (uint32_t)a[0] | ((uint32_t)a[1] << 8) | ((uint32_t)a[2] << 16) |
+              ((uint32_t)a[3] << 24);
+    }
+    tmem_st32(tmem + lane_off, pk);
+    tmem_st_wait();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t d_tm = tmem + 256;
+  if (tid == 0) {
+    for (int kk = 0; kk < 4; ++kk) {
+      const uint64_t bd = sdesc_sw128(b_s + kk * 32, 16384, 1024);
+      if (mode == 0)
+        mma_ss_f8(d_tm, sdesc_sw128(a_s + kk * 32, 16384, 1024), bd, idesc_e4m3(128, N), kk > 0);
+      else
+        mma_ts_f8(d_tm, tmem + kk * 8, bd, idesc_e4m3(128, N), kk > 0);
+    }
+    tc_commit(bar);
+  }
+  const WaitCtl wc{err, abort_flag, 1000000000ull};
+  const bool ok = mbar_wait(bar, 0, wc, SITE_TEST);
+  tc_fence_after();
+  if (ok) {
+    for (int c = 0; c < N; c += 32) {
+      uint32_t v[32];
+      tmem_ld32(tmem + lane_off + 256 + c, v);
+      for (int i = 0; i < 32; ++i) C[tid * N + c + i] = __uint_as_float(v[i]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+cudaError_t launch_mma_fp8_probe(const uint8_t* A, const uint8_t* B, float* C, int mode, int N,
+                                 cudaStream_t st) {
+  const int smem = 32768 + 128 + 1024 + 32768;  // slack keeps any mis-decoded offset in bounds
+  cudaError_t e = cudaFuncSetAttribute(mma_fp8_probe_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  mma_fp8_probe_kernel<<<1, 128, smem, st>>>(A, B, C, mode, N, device_error_word());
+  return cudaGetLastError();
+}
+
 // CTA-pair (cta_group::2) MMA probe: a cluster of two CTAs computes
 //   mode 0: C[256][N] = A[256][128] * B[N][128]^T   (A, B K-major in shared memory)
 //   mode 1: C[256][N] = A[256][128] * B[128][N]     (A from TMEM, B MN-major)

@@ -74,6 +74,39 @@ FA_API int fa_fwd(const void* q, const void* k, const void* v, void* o, float* l
            void* stream);
 
 /*
+ * FP8 (e4m3) quantization of a bf16 attention input x [B, S, H, d] (device,
+ * 16-byte aligned; d = 64 or 128) for fa_fwd_fp8. The FlashAttention-4 pages
+ * name low precision only through the FlashAttention-3 title (their reference
+ * lists); the scaling below is this library's reading:
+ *   layout 0 (Q, K): codes [B, S, H, d] (1 byte each); scales float
+ *     [B, H, ceil(S/128)], one per 128-row block over its rows and d columns.
+ *   layout 1 (V): codes transposed, [B, H, d, S_pad] with S_pad = S rounded
+ *     up to 16 (the pad holds zero codes); scales float [B, H].
+ * scale = amax / 448 (1 if amax = 0); code = e4m3(x / scale), float32
+ * division, round to nearest even, saturating at +-448. Runs on `stream`
+ * (layout 1: a memset and three kernels, with `scales` as their scratch).
+ * Errors: FA_ERR_INVALID_ARG (NULL or misaligned pointer, bad sizes or
+ * layout), FA_ERR_UNSUPPORTED (d), FA_ERR_CUDA.
+ */
+FA_API int fa_quantize_fp8(const void* x, int B, int S, int H, int d, int layout, void* codes,
+                           float* scales, void* stream);
+
+/*
+ * FP8 forward: O (bf16 [B, Sq, Hq, d]) and LSE (fp32 [B, Hq, Sq]) of exact
+ * attention over the dequantized inputs Q^ = code * q_scale etc., from the
+ * outputs of fa_quantize_fp8 (q8, k8 layout 0 with [B, Sq, Hq, d] and
+ * [B, Sk, Hkv, d]; vt8 layout 1, [B, Hkv, d, Sk_pad]). Same masking, GQA and
+ * LSE conventions as fa_fwd (dense layouts, d = 128). Both products run on the
+ * tensor cores in e4m3 with fp32 accumulation; the softmax weights are rounded
+ * to e4m3 for the P V product, so O carries that rounding (relative error of
+ * each weight <= 2^-4) while the LSE does not. Errors as fa_fwd.
+ */
+FA_API int fa_fwd_fp8(const void* q8, const void* k8, const void* vt8, const float* q_scale,
+                      const float* k_scale, const float* v_scale, void* o, float* lse, int B,
+                      int Hq, int Hkv, int Sq, int Sk, int d, int causal, float scale,
+                      void* stream);
+
+/*
  * Bytes of device workspace fa_bwd / fa_bwd_varlen need: an fp32 dQ
  * accumulator [T][Hq][d] (used by the one-pass form only), the fp32 row terms
  * -D_i = -sum_c dO_ic O_ic and -LSE*log2(e) ([Hq][P] each, P = T padded per
@@ -259,6 +292,14 @@ FA_API float fa_exp2_poly_host(float x);
  * A, B bf16 row-major device buffers.
  */
 FA_API int fa_test_mma(const void* A, const void* B, float* C, int mode, int N, void* stream);
+
+/*
+ * One-tile e4m3 tcgen05 MMA probe (kind::f8f6f4, one CTA): fp32
+ * C[128][N] = A[128][128] * B[N][128]^T, N in {64,128}; A and B are row-major
+ * e4m3 codes (device). mode 0: A and B from shared memory; mode 1: A from
+ * tensor memory.
+ */
+FA_API int fa_test_mma_fp8(const void* A, const void* B, float* C, int mode, int N, void* stream);
 
 /*
  * CTA-pair (cta_group::2) tcgen05 MMA probe: a cluster of two CTAs computes

@@ -1,0 +1,131 @@
+"""FP8 (e4m3) path: quantization and forward against the oracle.
+
+* fa_quantize_fp8: codes and scales bit-exact against the oracle's quantizer
+  (both sides take every decision in float32: amax, amax / 448, x / scale,
+  round to nearest even with saturation).
+* fa_fwd_fp8 against exact fp64 attention over the dequantized inputs:
+  - LSE max-abs <= 1e-3: the scores are exact sums of code products
+    accumulated in fp32, as in the bf16 forward;
+  - O rel-L2 <= 5e-2 (per head): the kernel rounds each softmax weight to
+    e4m3 (3 mantissa bits, relative rounding error <= 2^-4, so an RMS of at
+    most 2^-4 / sqrt(3) = 3.6% per weight). The output is a weighted sum of
+    V rows, so independent relative errors in the weights give an output
+    error whose RMS is at most that of the weights, 3.6% of the RMS output;
+    5e-2 leaves headroom for bf16 output rounding. A structural error (a
+    wrong block scale, a dropped key block, a transposed operand) is off by
+    tens of percent or more;
+  - Q = 0 makes every weight exactly 1 (2^8 in the kernel, exact in e4m3), so
+    O is the plain mean of the visible V rows: checked to 4e-3 max-abs (bf16
+    output rounding).
+"""
+import numpy as np
+import pytest
+import torch
+
+import exact_attention_smem_gb300 as fa
+from oracle import fp8_e4m3 as f8
+from attn_inputs import random_inputs
+from gpu_helpers import LSE_TOL, max_abs
+
+pytestmark = pytest.mark.gpu
+
+O_REL_L2_FP8 = 5e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _dev():
+    fa.load()
+    torch.cuda.set_device(0)
+    fa.fa_get_device_error(clear=True)
+    yield
+    assert fa.fa_get_device_error(clear=True) == 0
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("S", [1, 127, 300])
+def test_quantize_rows_bit_exact(S, d):
+    g = torch.Generator().manual_seed(10 + S + d)
+    x = (torch.randn(2, S, 3, d, generator=g) * torch.rand(1, S, 3, 1, generator=g) * 4)
+    x = x.to(torch.bfloat16)
+    if S > 128:
+        x[1, 128:256, 2] = 0                          # an all-zero block
+    codes, scales = fa.quantize_fp8(x.cuda(), 0)
+    torch.cuda.synchronize()
+    rc, rs = f8.quantize_row_blocks(x.float().numpy())
+    assert np.array_equal(codes.cpu().numpy(), rc)
+    assert np.array_equal(scales.cpu().numpy(), rs)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("S", [1, 37, 300, 1000])
+def test_quantize_v_bit_exact(S, d):
+    g = torch.Generator().manual_seed(20 + S + d)
+    x = (torch.randn(2, S, 3, d, generator=g) * 3).to(torch.bfloat16)
+    codes, scales = fa.quantize_fp8(x.cuda(), 1)
+    torch.cuda.synchronize()
+    rc, rs = f8.quantize_v_transposed(x.float().numpy())
+    assert codes.shape == rc.shape
+    assert np.array_equal(codes.cpu().numpy(), rc)
+    assert np.array_equal(scales.cpu().numpy(), rs)
+
+
+def _fp8_case(B, Hq, Hkv, Sq, Sk, causal, seed, zero_q=False):
+    x = random_inputs(B=B, Hq=Hq, Hkv=Hkv, Sq=Sq, Sk=Sk, d=128, seed=seed, device="cuda")
+    q = torch.zeros_like(x.q) if zero_q else x.q
+    q8, qs = fa.quantize_fp8(q, 0)
+    k8, ks = fa.quantize_fp8(x.k, 0)
+    v8, vs = fa.quantize_fp8(x.v, 1)
+    scale = 128 ** -0.5
+    o, lse = fa.forward_fp8(q8, qs, k8, ks, v8, vs, causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    ro, rl = f8.forward_fp8(q8.cpu().numpy(), qs.cpu().numpy(), k8.cpu().numpy(),
+                            ks.cpu().numpy(), v8.cpu().numpy(), vs.cpu().numpy(), scale, causal)
+    return o.float().cpu().numpy(), lse.cpu(), ro, rl
+
+
+def _rel_l2_per_head(o, ro):
+    worst = 0.0
+    for h in range(o.shape[2]):
+        a, b = o[:, :, h], ro[:, :, h]
+        fin = np.isfinite(b)
+        num = np.linalg.norm((a - b)[fin])
+        den = np.linalg.norm(b[fin])
+        if den > 0:
+            worst = max(worst, num / den)
+    return worst
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("B,Hq,Hkv,Sq,Sk", [(2, 4, 2, 300, 300), (1, 2, 2, 200, 700),
+                                            (1, 2, 1, 700, 200), (1, 2, 2, 1024, 1024)])
+def test_fp8_forward_parity(B, Hq, Hkv, Sq, Sk, causal):
+    o, lse, ro, rl = _fp8_case(B, Hq, Hkv, Sq, Sk, causal, seed=40 + Sq + Sk + causal)
+    assert max_abs(lse, rl) <= LSE_TOL
+    assert _rel_l2_per_head(o, ro) <= O_REL_L2_FP8
+    # rows with no visible key: O = 0, LSE = +inf
+    empty = ~np.isfinite(rl)
+    if empty.any():
+        ln = lse.numpy()
+        assert np.all(np.isinf(ln[empty])) and np.all(ln[empty] > 0)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp8_uniform_weights_exact(causal):
+    o, lse, ro, rl = _fp8_case(1, 2, 2, 384, 500, causal, seed=77, zero_q=True)
+    assert max_abs(lse, rl) <= LSE_TOL
+    fin = np.isfinite(ro)
+    assert np.abs(o[fin] - ro[fin]).max() <= 4e-3
+
+
+def test_fp8_rejects_bad_arguments():
+    x = torch.zeros(16, device="cuda", dtype=torch.uint8)
+    f = torch.zeros(4, device="cuda")
+    with pytest.raises(fa.FAError) as e:
+        fa.fa_fwd_fp8(x, x, x, f, f, f, x, f, 1, 2, 2, 16, 16, 64, 0, 0.1)
+    assert e.value.status == 2
+    with pytest.raises(fa.FAError) as e:
+        fa.fa_fwd_fp8(x, x, x, f, f, f, x, f, 1, 3, 2, 16, 16, 128, 0, 0.1)
+    assert e.value.status == 1
+    with pytest.raises(fa.FAError) as e:
+        fa.fa_quantize_fp8(x, 1, 16, 1, 128, 2, x, f)
+    assert e.value.status == 1

@@ -61,6 +61,26 @@ def test_mma_probe(mode, N):
     assert np.abs(got - want).max() <= 1e-3 * max(1.0, np.abs(want).max())
 
 
+@pytest.mark.parametrize("N", [64, 128])
+@pytest.mark.parametrize("mode", [0, 1])
+def test_mma_fp8_probe(mode, N):
+    """kind::f8f6f4 with e4m3 operands: the products of e4m3 values are exact
+    in fp32, so a 128-term fp32 sum is within 128 * 2^-24 (< 1e-5) of the
+    exact value, relative to the sum of the terms' magnitudes."""
+    rng = np.random.default_rng(300 + mode * 7 + N)
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], dtype=np.uint8)
+    A = rng.choice(codes, (128, 128))
+    B = rng.choice(codes, (N, 128))
+    C = torch.full((128, N), float("nan"), device="cuda")
+    fa.fa_test_mma_fp8(torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda(), C, mode, N)
+    torch.cuda.synchronize()
+    a, b = oracle.fp8_e4m3.e4m3_decode(A), oracle.fp8_e4m3.e4m3_decode(B)
+    want = a @ b.T
+    got = C.cpu().double().numpy()
+    scale = (np.abs(a) @ np.abs(b).T).max()
+    assert np.abs(got - want).max() <= 1e-5 * scale
+
+
 @pytest.mark.parametrize("N", [128])
 @pytest.mark.parametrize("mode", [0, 1])
 def test_mma_pair_probe(mode, N):
