@@ -7,6 +7,7 @@ no flush is needed between steps. FLOPs: forward 4*B*Hq*Sq*Sk*d, halved for
 causal; backward 2.5x forward.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+  python bench.py --fp8 [--workload W]     # FP8 (e4m3) forward only, one GPU
 
 Prints one JSON line (rank 0). N > 1 (torchrun) runs one independent replica
 per GPU (the path has no exchange step) and reports the whole-job aggregate.
@@ -262,6 +263,77 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def run_fp8(args):
+    """The FP8 (e4m3) forward on one GPU: Q, K, V quantized once before the
+    timed region (codes resident in HBM), then K timed forward launches."""
+    import torch
+
+    import exact_attention_smem_gb300 as fa
+    from attn_inputs import WORKLOADS, make_inputs
+
+    ws, rank, local = _dist()
+    if ws > 1:
+        raise SystemExit("--fp8 runs on one GPU")
+    torch.cuda.set_device(local)
+    fa.load()
+    w = WORKLOADS[WORKLOAD]
+    x = make_inputs(w, "cuda")
+    B, Hq, Hkv, S, d = w.B, w.Hq, w.Hkv, w.Sq, w.d
+    stream = torch.cuda.current_stream()
+    fa.quantize_fp8(x.q, 0), fa.quantize_fp8(x.v, 1)       # first launches (module loading)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    ev[0].record(stream)
+    q8, qs = fa.quantize_fp8(x.q, 0)
+    k8, ks = fa.quantize_fp8(x.k, 0)
+    v8, vs = fa.quantize_fp8(x.v, 1)
+    ev[1].record(stream)
+    torch.cuda.synchronize()
+    quant_ms = ev[0].elapsed_time(ev[1])
+    o = torch.empty_like(x.q)
+    lse = torch.empty(B, Hq, S, dtype=torch.float32, device="cuda")
+
+    def step():
+        fa.fa_fwd_fp8(q8, k8, v8, qs, ks, vs, o, lse, B, Hq, Hkv, S, S, d, True, w.scale, stream)
+
+    clk = Clocks(local).__enter__()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_error() == 0
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    wall0 = time.time()
+    t0.record(stream)
+    for _ in range(args.steps):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    wall1 = time.time()
+    clk.__exit__(None, None, None)
+    assert fa.fa_get_device_error() == 0
+    ms = t0.elapsed_time(t1)
+    f_fwd, _ = flops(w)
+    value = job_tflops(f_fwd, args.steps, 1, ms)
+    _, peak_s, kind = _peaks()
+    peak8 = 2.0 * peak_s                     # the nominal dense fp8 : bf16 ratio
+    print(json.dumps({
+        "metric": "attention fwd FP8 (e4m3) TFLOPs/s on 1 GB300", "value": round(value, 2),
+        "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms / args.steps, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "e4m3 (fp32 accumulate)",
+        "data": "synthetic (seeded N(0,1) bf16, quantized before the timed region)",
+        "config": {"workload": WORKLOAD, "B": B, "Hq": Hq, "Hkv": Hkv, "S": S, "d": d,
+                   "causal": True, "step": "fwd", "l2": l2_note(w)},
+        "roofline": {"bound": "tensor", "kernel": "fwd_fp8_kernel (tcgen05 kind::f8f6f4)",
+                     "achieved": round(value, 1), "peak": round(peak8, 1), "unit": "TFLOP/s",
+                     "frac": round(value / peak8, 4),
+                     "peak_kind": f"{kind} sustained bf16 x 2 (nominal fp8:bf16 ratio)",
+                     "traffic": profiled_traffic("fwd_fp8.cu", f"fwd_fp8_kernel_{WORKLOAD}.md")},
+        "quantize_qkv_ms": round(quant_ms, 3),
+        "gpu_launches": args.steps,
+        "clocks": clk.summary(wall0, wall1),
+    }))
+
+
 def run_e2e(fa, w, x, args, stream):
     """The step through the C ABI with inputs and results in pinned host memory.
 
@@ -411,6 +483,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline leg")
+    ap.add_argument("--fp8", action="store_true", help="time the FP8 (e4m3) forward instead")
     ap.add_argument("--workload", default=WORKLOAD,
                     choices=["long_s32768_causal", "mha_s2048_causal", "gqa_s8192_causal"],
                     help="dense causal workload to run (the bench line is long_s32768_causal; "
@@ -419,6 +492,8 @@ def main():
     globals()["WORKLOAD"] = args.workload
     if args.impl == "reference":
         run_reference(args)
+    elif args.fp8:
+        run_fp8(args)
     else:
         run_ours(args)
 

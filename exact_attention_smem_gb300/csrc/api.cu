@@ -383,7 +383,7 @@ extern "C" int fa_fwd_fp8(const void* q8, const void* k8, const void* vt8, const
   cudaEvent_t ev0, ev1;
   take_events(0, &ev0, &ev1);
   if (ev0) cudaEventRecord(ev0, static_cast<cudaStream_t>(stream));
-  cudaError_t e = launch_fwd_fp8(p, grid, static_cast<cudaStream_t>(stream));
+  cudaError_t e = launch_fwd_fp8(p, grid, static_cast<cudaStream_t>(stream), kn.fp8_poly8);
   if (ev1) cudaEventRecord(ev1, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(FA_ERR_CUDA, "FP8 forward launch: %s", cudaGetErrorString(e));
   return FA_OK;
@@ -622,10 +622,10 @@ extern "C" int fa_debug_set(const char* key, double value) {
   if (!strcmp(key, "tau")) {
     if (!(value >= 0.0 && value <= 16.0)) return fail(FA_ERR_INVALID_ARG, "tau in [0, 16]");
     g_knobs.tau_log2 = (float)value;
-  } else if (!strcmp(key, "poly8") || !strcmp(key, "bwd_poly8")) {
+  } else if (!strcmp(key, "poly8") || !strcmp(key, "bwd_poly8") || !strcmp(key, "fp8_poly8")) {
     const int v = (int)value;
     if (v != 0 && v != 2 && v != 4) return fail(FA_ERR_INVALID_ARG, "poly8 in {0, 2, 4}");
-    (key[0] == 'p' ? g_knobs.poly8 : g_knobs.bwd_poly8) = v;
+    (key[0] == 'p' ? g_knobs.poly8 : key[0] == 'b' ? g_knobs.bwd_poly8 : g_knobs.fp8_poly8) = v;
   } else if (!strcmp(key, "bwd_mode")) {
     if (value != 0.0 && value != 1.0 && value != 2.0)
       return fail(FA_ERR_INVALID_ARG, "bwd_mode in {0, 1, 2}");

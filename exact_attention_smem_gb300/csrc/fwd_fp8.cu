@@ -22,6 +22,7 @@
 // Rescaling is unconditional (threshold 0): a larger threshold would let the
 // weights exceed 448 before the reference moves.
 // Head dim 128, dense [B, S, H, d] layouts (no packed sequences).
+#include "exp2_poly.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 #include "sched.cuh"
@@ -97,6 +98,7 @@ __device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
   return lo | (hi << 16);
 }
 
+template <int POLY8>
 __global__ void __launch_bounds__(NUM_THREADS, 1) fwd_fp8_kernel(const __grid_constant__ FwdParams p) {
   using C = Cfg;
   extern __shared__ uint8_t smem_raw[];
@@ -373,7 +375,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) fwd_fp8_kernel(const __grid_co
           float x0, x1, x2, x3;
           f2unpack(ffma2(f2pack(u2f(sr[4 * c]), u2f(sr[4 * c + 1])), c2, negm2), x0, x1);
           f2unpack(ffma2(f2pack(u2f(sr[4 * c + 2]), u2f(sr[4 * c + 3])), c2, negm2), x2, x3);
-          const float p0 = ex2_mufu(x0), p1 = ex2_mufu(x1), p2 = ex2_mufu(x2), p3 = ex2_mufu(x3);
+          // POLY8 of every 8 exponentials on the FMA pipe, the rest on MUFU
+          const float p0 = ((4 * c) & 7) < POLY8 ? exp2_poly(x0) : ex2_mufu(x0);
+          const float p1 = ((4 * c + 1) & 7) < POLY8 ? exp2_poly(x1) : ex2_mufu(x1);
+          const float p2 = ((4 * c + 2) & 7) < POLY8 ? exp2_poly(x2) : ex2_mufu(x2);
+          const float p3 = ((4 * c + 3) & 7) < POLY8 ? exp2_poly(x3) : ex2_mufu(x3);
           la2[c & 1] = fadd2(la2[c & 1], fadd2(f2pack(p0, p1), f2pack(p2, p3)));
           pk[c] = e4m3x4(p0, p1, p2, p3);
         }
@@ -427,13 +433,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) fwd_fp8_kernel(const __grid_co
 
 }  // namespace fwd8
 
-cudaError_t launch_fwd_fp8(const FwdParams& p, int grid, cudaStream_t stream) {
-  auto kern = fwd8::fwd_fp8_kernel;
+template <int POLY8>
+static cudaError_t launch_fp8_one(const FwdParams& p, int grid, cudaStream_t stream) {
+  auto kern = fwd8::fwd_fp8_kernel<POLY8>;
   const int smem = fwd8::Cfg::SMEM_BYTES;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   kern<<<grid, fwd8::NUM_THREADS, smem, stream>>>(p);
   return cudaGetLastError();
+}
+
+cudaError_t launch_fwd_fp8(const FwdParams& p, int grid, cudaStream_t stream, int poly8) {
+  switch (poly8) {
+    case 0: return launch_fp8_one<0>(p, grid, stream);
+    case 2: return launch_fp8_one<2>(p, grid, stream);
+    case 4: return launch_fp8_one<4>(p, grid, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace fa

@@ -32,6 +32,7 @@ struct Knobs {
   float tau_log2 = 0.0f;         // rescale threshold, base-2 units
   int poly8 = 0;                 // eighths of the exponentials done by the polynomial (fwd)
   int bwd_poly8 = 0;             // same for the backward
+  int fp8_poly8 = 0;             // same for the FP8 forward
   int bwd_mode = 1;              // 1: two-pass backward (dK/dV pass + dQ pass); 2: the same
                                  // with the dK/dV pass on CTA pairs (d = 128; d = 64 runs
                                  // mode 1); 0: one pass with dQ by fp32 atomics + convert
@@ -118,7 +119,7 @@ __host__ __device__ __forceinline__ long long pad_hstride(long long T, int nseq)
 // Launchers (fwd.cu / bwd.cu). Return a cudaError_t.
 cudaError_t launch_fwd(const FwdParams& p, int d, int grid, cudaStream_t stream, int poly8);
 cudaError_t launch_fwd_big(const FwdParams& p, int d, int grid, cudaStream_t stream, int poly8);
-cudaError_t launch_fwd_fp8(const FwdParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_fwd_fp8(const FwdParams& p, int grid, cudaStream_t stream, int poly8);
 cudaError_t launch_quantize_fp8(const __nv_bfloat16* x, int B, int S, int H, int d, int layout,
                                 uint8_t* codes, float* scales, cudaStream_t st);
 int fwd_units_total(const FwdParams& p);

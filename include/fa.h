@@ -222,6 +222,7 @@ FA_API int fa_get_device_error(int* code, int clear);
  *   "poly8"      forward: eighths of the exponentials computed by the FMA-pipe
  *                polynomial instead of MUFU ex2 (0, 2 or 4)
  *   "bwd_poly8"  the same for the backward
+ *   "fp8_poly8"  the same for the FP8 forward
  *   "timeout_ms" bounded-wait deadline in milliseconds (default 2000)
  *   "grid"       persistent grid size override (0 = one CTA per SM)
  *   "bwd_mode"   backward form: 1 two passes (default), 2 the same with the

@@ -129,3 +129,16 @@ def test_fp8_rejects_bad_arguments():
     with pytest.raises(fa.FAError) as e:
         fa.fa_quantize_fp8(x, 1, 16, 1, 128, 2, x, f)
     assert e.value.status == 1
+
+
+@pytest.mark.parametrize("poly8", [2, 4])
+def test_fp8_forward_polynomial_exp2(poly8):
+    """Some exponentials from the FMA-pipe polynomial (relative error ~1e-7,
+    far below the e4m3 rounding of the weights): same bounds."""
+    fa.fa_debug_set("fp8_poly8", poly8)
+    try:
+        o, lse, ro, rl = _fp8_case(2, 4, 2, 300, 700, True, seed=90 + poly8)
+    finally:
+        fa.fa_debug_set("fp8_poly8", 0)
+    assert max_abs(lse, rl) <= LSE_TOL
+    assert _rel_l2_per_head(o, ro) <= O_REL_L2_FP8
