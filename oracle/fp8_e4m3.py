@@ -34,7 +34,7 @@ from __future__ import annotations
 
 import numpy as np
 
-from .attention_fp64 import forward as _forward_fp64
+from .attention_fp64 import attend_head as _attend_head
 
 E4M3_MAX = 448.0
 BLOCK = 128
@@ -136,8 +136,23 @@ def dequantize_v_transposed(codes, scales, S: int):
 def forward_fp8(q_codes, q_scales, k_codes, k_scales, vt_codes, v_scales, scale: float,
                 causal: bool, heads=None, seqs=None):
     """The FP8 forward's definition: exact fp64 attention over the dequantized
-    inputs. Returns (o, lse) like ``attention_fp64.forward`` (dense layout)."""
-    q = dequantize_row_blocks(q_codes, q_scales)
-    k = dequantize_row_blocks(k_codes, k_scales)
-    v = dequantize_v_transposed(vt_codes, v_scales, k.shape[1])
-    return _forward_fp64(q, k, v, scale, causal, heads=heads, seqs=seqs)
+    inputs. Returns (o, lse) like ``attention_fp64.forward`` (dense layout;
+    entries of heads or sequences outside the subset are NaN). Dequantizes one
+    (sequence, head) at a time, so a subset of a large problem stays small."""
+    qc, kc, vc = np.asarray(q_codes), np.asarray(k_codes), np.asarray(vt_codes)
+    qs, ks, vs = (np.asarray(x, dtype=np.float64) for x in (q_scales, k_scales, v_scales))
+    B, Sq, Hq, d = qc.shape
+    Sk, Hkv = kc.shape[1], kc.shape[2]
+    group = Hq // Hkv
+    o = np.full((B, Sq, Hq, d), np.nan)
+    lse = np.full((B, Hq, Sq), np.nan)
+    for b in range(B):
+        if seqs is not None and b not in seqs:
+            continue
+        for h in (range(Hq) if heads is None else heads):
+            g = h // group
+            qh = e4m3_decode(qc[b, :, h]) * np.repeat(qs[b, h], BLOCK)[:Sq, None]
+            kh = e4m3_decode(kc[b, :, g]) * np.repeat(ks[b, g], BLOCK)[:Sk, None]
+            vh = e4m3_decode(vc[b, g, :, :Sk]).T * vs[b, g]
+            o[b, :, h], lse[b, h] = _attend_head(qh, kh, vh, scale, causal)
+    return o, lse

@@ -142,3 +142,34 @@ def test_fp8_forward_polynomial_exp2(poly8):
         fa.fa_debug_set("fp8_poly8", 0)
     assert max_abs(lse, rl) <= LSE_TOL
     assert _rel_l2_per_head(o, ro) <= O_REL_L2_FP8
+
+
+@pytest.mark.parametrize("name", ["long_s32768_causal", "gqa_s8192_causal"])
+def test_fp8_full_size_parity(name):
+    """The workloads `bench.py --fp8` times, at full size in its launch
+    configuration; the oracle checks query heads {0, last} (long) or KV group 0
+    of the first and last batch entries (GQA)."""
+    from attn_inputs import WORKLOADS, make_inputs
+    w = WORKLOADS[name]
+    x = make_inputs(w, "cuda")
+    q8, qs = fa.quantize_fp8(x.q, 0)
+    k8, ks = fa.quantize_fp8(x.k, 0)
+    v8, vs = fa.quantize_fp8(x.v, 1)
+    del x
+    o, lse = fa.forward_fp8(q8, qs, k8, ks, v8, vs, causal=True, scale=w.scale)
+    torch.cuda.synchronize()
+    if name == "gqa_s8192_causal":
+        heads, seqs = list(range(w.Hq // w.Hkv)), [0, w.B - 1]
+    else:
+        heads, seqs = [0, w.Hq - 1], None
+    ro, rl = f8.forward_fp8(q8.cpu().numpy(), qs.cpu().numpy(), k8.cpu().numpy(),
+                            ks.cpu().numpy(), v8.cpu().numpy(), vs.cpu().numpy(), w.scale, True,
+                            heads=heads, seqs=seqs)
+    bsel = list(range(w.B)) if seqs is None else seqs
+    lse_c = lse.cpu()
+    e_lse = max_abs(lse_c[bsel][:, heads], rl[bsel][:, heads])
+    o_c = o[bsel][:, :, heads].float().cpu().numpy()
+    e_o = _rel_l2_per_head(o_c, ro[bsel][:, :, heads])
+    print(f"\nfp8 {name}: LSE max-abs {e_lse:.2e}, O rel-L2 (worst head) {e_o:.2e}")
+    assert e_lse <= LSE_TOL
+    assert e_o <= O_REL_L2_FP8
