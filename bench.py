@@ -479,7 +479,8 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default 10; 50 with --fp8, whose steps are short)")
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline leg")
@@ -489,6 +490,8 @@ def main():
                     help="dense causal workload to run (the bench line is long_s32768_causal; "
                          "the others serve small profiling captures)")
     args = ap.parse_args()
+    if args.steps is None:
+        args.steps = 50 if args.fp8 else 10
     globals()["WORKLOAD"] = args.workload
     if args.impl == "reference":
         run_reference(args)

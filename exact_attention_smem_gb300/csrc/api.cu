@@ -370,6 +370,7 @@ extern "C" int fa_fwd_fp8(const void* q8, const void* k8, const void* vt8, const
   p.scale_log2 = (float)((double)scale * 1.4426950408889634);
   p.err = di->err_word;
   p.timeout_ns = (unsigned long long)kn.timeout_ns;
+  p.tau = kn.fp8_tau;
   p.q_scale = q_scale;
   p.k_scale = k_scale;
   p.v_scale = v_scale;
@@ -622,6 +623,9 @@ extern "C" int fa_debug_set(const char* key, double value) {
   if (!strcmp(key, "tau")) {
     if (!(value >= 0.0 && value <= 16.0)) return fail(FA_ERR_INVALID_ARG, "tau in [0, 16]");
     g_knobs.tau_log2 = (float)value;
+  } else if (!strcmp(key, "fp8_tau")) {
+    if (!(value >= 0.0 && value <= 1.5)) return fail(FA_ERR_INVALID_ARG, "fp8_tau in [0, 1.5]");
+    g_knobs.fp8_tau = (float)value;
   } else if (!strcmp(key, "poly8") || !strcmp(key, "bwd_poly8") || !strcmp(key, "fp8_poly8")) {
     const int v = (int)value;
     if (v != 0 && v != 2 && v != 4) return fail(FA_ERR_INVALID_ARG, "poly8 in {0, 2, 4}");

@@ -14,13 +14,13 @@
 //     contiguous, so V^T is the K-major B operand of P V);
 //   * the block scales enter the softmax: S_raw (the exact fp32 sum of code
 //     products) times scale * log2(e) * q_scale(tile) * k_scale(block);
-//   * P is written to TMEM as e4m3, four weights per column, as 256 * p: the
-//     largest weight (256 <= 448) stays in range and weights down to 2^-14
-//     keep three mantissa bits instead of falling into e4m3's subnormals;
-//     the row sum l is taken over the same 256 * p in fp32, the LSE removes
-//     the factor, and O = O_acc * v_scale / l.
-// Rescaling is unconditional (threshold 0): a larger threshold would let the
-// weights exceed 448 before the reference moves.
+//   * P is written to TMEM as e4m3, four weights per column, as 2^7 * p
+//     relative to the row's reference maximum: weights down to 2^-13 of it
+//     keep three mantissa bits instead of falling into e4m3's subnormals,
+//     and with the rescale threshold tau clamped to 1.5 (base 2) the largest
+//     weight, 2^(7 + tau) <= 362, stays below e4m3's 448; the row sum l is
+//     taken over the same fp32 weights, the LSE removes the factor, and
+//     O = O_acc * v_scale / l.
 // Head dim 128, dense [B, S, H, d] layouts (no packed sequences).
 #include "exp2_poly.cuh"
 #include "internal.h"
@@ -45,7 +45,8 @@ constexpr int MMA_WARP = 8;
 constexpr int TMA_WARP = 9;
 constexpr int REGS_SOFTMAX = 192;
 constexpr int REGS_CONTROL = 112;
-constexpr float P_LOG2_OFFSET = 8.f;  // weights stored as 2^8 * p
+constexpr float P_LOG2_OFFSET = 7.f;  // weights stored as 2^7 * p
+constexpr float TAU_MAX = 1.5f;       // 2^(7 + 1.5) = 362 < 448
 
 struct Cfg {
   static constexpr int TILE_BYTES = 128 * 128;          // 128 rows x 128 one-byte elements
@@ -283,6 +284,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) fwd_fp8_kernel(const __grid_co
     const uint32_t lane_off = (uint32_t)(lg * 32) << 16;
     const uint32_t tS = tmem + lane_off + C::TM_S + t * 128;
     const uint32_t tO = tmem + lane_off + C::TM_O + t * D;
+    const float tau = fminf(fmaxf(p.tau, 0.f), TAU_MAX);   // the host allows [0, 1.5]
     Walker w;
     w.init(spec);
     uint32_t sp_it = 0;
@@ -344,8 +346,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) fwd_fp8_kernel(const __grid_co
         const float m_blk = fmaxf(fmax3(mx[0], mx[1], mx[2]), mx[3]) * c_j;
         if (j == 0) {
           m_ref = m_blk;
-        } else if (__any_sync(0xffffffffu, m_blk > m_ref)) {
-          const bool need = m_blk > m_ref;
+        } else if (__any_sync(0xffffffffu, m_blk > m_ref + tau)) {
+          const bool need = m_blk > m_ref + tau;
           const float m_new = need ? m_blk : m_ref;
           const float alpha = need ? ex2_mufu(m_ref - m_new) : 1.0f;
           const uint64_t a2 = f2pack(alpha, alpha);
@@ -365,7 +367,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) fwd_fp8_kernel(const __grid_co
           l *= alpha;
           m_ref = m_new;
         }
-        // weights 2^8 * p = exp2(S * c_j - m + 8), summed in fp32 and packed as e4m3
+        // weights 2^7 * p = exp2(S * c_j - m + 7), summed in fp32 and packed as e4m3
         const float msub = (m_ref == -INFINITY ? 0.f : m_ref) - P_LOG2_OFFSET;
         const uint64_t c2 = f2pack(c_j, c_j), negm2 = f2pack(-msub, -msub);
         uint64_t la2[2] = {f2pack(0.f, 0.f), f2pack(0.f, 0.f)};

@@ -30,6 +30,7 @@ enum WaitSite : int {
 // Runtime knobs (settable through fa_debug_set; defaults are the tuned values).
 struct Knobs {
   float tau_log2 = 0.0f;         // rescale threshold, base-2 units
+  float fp8_tau = 1.5f;          // the same for the FP8 forward (at most 1.5)
   int poly8 = 0;                 // eighths of the exponentials done by the polynomial (fwd)
   int bwd_poly8 = 0;             // same for the backward
   int fp8_poly8 = 0;             // same for the FP8 forward

@@ -219,6 +219,8 @@ FA_API int fa_get_device_error(int* code, int clear);
 /*
  * Test and tuning knobs (not part of the numerical contract). Keys:
  *   "tau"        conditional-rescale threshold, base-2 units (default 0)
+ *   "fp8_tau"    the same for the FP8 forward, in [0, 1.5] (default 1.5: the
+ *                stored weights 2^(7 + tau) * p stay below e4m3's 448)
  *   "poly8"      forward: eighths of the exponentials computed by the FMA-pipe
  *                polynomial instead of MUFU ex2 (0, 2 or 4)
  *   "bwd_poly8"  the same for the backward

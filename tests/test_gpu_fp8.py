@@ -14,7 +14,7 @@
     5e-2 leaves headroom for bf16 output rounding. A structural error (a
     wrong block scale, a dropped key block, a transposed operand) is off by
     tens of percent or more;
-  - Q = 0 makes every weight exactly 1 (2^8 in the kernel, exact in e4m3), so
+  - Q = 0 makes every weight exactly 1 (2^7 in the kernel, exact in e4m3), so
     O is the plain mean of the visible V rows: checked to 4e-3 max-abs (bf16
     output rounding).
 """
@@ -173,3 +173,19 @@ def test_fp8_full_size_parity(name):
     print(f"\nfp8 {name}: LSE max-abs {e_lse:.2e}, O rel-L2 (worst head) {e_o:.2e}")
     assert e_lse <= LSE_TOL
     assert e_o <= O_REL_L2_FP8
+
+
+@pytest.mark.parametrize("tau", [0.0, 1.0])
+def test_fp8_forward_rescale_threshold(tau):
+    """Thresholds other than the default 1.5 (the largest weight the kernel
+    stores, 2^(7 + tau), stays below e4m3's 448 for any tau <= 1.5): same
+    bounds."""
+    fa.fa_debug_set("fp8_tau", tau)
+    try:
+        o, lse, ro, rl = _fp8_case(2, 4, 2, 300, 1000, True, seed=120 + int(tau))
+    finally:
+        fa.fa_debug_set("fp8_tau", 1.5)
+    assert max_abs(lse, rl) <= LSE_TOL
+    assert _rel_l2_per_head(o, ro) <= O_REL_L2_FP8
+    with pytest.raises(fa.FAError):
+        fa.fa_debug_set("fp8_tau", 2.0)
