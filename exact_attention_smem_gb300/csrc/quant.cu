@@ -12,7 +12,9 @@
 //         K-major operand of the P V product.
 // scale = amax / 448 (the largest e4m3 value), 1 when amax = 0; code =
 // e4m3(x / scale), rounded to nearest even with saturation, all in float32.
-// HBM-bound: each kernel reads its input once and writes the codes once.
+// HBM-bound: Q and K are read once and their codes written once; V is read
+// twice (its per-head amax first) and its codes written once, transposed
+// through shared memory.
 #include "internal.h"
 
 #include <cuda_fp8.h>
@@ -129,10 +131,12 @@ __global__ void __launch_bounds__(THREADS) v_quant_t_kernel(const __nv_bfloat16*
   const int k0 = blk * ROWS;
   const int nrows = S - k0 < ROWS ? S - k0 : ROWS;
   const float s = scale_of(__uint_as_float(vmax[(long long)b * H + h]));
+  // lanes take consecutive keys of one 8-column group, so a warp's byte
+  // writes into each tile row land in 32 consecutive bytes (no bank conflict)
 #pragma unroll
   for (int i = 0; i < PER; ++i) {
     const int idx = i * THREADS + threadIdx.x;
-    const int r = idx / VPR, c = (idx % VPR) * 8;
+    const int r = idx % ROWS, c = (idx / ROWS) * 8;
     uint2 q = make_uint2(0, 0);
     if (r < nrows)
       q = quant8(*reinterpret_cast<const uint4*>(x + (((long long)b * S + k0 + r) * H + h) * D + c), s);
