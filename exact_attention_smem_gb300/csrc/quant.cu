@@ -11,7 +11,8 @@
 //         rounded up to 16, the pad holding zero codes), so that V^T is a
 //         K-major operand of the P V product.
 // scale = amax / 448 (the largest e4m3 value), 1 when amax = 0; code =
-// e4m3(x / scale), rounded to nearest even with saturation, all in float32.
+// e4m3(x * r) with r = 1 / scale (one float32 division per block, a multiply
+// per element), rounded to nearest even with saturation, all in float32.
 // HBM-bound: Q and K are read once and their codes written once; V is read
 // twice (its per-head amax first) and its codes written once, transposed
 // through shared memory.
@@ -39,11 +40,14 @@ __device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
   return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
 }
 
-// eight bf16 values / s -> eight e4m3 codes (first value in the lowest byte)
-__device__ __forceinline__ uint2 quant8(const uint4& v, float s) {
+// eight bf16 values * rs -> eight e4m3 codes (first value in the lowest byte);
+// __fmul_rn keeps each product a plain rounded multiply (never fused)
+__device__ __forceinline__ uint2 quant8(const uint4& v, float rs) {
   uint2 r;
-  r.x = e4m3x2(bf16_lo(v.x) / s, bf16_hi(v.x) / s) | (e4m3x2(bf16_lo(v.y) / s, bf16_hi(v.y) / s) << 16);
-  r.y = e4m3x2(bf16_lo(v.z) / s, bf16_hi(v.z) / s) | (e4m3x2(bf16_lo(v.w) / s, bf16_hi(v.w) / s) << 16);
+  r.x = e4m3x2(__fmul_rn(bf16_lo(v.x), rs), __fmul_rn(bf16_hi(v.x), rs)) |
+        (e4m3x2(__fmul_rn(bf16_lo(v.y), rs), __fmul_rn(bf16_hi(v.y), rs)) << 16);
+  r.y = e4m3x2(__fmul_rn(bf16_lo(v.z), rs), __fmul_rn(bf16_hi(v.z), rs)) |
+        (e4m3x2(__fmul_rn(bf16_lo(v.w), rs), __fmul_rn(bf16_hi(v.w), rs)) << 16);
   return r;
 }
 
@@ -84,13 +88,14 @@ __global__ void __launch_bounds__(THREADS) quant_rows_kernel(const __nv_bfloat16
     }
   }
   const float s = scale_of(block_max(m, red));
+  const float rs = 1.f / s;
   if (threadIdx.x == 0) scales[((long long)b * H + h) * gridDim.x + blk] = s;
 #pragma unroll
   for (int i = 0; i < PER; ++i) {
     const int idx = i * THREADS + threadIdx.x;
     const int r = idx / VPR, c = (idx % VPR) * 8;
     if (r < nrows)
-      *reinterpret_cast<uint2*>(codes + (((long long)b * S + r0 + r) * H + h) * D + c) = quant8(v[i], s);
+      *reinterpret_cast<uint2*>(codes + (((long long)b * S + r0 + r) * H + h) * D + c) = quant8(v[i], rs);
   }
 }
 
@@ -130,7 +135,7 @@ __global__ void __launch_bounds__(THREADS) v_quant_t_kernel(const __nv_bfloat16*
   const int blk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int k0 = blk * ROWS;
   const int nrows = S - k0 < ROWS ? S - k0 : ROWS;
-  const float s = scale_of(__uint_as_float(vmax[(long long)b * H + h]));
+  const float rs = 1.f / scale_of(__uint_as_float(vmax[(long long)b * H + h]));
   // lanes take consecutive keys of one 8-column group, so a warp's byte
   // writes into each tile row land in 32 consecutive bytes (no bank conflict)
 #pragma unroll
@@ -139,7 +144,7 @@ __global__ void __launch_bounds__(THREADS) v_quant_t_kernel(const __nv_bfloat16*
     const int r = idx % ROWS, c = (idx / ROWS) * 8;
     uint2 q = make_uint2(0, 0);
     if (r < nrows)
-      q = quant8(*reinterpret_cast<const uint4*>(x + (((long long)b * S + k0 + r) * H + h) * D + c), s);
+      q = quant8(*reinterpret_cast<const uint4*>(x + (((long long)b * S + k0 + r) * H + h) * D + c), rs);
 #pragma unroll
     for (int e = 0; e < 8; ++e)
       tile[(c + e) * TS + r] = (uint8_t)(((e < 4 ? q.x : q.y) >> (8 * (e & 3))) & 0xffu);

@@ -82,8 +82,9 @@ FA_API int fa_fwd(const void* q, const void* k, const void* v, void* o, float* l
  *     [B, H, ceil(S/128)], one per 128-row block over its rows and d columns.
  *   layout 1 (V): codes transposed, [B, H, d, S_pad] with S_pad = S rounded
  *     up to 16 (the pad holds zero codes); scales float [B, H].
- * scale = amax / 448 (1 if amax = 0); code = e4m3(x / scale), float32
- * division, round to nearest even, saturating at +-448. Runs on `stream`
+ * scale = amax / 448 (1 if amax = 0); code = e4m3(x * r) with r = 1 / scale
+ * (scale, r and each product rounded to float32), round to nearest even,
+ * saturating at +-448. Runs on `stream`
  * (layout 1: a memset and three kernels, with `scales` as their scratch).
  * Errors: FA_ERR_INVALID_ARG (NULL or misaligned pointer, bad sizes or
  * layout), FA_ERR_UNSUPPORTED (d), FA_ERR_CUDA.

@@ -16,10 +16,11 @@ choice below is a stated reading, the plainest one the rest supports:
   representable value, ties to the even code, and saturates to +-448.
 * Q and K are quantized per (sequence, head, block of 128 rows): scale =
   amax / 448 over the block's rows and all d columns (1 when amax = 0), code =
-  e4m3(x / scale). V is quantized per (sequence, head) over all its rows, and
-  stored transposed ([B, H, d, S_pad], keys contiguous, S_pad = S rounded up
-  to 16, the pad written as zero codes). The scale and x / scale are computed
-  in float32 (IEEE division), so the GPU makes the same decisions.
+  e4m3(x * r) with r = 1 / scale rounded to float32 once per block. V is
+  quantized per (sequence, head) over all its rows, and stored transposed
+  ([B, H, d, S_pad], keys contiguous, S_pad = S rounded up to 16, the pad
+  written as zero codes). scale, r and x * r are each rounded to float32
+  (IEEE division and multiply), so the GPU makes the same decisions.
 * The FP8 forward is exact attention over the dequantized inputs
   q_hat = decode(code) * scale (and likewise k_hat, v_hat). The kernel rounds
   the softmax weights to e4m3 before its P V product; that rounding is the one
@@ -93,7 +94,7 @@ def quantize_row_blocks(x, block: int = BLOCK):
                 amax = np.float32(np.abs(blk).max()) if blk.size else np.float32(0)
                 s = np.float32(amax / np.float32(E4M3_MAX)) if amax > 0 else np.float32(1.0)
                 scales[b, h, i] = s
-                codes[b, i * block:(i + 1) * block, h, :] = e4m3_encode(blk / s)
+                codes[b, i * block:(i + 1) * block, h, :] = e4m3_encode(blk * (np.float32(1) / s))
     return codes, scales
 
 
@@ -114,7 +115,7 @@ def quantize_v_transposed(v):
             amax = np.float32(np.abs(blk).max()) if blk.size else np.float32(0)
             s = np.float32(amax / np.float32(E4M3_MAX)) if amax > 0 else np.float32(1.0)
             scales[b, h] = s
-            codes[b, h, :, :S] = e4m3_encode(blk / s).T
+            codes[b, h, :, :S] = e4m3_encode(blk * (np.float32(1) / s)).T
     return codes, scales
 
 

@@ -1,8 +1,8 @@
 """FP8 (e4m3) path: quantization and forward against the oracle.
 
 * fa_quantize_fp8: codes and scales bit-exact against the oracle's quantizer
-  (both sides take every decision in float32: amax, amax / 448, x / scale,
-  round to nearest even with saturation).
+  (both sides take every decision in float32: amax, amax / 448, 1 / scale,
+  x * (1 / scale), round to nearest even with saturation).
 * fa_fwd_fp8 against exact fp64 attention over the dequantized inputs:
   - LSE max-abs <= 1e-3: the scores are exact sums of code products
     accumulated in fp32, as in the bf16 forward;

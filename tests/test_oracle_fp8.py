@@ -104,7 +104,9 @@ def test_v_quantizer_layout():
     for b in range(2):
         for h in range(2):
             assert scales[b, h] == np.float32(np.abs(v[b, :, h]).max() / np.float32(448))
-            assert np.array_equal(codes[b, h, :, :37].T, f8.e4m3_encode(v[b, :, h] / scales[b, h]))
+            r = np.float32(1) / scales[b, h]
+            assert r.dtype == np.float32 and (v[b, :, h] * r).dtype == np.float32
+            assert np.array_equal(codes[b, h, :, :37].T, f8.e4m3_encode(v[b, :, h] * r))
     back = f8.dequantize_v_transposed(codes, scales, 37)
     assert np.abs(back - v).max() <= np.abs(v).max() * 2.0 ** -4
 
