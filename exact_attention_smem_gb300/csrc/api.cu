@@ -299,6 +299,7 @@ extern "C" int fa_quantize_fp8(const void* x, int B, int S, int H, int d, int la
   if (d != 64 && d != 128) return fail(FA_ERR_UNSUPPORTED, "head dim %d (supported: 64, 128)", d);
   if ((long long)B * H > (1LL << 30) || (long long)S * H * d > (1LL << 40))
     return fail(FA_ERR_INVALID_ARG, "sizes too large");
+  if (B == 0 || S == 0) return FA_OK;
   DevInfo* di = nullptr;
   int st = device_info(&di);
   if (st != FA_OK) return st;

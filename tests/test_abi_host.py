@@ -88,3 +88,36 @@ def test_debug_knobs(lib):
     assert lib.fa_debug_set(b"poly8", 3.0) == 1
     assert lib.fa_debug_set(b"nope", 1.0) == 1
     assert lib.fa_debug_set(None, 1.0) == 1
+
+
+def test_fp8_entry_points_validate_before_any_device_work(lib):
+    f = FAKE
+    # fa_fwd_fp8(q8, k8, vt8, q_scale, k_scale, v_scale, o, lse, B, Hq, Hkv, Sq, Sk, d, causal, scale)
+    ok = [f] * 8 + [1, 2, 2, 16, 16, 128, 1, 0.1]
+    def fwd8(**kw):
+        a = list(ok)
+        for i, v in kw.items():
+            a[int(i[1:])] = v
+        return lib.fa_fwd_fp8(*a, None)
+    assert fwd8(a0=None) == 1 and fwd8(a5=None) == 1 and fwd8(a7=None) == 1
+    assert fwd8(a2=f + 4) == 1                      # vt8 not 16-byte aligned
+    assert fwd8(a13=64) == 2                        # head dim 128 only
+    assert fwd8(a9=3) == 1                          # Hq % Hkv
+    assert fwd8(a15=float("nan")) == 1 and fwd8(a15=0.0) == 1
+    assert fwd8(a8=0) == 0 and fwd8(a11=0) == 0     # nothing to do
+    # fa_quantize_fp8(x, B, S, H, d, layout, codes, scales)
+    assert lib.fa_quantize_fp8(None, 1, 16, 1, 128, 0, f, f, None) == 1
+    assert lib.fa_quantize_fp8(f, 1, 16, 1, 128, 2, f, f, None) == 1
+    assert lib.fa_quantize_fp8(f, 1, 16, 1, 96, 0, f, f, None) == 2
+    assert lib.fa_quantize_fp8(f + 8, 1, 16, 1, 128, 1, f, f, None) == 1
+    assert lib.fa_quantize_fp8(f, 0, 16, 1, 128, 1, f, f, None) == 0
+    assert lib.fa_last_error() is not None
+
+
+def test_fp8_knobs(lib):
+    assert lib.fa_debug_set(b"fp8_tau", 0.0) == 0
+    assert lib.fa_debug_set(b"fp8_tau", 1.5) == 0
+    assert lib.fa_debug_set(b"fp8_tau", 1.6) == 1     # 2^(7 + tau) must stay below 448
+    assert lib.fa_debug_set(b"fp8_poly8", 2.0) == 0
+    assert lib.fa_debug_set(b"fp8_poly8", 0.0) == 0
+    assert lib.fa_debug_set(b"fp8_poly8", 1.0) == 1
