@@ -12,66 +12,119 @@
 // entry 14: Ring Attention with Blockwise Transformers).
 // A row that saw no key in a part has LSE_p = +inf and O_p = 0 (the forward's
 // convention) and counts zero; a row that saw no key in any part gets O = 0,
-// LSE = +inf. Memory-bound: one warp per (row, head).
+// LSE = +inf. Memory-bound: a group of d/8 lanes per (row, head), each lane
+// moving 16 bytes per part; items run with the row index fastest, the order
+// of both LSE layouts, so their LSE reads are contiguous.
 #include "internal.h"
 #include "ptx.cuh"
 
 #include <cmath>
 
 namespace fa {
+using ptx::pack_bf16x2;
 
 namespace {
 
 constexpr int MAX_PARTS = 64;
+constexpr int THREADS = 256;
 
-__global__ void merge_kernel(const __nv_bfloat16* __restrict__ o_parts,
-                             const float* __restrict__ lse_parts, int P, long long rows, int Hq,
-                             int S, int d, int packed, __nv_bfloat16* __restrict__ o,
-                             float* __restrict__ lse) {
-  const int lane = threadIdx.x & 31;
-  const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
-  const long long part_o = rows * Hq * d, part_l = rows * Hq;
-  for (long long rh = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-       rh < rows * Hq; rh += warps) {
-    const long long t = rh / Hq;
-    const int h = (int)(rh % Hq);
-    // the forward's LSE layout: dense [B][Hq][S], packed [Hq][T]
-    const long long li = packed ? (long long)h * rows + t
-                                : ((t / S) * Hq + h) * (long long)S + (t % S);
+__device__ __forceinline__ void add8(float (&acc)[8], float w, const uint4& v) {
+  const uint32_t x[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    acc[2 * i] = fmaf(w, __uint_as_float(x[i] << 16), acc[2 * i]);
+    acc[2 * i + 1] = fmaf(w, __uint_as_float(x[i] & 0xffff0000u), acc[2 * i + 1]);
+  }
+}
+
+// LPI lanes per item (a power of two >= d / 8); lane `sub` owns columns
+// [8 sub, 8 sub + 8). Item i: dense (b, h, s) = (i / (Hq S), i / S % Hq, i % S),
+// packed (h, t) = (i / T, i % T); its LSE entry is i in both layouts.
+template <int LPI>
+__global__ void __launch_bounds__(THREADS) merge_kernel(const __nv_bfloat16* __restrict__ o_parts,
+                                                        const float* __restrict__ lse_parts, int P,
+                                                        long long rows, int Hq, int S, int d,
+                                                        int packed, __nv_bfloat16* __restrict__ o,
+                                                        float* __restrict__ lse) {
+  constexpr int IPB = THREADS / LPI;
+  const int sub = threadIdx.x % LPI;
+  const bool active = sub * 8 < d;
+  const long long items = rows * Hq, part_o = rows * Hq * d;
+  for (long long i = (long long)blockIdx.x * IPB + threadIdx.x / LPI; i < items;
+       i += (long long)gridDim.x * IPB) {
+    long long t;
+    int h;
+    if (packed) {
+      h = (int)(i / rows);
+      t = i - (long long)h * rows;
+    } else {
+      const long long bh = i / S;
+      t = (bh / Hq) * S + (i - bh * S);
+      h = (int)(bh % Hq);
+    }
     float m = -INFINITY;
-    for (int q = lane; q < P; q += 32) {
-      const float l = lse_parts[q * part_l + li];
+    for (int q = 0; q < P; ++q) {
+      const float l = lse_parts[q * items + i];
       if (l != INFINITY) m = fmaxf(m, l);
     }
-    for (int sh = 16; sh > 0; sh >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, sh));
-    __nv_bfloat16* orow = o + rh * d;
+    const long long orow = (t * Hq + h) * d + sub * 8;
     if (m == -INFINITY) {                                // no key in any part
-      for (int c = lane; c < d; c += 32) orow[c] = __float2bfloat16(0.f);
-      if (lane == 0) lse[li] = INFINITY;
+      if (active) *reinterpret_cast<uint4*>(o + orow) = make_uint4(0, 0, 0, 0);
+      if (sub == 0) lse[i] = INFINITY;
       continue;
     }
     float wsum = 0.f;
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // columns lane + 32e (d <= 256)
-    for (int q = 0; q < P; ++q) {
-      const float l = lse_parts[q * part_l + li];
-      if (l == INFINITY) continue;
-      const float wq = expf(l - m);
-      wsum += wq;
-      const __nv_bfloat16* prow = o_parts + q * part_o + rh * d;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    int q = 0;
+    for (; q + 4 <= P; q += 4) {                         // four parts' loads in flight
+      float w[4];
+      uint4 v[4];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int c = lane + 32 * e;
-        if (c < d) acc[e] = fmaf(wq, __bfloat162float(prow[c]), acc[e]);
+      for (int u = 0; u < 4; ++u) {
+        const float l = lse_parts[(q + u) * items + i];
+        w[u] = l == INFINITY ? 0.f : expf(l - m);
+        v[u] = active && l != INFINITY
+                   ? *reinterpret_cast<const uint4*>(o_parts + (q + u) * part_o + orow)
+                   : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {                   // a part without keys adds 0 * 0
+        wsum += w[u];
+        add8(acc, w[u], v[u]);
       }
     }
-    const float inv = 1.0f / wsum;
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const int c = lane + 32 * e;
-      if (c < d) orow[c] = __float2bfloat16(acc[e] * inv);
+    for (; q < P; ++q) {
+      const float l = lse_parts[q * items + i];
+      if (l == INFINITY) continue;
+      const float w = expf(l - m);
+      wsum += w;
+      add8(acc, w, active ? *reinterpret_cast<const uint4*>(o_parts + q * part_o + orow)
+                          : make_uint4(0, 0, 0, 0));
     }
-    if (lane == 0) lse[li] = m + logf(wsum);
+    if (active) {
+      const float inv = 1.0f / wsum;
+      uint4 r;
+      r.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+      r.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+      r.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
+      r.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
+      *reinterpret_cast<uint4*>(o + orow) = r;
+    }
+    if (sub == 0) lse[i] = m + logf(wsum);
   }
+}
+
+template <int LPI>
+cudaError_t launch_lpi(const __nv_bfloat16* o_parts, const float* lse_parts, int P,
+                       long long rows, int Hq, int S, int d, int packed, __nv_bfloat16* o,
+                       float* lse, cudaStream_t stream) {
+  constexpr int IPB = THREADS / LPI;
+  const long long items = rows * Hq;
+  const long long want = (items + IPB - 1) / IPB;
+  const int blocks = (int)(want < 152 * 16 ? want : 152 * 16);
+  merge_kernel<LPI><<<blocks, THREADS, 0, stream>>>(o_parts, lse_parts, P, rows, Hq, S, d, packed,
+                                                    o, lse);
+  return cudaGetLastError();
 }
 
 }  // namespace
@@ -79,13 +132,11 @@ __global__ void merge_kernel(const __nv_bfloat16* __restrict__ o_parts,
 cudaError_t launch_merge(const __nv_bfloat16* o_parts, const float* lse_parts, int P,
                          long long rows, int Hq, int S, int d, int packed, __nv_bfloat16* o,
                          float* lse, cudaStream_t stream) {
-  if (P < 1 || P > MAX_PARTS) return cudaErrorInvalidValue;
-  const long long items = rows * Hq;
-  if (items == 0) return cudaSuccess;
-  const long long want = (items + 7) / 8;
-  const int blocks = (int)(want < 152 * 32 ? want : 152 * 32);
-  merge_kernel<<<blocks, 256, 0, stream>>>(o_parts, lse_parts, P, rows, Hq, S, d, packed, o, lse);
-  return cudaGetLastError();
+  if (P < 1 || P > MAX_PARTS || d % 64 != 0 || d > 256) return cudaErrorInvalidValue;
+  if (rows * Hq == 0) return cudaSuccess;
+  if (d == 64) return launch_lpi<8>(o_parts, lse_parts, P, rows, Hq, S, d, packed, o, lse, stream);
+  if (d == 128) return launch_lpi<16>(o_parts, lse_parts, P, rows, Hq, S, d, packed, o, lse, stream);
+  return launch_lpi<32>(o_parts, lse_parts, P, rows, Hq, S, d, packed, o, lse, stream);
 }
 
 }  // namespace fa

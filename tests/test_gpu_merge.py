@@ -103,3 +103,20 @@ def test_rejects_bad_arguments():
     with pytest.raises(fa.FAError) as e:
         fa.fa_merge(x, x, 2, 1, 1, 1, 96, False, x, x)
     assert e.value.status == 2
+
+
+@pytest.mark.parametrize("d", [192, 256])
+def test_six_shards_large_head_dim(d):
+    """Six uneven key shards (the merge's four-part group plus a remainder)
+    at the head dims of the one-tile forward."""
+    x = random_inputs(B=1, Hq=2, Hkv=1, Sq=257, Sk=900, d=d, seed=340 + d, device="cuda")
+    scale = d ** -0.5
+    cuts = [0, 1, 130, 300, 301, 640, 900]
+    parts = []
+    for a, b in zip(cuts[:-1], cuts[1:]):
+        k, v = x.k[:, a:b].contiguous(), x.v[:, a:b].contiguous()
+        parts.append(fa.forward(x.q, k, v, causal=False, scale=scale))
+    o, lse = _merge(parts, 1, 2, 257, d)
+    ro, rl = oracle.forward(x.q.cpu(), x.k.cpu(), x.v.cpu(), scale, False)
+    assert max_abs(o, ro) <= O_TOL
+    assert max_abs(lse, rl) <= LSE_TOL
