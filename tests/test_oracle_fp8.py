@@ -132,3 +132,23 @@ def test_fp8_forward_is_attention_of_dequantized_inputs(causal):
     o8, l8 = f8.forward_fp8(qc, qs, qc, qs, vc, vs, 0.125, causal)
     o, l = fwd64(x, x, x, 0.125, causal)
     assert np.allclose(o8, o, atol=1e-12) and np.allclose(l8, l, atol=1e-12)
+
+
+@pytest.mark.parametrize("Sk", [128, 2048])
+def test_weight_rounding_error_matches_the_tolerance_derivation(Sk):
+    """The FP8 forward's O tolerance (rel-L2 5e-2) comes from rounding each
+    softmax weight to e4m3 (relative error <= 2^-4, RMS <= 2^-4/sqrt(3) = 3.6%).
+    Rounding exact weights (as 2^7 p, the kernel's storage) with the oracle's
+    codec on random rows gives an output error of that size: below the bound,
+    and not so far below that the bound would be vacuous."""
+    rng = np.random.default_rng(Sk)
+    rows, d = 256, 64
+    s = rng.standard_normal((rows, Sk))                  # scores ~ N(0, 1)
+    v = rng.standard_normal((Sk, d))
+    p = np.exp2((s - s.max(axis=1, keepdims=True)) * 1.4426950408889634 + 7)
+    o = (p @ v) / p.sum(axis=1, keepdims=True)
+    p8 = f8.e4m3_decode(f8.e4m3_encode(p))
+    o8 = (p8 @ v) / p.sum(axis=1, keepdims=True)         # row sum from the fp32 weights
+    rel = np.linalg.norm(o8 - o) / np.linalg.norm(o)
+    assert 0.005 < rel < 0.05
+    assert np.abs(p8 / np.where(p > 0, p, 1) - 1)[p >= 2.0 ** -6].max() <= 2.0 ** -4
