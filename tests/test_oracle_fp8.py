@@ -152,3 +152,76 @@ def test_weight_rounding_error_matches_the_tolerance_derivation(Sk):
     rel = np.linalg.norm(o8 - o) / np.linalg.norm(o)
     assert 0.005 < rel < 0.05
     assert np.abs(p8 / np.where(p > 0, p, 1) - 1)[p >= 2.0 ** -6].max() <= 2.0 ** -4
+
+
+# ---------------------------------------------------------------------------
+# Mutation tests: plant a plausible mistake in a copy of the FP8 oracle and
+# check that at least one pin catches it.
+# ---------------------------------------------------------------------------
+import inspect  # noqa: E402
+
+_F8_MUTATIONS = [
+    ("np.exp2(e.astype(np.float64) - 7)", "np.exp2(e.astype(np.float64) - 8)"),   # exponent bias
+    ("(hi % 2 == 0)", "(hi % 2 == 1)"),                                            # ties to odd
+    ("amax / np.float32(E4M3_MAX)", "amax / np.float32(447)"),                     # scale constant
+    ("e4m3_encode(blk * (np.float32(1) / s)).T", "e4m3_encode(blk * (np.float32(1) / s)).T[::-1]"),  # V^T rows
+    ("vh = e4m3_decode(vc[b, g, :, :Sk]).T * vs[b, g]", "vh = e4m3_decode(vc[b, g, :, :Sk]).T"),  # V scale
+    ("g = h // group", "g = h % Hkv"),                                             # GQA head map
+    ("np.repeat(qs[b, h], BLOCK)[:Sq, None]", "qs[b, h, 0]"),                      # one Q scale
+]
+
+
+def _f8_mutant(old, new):
+    src = inspect.getsource(f8)
+    assert old in src, old
+    src = src.replace(old, new).replace(
+        "from .attention_fp64 import attend_head as _attend_head",
+        "from oracle.attention_fp64 import attend_head as _attend_head")
+    ns = {"__name__": "fp8_mutant"}
+    exec(compile(src, "<fp8_mutant>", "exec"), ns)
+    return ns
+
+
+def _f8_pins_pass(m):
+    try:
+        dec, enc = m["e4m3_decode"], m["e4m3_encode"]
+        if not (dec(0x7E) == 448.0 and dec(0x08) == 2.0 ** -6 and dec(0x01) == 2.0 ** -9
+                and dec(0x38) == 1.0):
+            return False
+        if not (enc(1.0 + 1 / 16) == 0x38 and enc(1.0 + 3 / 16) == 0x3A and enc(2.0 ** -10) == 0):
+            return False
+        codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], dtype=np.uint8)
+        if not np.array_equal(enc(dec(codes)), codes):
+            return False
+        rng = np.random.default_rng(11)
+        x = rng.standard_normal((1, 300, 4, 64)).astype(np.float32) * rng.uniform(
+            0.2, 3, (1, 300, 1, 1)).astype(np.float32)
+        qc, qs = m["quantize_row_blocks"](x)
+        for i in range(3):
+            amax = np.abs(x[0, i * 128:(i + 1) * 128, 1]).max()
+            if qs[0, 1, i] != np.float32(amax / np.float32(448)):
+                return False
+        vc, vs = m["quantize_v_transposed"](x[:, :, :2])
+        r = np.float32(1) / vs[0, 1]
+        if not np.array_equal(vc[0, 1, :, :300].T, f8.e4m3_encode(x[0, :, 1] * r)):
+            return False
+        # varying block scales and GQA: forward_fp8 against fp64 attention over
+        # the dequantized inputs, built with the pinned dequantizers
+        kc, ks = m["quantize_row_blocks"](x[:, :, :2])
+        for causal in (False, True):
+            o8, l8 = m["forward_fp8"](qc, qs, kc, ks, vc, vs, 0.125, causal)
+            q = f8.dequantize_row_blocks(qc, qs)
+            k = f8.dequantize_row_blocks(kc, ks)
+            v = f8.dequantize_v_transposed(vc, vs, 300)
+            o, l = fwd64(q, k, v, 0.125, causal)
+            if not (np.allclose(o8, o, atol=1e-12) and np.allclose(l8, l, atol=1e-12)):
+                return False
+    except Exception:
+        return False
+    return True
+
+
+@pytest.mark.parametrize("old,new", _F8_MUTATIONS, ids=[m[1][:28] for m in _F8_MUTATIONS])
+def test_fp8_pins_catch_planted_mistakes(old, new):
+    assert _f8_pins_pass(_f8_mutant("", ""))          # the unmodified copy passes
+    assert not _f8_pins_pass(_f8_mutant(old, new))
