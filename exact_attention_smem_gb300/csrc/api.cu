@@ -571,6 +571,8 @@ extern "C" int fa_merge(const void* o_parts, const float* lse_parts, int P, int 
   const void* ptrs[4] = {o_parts, lse_parts, o, lse};
   for (int i = 0; i < 4; ++i)
     if (!ptrs[i]) return fail(FA_ERR_INVALID_ARG, "pointer %d is NULL", i);
+  if (!aligned16(o_parts) || !aligned16(o))   // the kernel moves 16-byte vectors
+    return fail(FA_ERR_INVALID_ARG, "o_parts and o must be 16-byte aligned");
   if (P < 1 || P > 64) return fail(FA_ERR_INVALID_ARG, "parts P=%d (1..64)", P);
   if (B < 0 || Hq <= 0 || S < 0) return fail(FA_ERR_INVALID_ARG, "bad sizes B=%d Hq=%d S=%d", B, Hq, S);
   if (d != 64 && d != 128 && d != 192 && d != 256)

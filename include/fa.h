@@ -196,8 +196,10 @@ FA_API int fa_bwd_varlen(const void* q, const void* k, const void* v, const void
  *             ([B,Hq,S] dense, [Hq,T] packed)
  *   packed    0 dense, 1 packed (B is then unused)
  *   o, lse    outputs in the same layouts (must not alias the parts)
- * 1 <= P <= 64, d in {64, 128, 192, 256}. Asynchronous on `stream`; allocates
- * nothing.
+ * 1 <= P <= 64, d in {64, 128, 192, 256}; o_parts and o 16-byte aligned.
+ * Asynchronous on `stream`; allocates nothing. Errors: FA_ERR_INVALID_ARG
+ * (NULL or misaligned pointer, P or sizes out of range), FA_ERR_UNSUPPORTED
+ * (d), FA_ERR_CUDA.
  */
 FA_API int fa_merge(const void* o_parts, const float* lse_parts, int P, int B, int Hq, int S,
                     int d, int packed, void* o, float* lse, void* stream);

@@ -121,3 +121,15 @@ def test_fp8_knobs(lib):
     assert lib.fa_debug_set(b"fp8_poly8", 2.0) == 0
     assert lib.fa_debug_set(b"fp8_poly8", 0.0) == 0
     assert lib.fa_debug_set(b"fp8_poly8", 1.0) == 1
+
+
+def test_merge_validates_before_any_device_work(lib):
+    f = FAKE
+    # fa_merge(o_parts, lse_parts, P, B, Hq, S, d, packed, o, lse, stream)
+    assert lib.fa_merge(None, f, 2, 1, 1, 16, 128, 0, f, f, None) == 1
+    assert lib.fa_merge(f + 2, f, 2, 1, 1, 16, 128, 0, f, f, None) == 1   # 16-byte vectors
+    assert lib.fa_merge(f, f, 2, 1, 1, 16, 128, 0, f + 8, f, None) == 1
+    assert lib.fa_merge(f, f, 0, 1, 1, 16, 128, 0, f, f, None) == 1
+    assert lib.fa_merge(f, f, 65, 1, 1, 16, 128, 0, f, f, None) == 1
+    assert lib.fa_merge(f, f, 2, 1, 1, 16, 96, 0, f, f, None) == 2
+    assert lib.fa_merge(f, f, 2, 0, 1, 16, 128, 0, f, f, None) == 0      # nothing to do
