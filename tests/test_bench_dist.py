@@ -47,3 +47,30 @@ def test_single_process_is_identity():
     import bench
     assert bench.max_over_ranks(3.5) == 3.5
     assert bench.job_tflops(2e12, 5, 1, 1000.0) == pytest.approx(10.0)
+
+
+def test_reference_arm_json_contract():
+    """`bench.py --impl reference` (the fp64 oracle on the host cores, a
+    bounded sample per step) prints one JSON line with the bench contract's
+    keys, its own e2e with no host-device bytes and a cpu_baseline entry."""
+    import json
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference",
+                        "--steps", "1", "--warmup", "0", "--workload", "mha_s2048_causal"],
+                       capture_output=True, text=True, timeout=300, cwd=root)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    out = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "cpu_baseline", "e2e"):
+        assert key in out, key
+    assert out["impl"] == "reference" and out["value"] > 0 and out["unit"] == "TFLOP/s"
+    assert out["higher_is_better"] is True and out["dtype"] == "f64"
+    assert out["config"]["workload"] == "mha_s2048_causal"
+    assert out["cpu_baseline"]["kind"] == "oracle" and out["cpu_baseline"]["value"] == out["value"]
+    assert out["e2e"]["h2d_bytes_per_step"] == 0 and out["e2e"]["d2h_bytes_per_step"] == 0
