@@ -133,3 +133,18 @@ def test_merge_validates_before_any_device_work(lib):
     assert lib.fa_merge(f, f, 65, 1, 1, 16, 128, 0, f, f, None) == 1
     assert lib.fa_merge(f, f, 2, 1, 1, 16, 96, 0, f, f, None) == 2
     assert lib.fa_merge(f, f, 2, 0, 1, 16, 128, 0, f, f, None) == 0      # nothing to do
+
+
+def test_every_knob_is_documented_and_accepted(lib):
+    """The keys fa_debug_set accepts are exactly the ones fa.h documents."""
+    api = open(os.path.join(ROOT, "exact_attention_smem_gb300", "csrc", "api.cu")).read()
+    accepted = set(re.findall(r'strcmp\(key, "([a-z_0-9]+)"\)', api))
+    hdr = open(os.path.join(ROOT, "include", "fa.h")).read()
+    block = hdr[hdr.index("Test and tuning knobs"):hdr.index("FA_API int fa_debug_set")]
+    documented = set(re.findall(r'"([a-z_0-9]+)"', block))
+    assert accepted == documented
+    defaults = {"tau": 0.0, "poly8": 0.0, "bwd_poly8": 0.0, "fp8_poly8": 0.0, "fp8_tau": 1.5,
+                "timeout_ms": 2000.0, "grid": 0.0, "bwd_mode": 1.0, "fwd_hblock": 0.0}
+    assert set(defaults) == accepted
+    for k, v in defaults.items():                     # every key takes its default value
+        assert lib.fa_debug_set(k.encode(), v) == 0, k
