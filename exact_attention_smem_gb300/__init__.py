@@ -13,7 +13,8 @@ from ._lib import (FAError, fa_bwd, fa_bwd_noalloc, fa_bwd_varlen, fa_bwd_worksp
                    fa_debug_set, fa_fwd_varlen, fa_fwd_fp8, fa_quantize_fp8,
                    fa_debug_set_events, fa_debug_set_trace,
                    fa_exp2_poly_host, fa_fwd, fa_merge, fa_micro, fa_get_device_error, fa_sched_list, fa_test_exp2,
-                   fa_test_mma, fa_test_mma_fp8, fa_test_mma_pair, fa_test_wait_timeout, load)
+                   fa_test_mma, fa_test_mma_fp8, fa_test_mma_pair, fa_test_roundtrip,
+                   fa_test_wait_timeout, load)
 
 
 def _dims(q, k, cu_seqlens):

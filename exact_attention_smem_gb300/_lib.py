@@ -51,6 +51,7 @@ _SIGS = {
     "fa_merge": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P]),
     "fa_test_mma_pair": (_I, [_P, _P, _P, _P, _I, _I, _P]),
     "fa_test_mma_fp8": (_I, [_P, _P, _P, _I, _I, _P]),
+    "fa_test_roundtrip": (_I, [_P, _P, _P, _P]),
     "fa_quantize_fp8": (_I, [_P, _I, _I, _I, _I, _I, _P, _P, _P]),
     "fa_fwd_fp8": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, ctypes.c_float,
                         _P]),
@@ -212,6 +213,11 @@ def fa_fwd_fp8(q8, k8, vt8, q_scale, k_scale, v_scale, o, lse, B, Hq, Hkv, Sq, S
     _check(load().fa_fwd_fp8(_ptr(q8), _ptr(k8), _ptr(vt8), _ptr(q_scale), _ptr(k_scale),
                              _ptr(v_scale), _ptr(o), _ptr(lse), B, Hq, Hkv, Sq, Sk, d,
                              int(causal), float(scale), _stream(stream)), "fa_fwd_fp8")
+
+
+def fa_test_roundtrip(src, dst, tmem_out, stream=None):
+    _check(load().fa_test_roundtrip(_ptr(src), _ptr(dst), _ptr(tmem_out), _stream(stream)),
+           "fa_test_roundtrip")
 
 
 def fa_test_mma_fp8(A, B, C, mode, N, stream=None):

@@ -27,6 +27,8 @@ cudaError_t launch_mma_pair_probe(const __nv_bfloat16* A, const __nv_bfloat16* B
 cudaError_t launch_micro(int kind, int iters, double* out, int ctas, cudaStream_t st);
 cudaError_t launch_mma_fp8_probe(const uint8_t* A, const uint8_t* B, float* C, int mode, int N,
                                  cudaStream_t st);
+cudaError_t launch_roundtrip_probe(const CUtensorMap& src, const CUtensorMap& dst,
+                                   uint32_t* tmem_out, cudaStream_t st);
 
 __device__ int g_error_word;  // first expired bounded wait (site code), per device
 
@@ -728,6 +730,19 @@ extern "C" int fa_test_mma_fp8(const void* A, const void* B, float* C, int mode,
   cudaError_t e = launch_mma_fp8_probe(static_cast<const uint8_t*>(A),
                                        static_cast<const uint8_t*>(B), C, mode, N,
                                        static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : fail(FA_ERR_CUDA, "%s", cudaGetErrorString(e));
+}
+
+extern "C" int fa_test_roundtrip(const void* src, void* dst, unsigned* tmem_out, void* stream) {
+  if (!src || !dst || !tmem_out || !aligned16(src) || !aligned16(dst))
+    return fail(FA_ERR_INVALID_ARG, "fa_test_roundtrip arguments");
+  DevInfo* di = nullptr;
+  int st = device_info(&di);
+  if (st != FA_OK) return st;
+  CUtensorMap ms, md;
+  if ((st = encode_rows(&ms, src, 128, 1, 64)) != FA_OK) return st;   // one 128 x 64 tile
+  if ((st = encode_rows(&md, dst, 128, 1, 64)) != FA_OK) return st;
+  cudaError_t e = launch_roundtrip_probe(ms, md, tmem_out, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FA_OK : fail(FA_ERR_CUDA, "%s", cudaGetErrorString(e));
 }
 

@@ -234,6 +234,83 @@ cudaError_t launch_mma_fp8_probe(const uint8_t* A, const uint8_t* B, float* C, i
   return cudaGetLastError();
 }
 
+// Round trips through the data paths the kernels use, one CTA of 128 threads:
+//   TMA: a 128-row x 64-column bf16 tile (128-byte swizzle) loaded from src
+//        into shared memory and stored back to dst by TMA;
+//   TMEM: thread r writes the words r * 1000 + c (c < 32) into its lane's
+//        columns [0, 32) and reads them back into tmem_out[r][c].
+struct RoundTrip {
+  CUtensorMap src, dst;
+  uint32_t* tmem_out;
+  int* err;
+};
+
+__global__ void __launch_bounds__(128, 1) roundtrip_probe_kernel(const __grid_constant__ RoundTrip p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (base - raw);
+  const uint32_t tile = base, bar = base + 16384;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + 16384 + 64);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 16384 + 72);
+  const int warp = threadIdx.x >> 5, tid = threadIdx.x;
+  if (tid == 0) {
+    mbar_init(bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(tmem_slot), 32);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const WaitCtl wc{p.err, abort_flag, 1000000000ull};
+  if (tid == 0) {
+    mbar_arrive_expect_tx(bar, 16384);
+    tma_load_3d(tile, &p.src, bar, 0, 0, 0);
+    if (mbar_wait(bar, 0, wc, SITE_TEST)) {
+      tma_store_3d(&p.dst, tile, 0, 0, 0);
+      tma_store_commit();
+      tma_store_wait_all();
+    }
+  }
+  __syncwarp();                       // warp 0 reconverges before the warp-wide TMEM ops
+  const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+  uint32_t v[32];
+#pragma unroll
+  for (int c = 0; c < 32; ++c) v[c] = (uint32_t)tid * 1000u + (uint32_t)c;
+  tmem_st32(tmem + lane_off, v);
+  tmem_st_wait();
+  uint32_t w[32];
+  tmem_ld32(tmem + lane_off, w);
+#pragma unroll
+  for (int c = 0; c < 32; ++c) p.tmem_out[tid * 32 + c] = w[c];
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 32);
+  }
+}
+
+cudaError_t launch_roundtrip_probe(const CUtensorMap& src, const CUtensorMap& dst,
+                                   uint32_t* tmem_out, cudaStream_t st) {
+  RoundTrip p;
+  p.src = src;
+  p.dst = dst;
+  p.tmem_out = tmem_out;
+  p.err = device_error_word();
+  const int smem = 16384 + 128 + 1024;
+  cudaError_t e = cudaFuncSetAttribute(roundtrip_probe_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  roundtrip_probe_kernel<<<1, 128, smem, st>>>(p);
+  return cudaGetLastError();
+}
+
 // CTA-pair (cta_group::2) MMA probe: a cluster of two CTAs computes
 //   mode 0: C[256][N] = A[256][128] * B[N][128]^T   (A, B K-major in shared memory)
 //   mode 1: C[256][N] = A[256][128] * B[128][N]     (A from TMEM, B MN-major)

@@ -308,6 +308,15 @@ FA_API int fa_test_mma(const void* A, const void* B, float* C, int mode, int N, 
 FA_API int fa_test_mma_fp8(const void* A, const void* B, float* C, int mode, int N, void* stream);
 
 /*
+ * Data-path round trips (one CTA): a 128-row x 64-column bf16 tile of src
+ * (device, 16-byte aligned, row-major) is loaded into shared memory by TMA
+ * (128-byte swizzle) and stored to dst by TMA; and each of 128 threads writes
+ * the words r * 1000 + c (c < 32) to its tensor-memory lane and reads them back
+ * into tmem_out[r][c] (device, 128 x 32 unsigned).
+ */
+FA_API int fa_test_roundtrip(const void* src, void* dst, unsigned* tmem_out, void* stream);
+
+/*
  * CTA-pair (cta_group::2) tcgen05 MMA probe: a cluster of two CTAs computes
  * C[256][N] (fp32), N = 128, with M=256 MMAs issued by CTA 0; CTA r
  * holds A rows [128r, 128r+128) and B's N columns [r*N/2, (r+1)*N/2).

@@ -81,6 +81,20 @@ def test_mma_fp8_probe(mode, N):
     assert np.abs(got - want).max() <= 1e-5 * scale
 
 
+def test_tma_and_tmem_round_trips():
+    """A TMA load + TMA store of one swizzled tile returns the tile bit for bit;
+    a tensor-memory store + load returns every lane's words."""
+    src = torch.randn(128, 64, generator=torch.Generator().manual_seed(5)).to(torch.bfloat16).cuda()
+    dst = torch.zeros_like(src)
+    out = torch.zeros(128, 32, dtype=torch.int32, device="cuda")
+    fa.fa_test_roundtrip(src, dst, out)
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_error(clear=True) == 0
+    assert torch.equal(dst.view(torch.int16), src.view(torch.int16))
+    want = torch.arange(128).view(128, 1) * 1000 + torch.arange(32).view(1, 32)
+    assert torch.equal(out.cpu(), want.to(torch.int32))
+
+
 @pytest.mark.parametrize("N", [128])
 @pytest.mark.parametrize("mode", [0, 1])
 def test_mma_pair_probe(mode, N):
