@@ -9,12 +9,10 @@ from __future__ import annotations
 
 import math
 
-from ._lib import (FAError, fa_bwd, fa_bwd_noalloc, fa_bwd_varlen, fa_bwd_workspace_bytes,  # noqa: F401
-                   fa_debug_set, fa_fwd_varlen, fa_fwd_fp8, fa_quantize_fp8,
-                   fa_debug_set_events, fa_debug_set_trace,
-                   fa_exp2_poly_host, fa_fwd, fa_merge, fa_micro, fa_get_device_error, fa_sched_list, fa_test_exp2,
-                   fa_test_mma, fa_test_mma_fp8, fa_test_mma_pair, fa_test_roundtrip,
-                   fa_test_wait_timeout, load)
+from ._lib import (FAError, fa_bwd, fa_bwd_noalloc, fa_bwd_varlen,  # noqa: F401
+                   fa_bwd_workspace_bytes, fa_debug_set, fa_debug_set_events, fa_debug_set_trace,
+                   fa_fwd, fa_fwd_fp8, fa_fwd_varlen, fa_get_device_error, fa_merge,
+                   fa_quantize_fp8, load)
 
 
 def _dims(q, k, cu_seqlens):

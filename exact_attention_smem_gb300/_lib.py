@@ -44,19 +44,10 @@ _SIGS = {
     "fa_debug_set": (_I, [ctypes.c_char_p, ctypes.c_double]),
     "fa_debug_set_events": (_I, [_I, _P, _P]),
     "fa_debug_set_trace": (_I, [_P, ctypes.c_size_t]),
-    "fa_test_exp2": (_I, [_P, _P, _I, _I, _P]),
-    "fa_exp2_poly_host": (_F, [_F]),
-    "fa_micro": (_I, [_I, _I, _P, _I, _P]),
-    "fa_test_mma": (_I, [_P, _P, _P, _I, _I, _P]),
     "fa_merge": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P]),
-    "fa_test_mma_pair": (_I, [_P, _P, _P, _P, _I, _I, _P]),
-    "fa_test_mma_fp8": (_I, [_P, _P, _P, _I, _I, _P]),
-    "fa_test_roundtrip": (_I, [_P, _P, _P, _P]),
     "fa_quantize_fp8": (_I, [_P, _I, _I, _I, _I, _I, _P, _P, _P]),
     "fa_fwd_fp8": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, ctypes.c_float,
                         _P]),
-    "fa_test_wait_timeout": (_I, [_P, ctypes.c_double, _P]),
-    "fa_sched_list": (_I, [_I, _I, _P, _I, _I, _I, _I, _I, _I, _I, _P, _I]),
 }
 
 
@@ -177,30 +168,9 @@ def fa_debug_set_trace(buf=None):
            "fa_debug_set_trace")
 
 
-def fa_test_exp2(x, y, mode, stream=None):
-    _check(load().fa_test_exp2(_ptr(x), _ptr(y), x.numel(), mode, _stream(stream)), "fa_test_exp2")
-
-
-def fa_micro(kind, iters, out_dev, ctas, stream=None):
-    _check(load().fa_micro(kind, iters, _ptr(out_dev), ctas, _stream(stream)), "fa_micro")
-
-
-def fa_exp2_poly_host(x: float) -> float:
-    return float(load().fa_exp2_poly_host(x))
-
-
-def fa_test_mma(A, B, C, mode, N, stream=None):
-    _check(load().fa_test_mma(_ptr(A), _ptr(B), _ptr(C), mode, N, _stream(stream)), "fa_test_mma")
-
-
 def fa_merge(o_parts, lse_parts, P, B, Hq, S, d, packed, o, lse, stream=None):
     _check(load().fa_merge(_ptr(o_parts), _ptr(lse_parts), P, B, Hq, S, d, int(packed), _ptr(o),
                            _ptr(lse), _stream(stream)), "fa_merge")
-
-
-def fa_test_mma_pair(A, B, C, flags, mode, N, stream=None):
-    _check(load().fa_test_mma_pair(_ptr(A), _ptr(B), _ptr(C), _ptr(flags), mode, N,
-                                   _stream(stream)), "fa_test_mma_pair")
 
 
 def fa_quantize_fp8(x, B, S, H, d, layout, codes, scales, stream=None):
@@ -213,35 +183,3 @@ def fa_fwd_fp8(q8, k8, vt8, q_scale, k_scale, v_scale, o, lse, B, Hq, Hkv, Sq, S
     _check(load().fa_fwd_fp8(_ptr(q8), _ptr(k8), _ptr(vt8), _ptr(q_scale), _ptr(k_scale),
                              _ptr(v_scale), _ptr(o), _ptr(lse), B, Hq, Hkv, Sq, Sk, d,
                              int(causal), float(scale), _stream(stream)), "fa_fwd_fp8")
-
-
-def fa_test_roundtrip(src, dst, tmem_out, stream=None):
-    _check(load().fa_test_roundtrip(_ptr(src), _ptr(dst), _ptr(tmem_out), _stream(stream)),
-           "fa_test_roundtrip")
-
-
-def fa_test_mma_fp8(A, B, C, mode, N, stream=None):
-    _check(load().fa_test_mma_fp8(_ptr(A), _ptr(B), _ptr(C), mode, N, _stream(stream)),
-           "fa_test_mma_fp8")
-
-
-def fa_test_wait_timeout(status_dev, timeout_ms, stream=None):
-    _check(load().fa_test_wait_timeout(_ptr(status_dev), float(timeout_ms), _stream(stream)),
-           "fa_test_wait_timeout")
-
-
-def fa_sched_list(kind, B, cu_seqlens_host, Sq, Sk, heads, causal, grid, cta, heads_per_group=0):
-    """Return the (seq, row block, head, cost) units of one CTA, in order."""
-    lib = load()
-    cu = None
-    if cu_seqlens_host is not None:
-        arr = (ctypes.c_int * len(cu_seqlens_host))(*[int(x) for x in cu_seqlens_host])
-        cu = ctypes.cast(arr, ctypes.c_void_p)
-    n = lib.fa_sched_list(kind, B, cu, Sq, Sk, heads, int(causal), grid, cta, heads_per_group,
-                          None, 0)
-    if n < 0:
-        raise ValueError("fa_sched_list: bad arguments")
-    out = (ctypes.c_int * (4 * max(n, 1)))()
-    lib.fa_sched_list(kind, B, cu, Sq, Sk, heads, int(causal), grid, cta, heads_per_group,
-                      ctypes.cast(out, ctypes.c_void_p), n)
-    return [tuple(out[4 * i:4 * i + 4]) for i in range(n)]

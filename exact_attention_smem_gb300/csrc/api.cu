@@ -1,7 +1,7 @@
-// C ABI (include/fa.h): argument validation, TMA descriptor encoding, device
-// property caching and kernel launches. Nothing here allocates device memory.
+// C ABI (include/fa.h): argument validation, launch configuration and kernel
+// launches (device properties and TMA encoding: host_common.cu). Nothing here allocates device memory.
 #include "../../include/fa.h"
-#include "exp2_poly.cuh"
+#include "host_common.h"
 #include "internal.h"
 #include "sched.cuh"
 
@@ -16,114 +16,10 @@
 #include <string>
 
 namespace fa {
-
-cudaError_t launch_exp2_probe(const float* x, float* y, int n, int mode, cudaStream_t st);
-cudaError_t launch_mma_probe(const __nv_bfloat16* A, const __nv_bfloat16* B, float* C, int mode,
-                             int N, cudaStream_t st);
-cudaError_t launch_wait_timeout_probe(int* status, unsigned long long timeout_ns,
-                                      cudaStream_t st);
-cudaError_t launch_mma_pair_probe(const __nv_bfloat16* A, const __nv_bfloat16* B, float* C,
-                                  int* flags, int mode, int N, cudaStream_t st);
-cudaError_t launch_micro(int kind, int iters, double* out, int ctas, cudaStream_t st);
-cudaError_t launch_mma_fp8_probe(const uint8_t* A, const uint8_t* B, float* C, int mode, int N,
-                                 cudaStream_t st);
-cudaError_t launch_roundtrip_probe(const CUtensorMap& src, const CUtensorMap& dst,
-                                   uint32_t* tmem_out, cudaStream_t st);
-
-__device__ int g_error_word;  // first expired bounded wait (site code), per device
-
 namespace {
-
-thread_local std::string t_last_error;
-
-int fail(int status, const char* fmt, ...) {
-  char buf[512];
-  va_list ap;
-  va_start(ap, fmt);
-  vsnprintf(buf, sizeof(buf), fmt, ap);
-  va_end(ap);
-  t_last_error = buf;
-  return status;
-}
 
 std::mutex g_mu;
 Knobs g_knobs;
-
-struct DevInfo {
-  bool init = false;
-  int sms = 0, major = 0, minor = 0;
-  int* err_word = nullptr;
-};
-DevInfo g_dev[64];
-
-PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-
-int device_info(DevInfo** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return fail(FA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
-  if (dev < 0 || dev >= 64) return fail(FA_ERR_CUDA, "device index %d out of range", dev);
-  std::lock_guard<std::mutex> lk(g_mu);
-  DevInfo& di = g_dev[dev];
-  if (!di.init) {
-    cudaDeviceProp prop;
-    e = cudaGetDeviceProperties(&prop, dev);
-    if (e != cudaSuccess)
-      return fail(FA_ERR_CUDA, "cudaGetDeviceProperties: %s", cudaGetErrorString(e));
-    di.sms = prop.multiProcessorCount;
-    di.major = prop.major;
-    di.minor = prop.minor;
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_error_word);
-    if (e != cudaSuccess)
-      return fail(FA_ERR_CUDA, "cudaGetSymbolAddress: %s", cudaGetErrorString(e));
-    di.err_word = static_cast<int*>(p);
-    if (!g_encode) {
-      cudaDriverEntryPointQueryResult q;
-      void* fn = nullptr;
-      e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
-                                           &q);
-      if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
-        return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
-      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    }
-    di.init = true;
-  }
-  if (di.major != 10 || di.minor != 3)
-    return fail(FA_ERR_ARCH, "device compute capability %d.%d; this library is built for 10.3 "
-                "(sm_103a)", di.major, di.minor);
-  *out = &di;
-  return FA_OK;
-}
-
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
-// [rows, heads, d] bf16 view, boxes of 64 columns x 1 head x box_rows rows, 128B swizzle.
-int encode_rows(CUtensorMap* tm, const void* ptr, long long rows, int heads, int d,
-                int box_rows = 128) {
-  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)rows};
-  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)heads * d * 2};
-  cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
-  cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = g_encode(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims,
-                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
-  return FA_OK;
-}
-
-// e4m3 codes: a 3-D view (innermost first) with 128-byte rows of 128 codes.
-int encode_u8(CUtensorMap* tm, const void* ptr, const cuuint64_t (&dims)[3],
-              const cuuint64_t (&strides)[2], const cuuint32_t (&box)[3]) {
-  cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = g_encode(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr), dims,
-                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
-  return FA_OK;
-}
 
 struct Shape {
   long long Tq, Tk;  // rows of the flattened q / k tensors
@@ -167,16 +63,6 @@ int validate_common(const void* const* ptrs, int nptrs, int B, int Hq, int Hkv, 
 
 }  // namespace
 
-int report_error(int status, const char* fmt, ...) {
-  char buf[512];
-  va_list ap;
-  va_start(ap, fmt);
-  vsnprintf(buf, sizeof(buf), fmt, ap);
-  va_end(ap);
-  t_last_error = buf;
-  return status;
-}
-
 Knobs knobs_snapshot() {
   std::lock_guard<std::mutex> lk(g_mu);
   return g_knobs;
@@ -189,16 +75,6 @@ void take_events(int which, cudaEvent_t* start, cudaEvent_t* stop) {
   g_knobs.ev[which][0] = g_knobs.ev[which][1] = nullptr;
 }
 
-int num_sms() {
-  DevInfo* di = nullptr;
-  return device_info(&di) == FA_OK ? di->sms : 0;
-}
-
-int* device_error_word() {
-  DevInfo* di = nullptr;
-  return device_info(&di) == FA_OK ? di->err_word : nullptr;
-}
-
 }  // namespace fa
 
 using namespace fa;
@@ -207,7 +83,7 @@ namespace {
 int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
              int Hkv, int Sq, int Sk, int d, int causal, float scale, const int* cu_seqlens,
              const int* cu_seqlens_k, void* stream) {
-  t_last_error.clear();
+  clear_last_error();
   const void* ptrs[5] = {q, k, v, o, lse};
   Shape sh;
   int st = validate_common(ptrs, 5, B, Hq, Hkv, Sq, Sk, d, scale, cu_seqlens, &sh, cu_seqlens_k);
@@ -283,8 +159,7 @@ extern "C" int fa_fwd_varlen(const void* q, const void* k, const void* v, void* 
                              float scale, const int* cu_seqlens_q, const int* cu_seqlens_k,
                              void* stream) {
   if (!cu_seqlens_q || !cu_seqlens_k) {
-    t_last_error = "fa_fwd_varlen needs both boundary lists";
-    return FA_ERR_INVALID_ARG;
+    return fail(FA_ERR_INVALID_ARG, "fa_fwd_varlen needs both boundary lists");
   }
   return fwd_impl(q, k, v, o, lse, nseq, Hq, Hkv, Tq, Tk, d, causal, scale, cu_seqlens_q,
                   cu_seqlens_k, stream);
@@ -292,7 +167,7 @@ extern "C" int fa_fwd_varlen(const void* q, const void* k, const void* v, void* 
 
 extern "C" int fa_quantize_fp8(const void* x, int B, int S, int H, int d, int layout, void* codes,
                                float* scales, void* stream) {
-  t_last_error.clear();
+  clear_last_error();
   if (!x || !codes || !scales) return fail(FA_ERR_INVALID_ARG, "NULL pointer");
   if (!aligned16(x) || !aligned16(codes))
     return fail(FA_ERR_INVALID_ARG, "x and codes must be 16-byte aligned");
@@ -315,7 +190,7 @@ extern "C" int fa_fwd_fp8(const void* q8, const void* k8, const void* vt8, const
                           const float* k_scale, const float* v_scale, void* o, float* lse, int B,
                           int Hq, int Hkv, int Sq, int Sk, int d, int causal, float scale,
                           void* stream) {
-  t_last_error.clear();
+  clear_last_error();
   const void* ptrs[8] = {q8, k8, vt8, q_scale, k_scale, v_scale, o, lse};
   for (int i = 0; i < 8; ++i)
     if (!ptrs[i]) return fail(FA_ERR_INVALID_ARG, "tensor pointer %d is NULL", i);
@@ -408,7 +283,7 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const f
              const void* dout, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Sq,
              int Sk, int d, int causal, float scale, const int* cu_seqlens,
              const int* cu_seqlens_k, void* workspace, size_t workspace_bytes, void* stream) {
-  t_last_error.clear();
+  clear_last_error();
   const void* ptrs[9] = {q, k, v, o, lse, dout, dq, dk, dv};
   Shape sh;
   int st = validate_common(ptrs, 9, B, Hq, Hkv, Sq, Sk, d, scale, cu_seqlens, &sh, cu_seqlens_k);
@@ -560,8 +435,7 @@ extern "C" int fa_bwd_varlen(const void* q, const void* k, const void* v, const 
                              float scale, const int* cu_seqlens_q, const int* cu_seqlens_k,
                              void* workspace, size_t workspace_bytes, void* stream) {
   if (!cu_seqlens_q || !cu_seqlens_k) {
-    t_last_error = "fa_bwd_varlen needs both boundary lists";
-    return FA_ERR_INVALID_ARG;
+    return fail(FA_ERR_INVALID_ARG, "fa_bwd_varlen needs both boundary lists");
   }
   return bwd_impl(q, k, v, o, lse, dout, dq, dk, dv, nseq, Hq, Hkv, Tq, Tk, d, causal, scale,
                   cu_seqlens_q, cu_seqlens_k, workspace, workspace_bytes, stream);
@@ -569,7 +443,7 @@ extern "C" int fa_bwd_varlen(const void* q, const void* k, const void* v, const 
 
 extern "C" int fa_merge(const void* o_parts, const float* lse_parts, int P, int B, int Hq, int S,
                         int d, int packed, void* o, float* lse, void* stream) {
-  t_last_error.clear();
+  clear_last_error();
   const void* ptrs[4] = {o_parts, lse_parts, o, lse};
   for (int i = 0; i < 4; ++i)
     if (!ptrs[i]) return fail(FA_ERR_INVALID_ARG, "pointer %d is NULL", i);
@@ -605,21 +479,10 @@ extern "C" const char* fa_status_string(int status) {
   }
 }
 
-extern "C" const char* fa_last_error(void) { return t_last_error.c_str(); }
+extern "C" const char* fa_last_error(void) { return last_error(); }
 
 extern "C" int fa_get_device_error(int* code, int clear) {
-  if (!code) return fail(FA_ERR_INVALID_ARG, "code is NULL");
-  DevInfo* di = nullptr;
-  int st = device_info(&di);
-  if (st != FA_OK) return st;
-  cudaError_t e = cudaDeviceSynchronize();
-  if (e == cudaSuccess) e = cudaMemcpyFromSymbol(code, g_error_word, sizeof(int));
-  if (e == cudaSuccess && clear) {
-    int zero = 0;
-    e = cudaMemcpyToSymbol(g_error_word, &zero, sizeof(int));
-  }
-  if (e != cudaSuccess) return fail(FA_ERR_CUDA, "error word read: %s", cudaGetErrorString(e));
-  return FA_OK;
+  return read_device_error(code, clear);
 }
 
 extern "C" int fa_debug_set(const char* key, double value) {
@@ -669,127 +532,4 @@ extern "C" int fa_debug_set_trace(void* trace_dev, size_t bytes) {
   std::lock_guard<std::mutex> lk(g_mu);
   g_knobs.trace = static_cast<long long*>(trace_dev);
   return FA_OK;
-}
-
-extern "C" int fa_test_exp2(const float* x, float* y, int n, int mode, void* stream) {
-  if (!x || !y || n < 0 || (mode != 0 && mode != 1))
-    return fail(FA_ERR_INVALID_ARG, "fa_test_exp2 arguments");
-  DevInfo* di = nullptr;
-  int st = device_info(&di);
-  if (st != FA_OK) return st;
-  cudaError_t e = launch_exp2_probe(x, y, n, mode, static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? FA_OK : fail(FA_ERR_CUDA, "%s", cudaGetErrorString(e));
-}
-
-extern "C" float fa_exp2_poly_host(float x) { return fa::exp2_poly(x); }
-
-extern "C" int fa_micro(int kind, int iters, double* out_dev, int ctas, void* stream) {
-  if (kind < 0 || kind > 51 || iters <= 0 || iters > (1 << 24) || !out_dev || ctas <= 0 ||
-      ctas > 4096)
-    return fail(FA_ERR_INVALID_ARG, "fa_micro arguments");
-  DevInfo* di = nullptr;
-  int st = device_info(&di);
-  if (st != FA_OK) return st;
-  cudaError_t e = launch_micro(kind, iters, out_dev, ctas, static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? FA_OK : fail(FA_ERR_CUDA, "%s", cudaGetErrorString(e));
-}
-
-extern "C" int fa_test_mma(const void* A, const void* B, float* C, int mode, int N,
-                           void* stream) {
-  if (!A || !B || !C || mode < 0 || mode > 2 || (N != 64 && N != 128))
-    return fail(FA_ERR_INVALID_ARG, "fa_test_mma arguments");
-  DevInfo* di = nullptr;
-  int st = device_info(&di);
-  if (st != FA_OK) return st;
-  cudaError_t e = launch_mma_probe(static_cast<const __nv_bfloat16*>(A),
-                                   static_cast<const __nv_bfloat16*>(B), C, mode, N,
-                                   static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? FA_OK : fail(FA_ERR_CUDA, "%s", cudaGetErrorString(e));
-}
-
-extern "C" int fa_test_mma_pair(const void* A, const void* B, float* C, int* flags, int mode,
-                                int N, void* stream) {
-  if (!A || !B || !C || !flags || (mode != 0 && mode != 1) || N != 128)
-    return fail(FA_ERR_INVALID_ARG, "fa_test_mma_pair arguments");
-  DevInfo* di = nullptr;
-  int st = device_info(&di);
-  if (st != FA_OK) return st;
-  cudaError_t e = launch_mma_pair_probe(static_cast<const __nv_bfloat16*>(A),
-                                        static_cast<const __nv_bfloat16*>(B), C, flags, mode, N,
-                                        static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? FA_OK : fail(FA_ERR_CUDA, "%s", cudaGetErrorString(e));
-}
-
-extern "C" int fa_test_mma_fp8(const void* A, const void* B, float* C, int mode, int N,
-                               void* stream) {
-  if (!A || !B || !C || (mode != 0 && mode != 1) || (N != 64 && N != 128))
-    return fail(FA_ERR_INVALID_ARG, "fa_test_mma_fp8 arguments");
-  DevInfo* di = nullptr;
-  int st = device_info(&di);
-  if (st != FA_OK) return st;
-  cudaError_t e = launch_mma_fp8_probe(static_cast<const uint8_t*>(A),
-                                       static_cast<const uint8_t*>(B), C, mode, N,
-                                       static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? FA_OK : fail(FA_ERR_CUDA, "%s", cudaGetErrorString(e));
-}
-
-extern "C" int fa_test_roundtrip(const void* src, void* dst, unsigned* tmem_out, void* stream) {
-  if (!src || !dst || !tmem_out || !aligned16(src) || !aligned16(dst))
-    return fail(FA_ERR_INVALID_ARG, "fa_test_roundtrip arguments");
-  DevInfo* di = nullptr;
-  int st = device_info(&di);
-  if (st != FA_OK) return st;
-  CUtensorMap ms, md;
-  if ((st = encode_rows(&ms, src, 128, 1, 64)) != FA_OK) return st;   // one 128 x 64 tile
-  if ((st = encode_rows(&md, dst, 128, 1, 64)) != FA_OK) return st;
-  cudaError_t e = launch_roundtrip_probe(ms, md, tmem_out, static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? FA_OK : fail(FA_ERR_CUDA, "%s", cudaGetErrorString(e));
-}
-
-extern "C" int fa_test_wait_timeout(int* status_dev, double timeout_ms, void* stream) {
-  if (!status_dev || !(timeout_ms > 0 && timeout_ms <= 10000))
-    return fail(FA_ERR_INVALID_ARG, "fa_test_wait_timeout arguments");
-  DevInfo* di = nullptr;
-  int st = device_info(&di);
-  if (st != FA_OK) return st;
-  cudaError_t e = launch_wait_timeout_probe(status_dev, (unsigned long long)(timeout_ms * 1e6),
-                                            static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? FA_OK : fail(FA_ERR_CUDA, "%s", cudaGetErrorString(e));
-}
-
-extern "C" int fa_sched_list(int kind, int B, const int* cu_seqlens_host, int Sq, int Sk,
-                             int heads, int causal, int grid, int cta, int heads_per_group,
-                             int* out, int max_units) {
-  if (kind < 0 || kind > 4 || B < 0 || Sq < 0 || Sk < 0 || heads <= 0 || grid <= 0 ||
-      cta < 0 || cta >= grid || heads_per_group < 0 || max_units < 0 || (max_units > 0 && !out))
-    return -1;
-  // kind: 0 forward, 1 one-pass backward, 2 dK/dV pass, 3 dQ pass, 4 dK/dV pass on CTA pairs
-  static const int kUnit[5] = {256, 128, 128, 128, 256}, kInner[5] = {128, 64, 128, 128, 128},
-                   kList[5] = {0, 1, 1, 0, 1};
-  SchedSpec s{cu_seqlens_host, B, Sq, Sk, heads, causal ? 1 : 0, kUnit[kind], kInner[kind],
-              kList[kind], heads_per_group};
-  if (heads_per_group == 0) {
-    long long per_head = 0;
-    for (int i = 0; i < B; ++i) {
-      int qs, ql, ks, kl;
-      s.seq(i, qs, ql, ks, kl);
-      per_head += s.nblocks(ql, kl);
-    }
-    s.hblock = pick_hblock(per_head, heads, grid);
-  }
-  Walker w;
-  w.init(s);
-  int count = 0;
-  for (int k = 0;; ++k) {
-    Unit u;
-    if (!w.seek(snake_index(k, grid, cta), u)) break;
-    if (count < max_units) {
-      out[4 * count + 0] = u.seq;
-      out[4 * count + 1] = u.m;
-      out[4 * count + 2] = u.head;
-      out[4 * count + 3] = u.cost;
-    }
-    ++count;
-  }
-  return count;
 }

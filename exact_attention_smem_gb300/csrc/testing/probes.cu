@@ -1,14 +1,14 @@
-// Test hooks exported through the C ABI for the GPU tests (not used by the
-// attention path):
+// Device probes of the test library (libfa_gb300_testing.so, declared in
+// include/fa_testing.h; not linked into the attention library):
 //   * the device exponentials (software polynomial and MUFU ex2) over an array;
 //   * a one-tile tcgen05 MMA probe that checks the shared-memory/instruction
 //     descriptors, the TMEM load/store layout and the TMEM-A operand form
 //     against a plain product computed by the test;
 //   * a bounded-wait probe whose wait can never complete, which must end with
 //     the timeout status instead of hanging.
-#include "exp2_poly.cuh"
-#include "internal.h"
-#include "ptx.cuh"
+#include "../exp2_poly.cuh"
+#include "../internal.h"
+#include "../ptx.cuh"
 
 namespace fa {
 using namespace ptx;

@@ -56,12 +56,17 @@ def _visible(nq: int, nk: int, causal: bool, row0: int = 0, rows: int | None = N
     return j <= i + (nk - nq)
 
 
-def attend_head(q, k, v, scale: float, causal: bool, row_chunk: int = 1024):
-    """Forward for one (sequence, query head): q [Sq, d], k/v [Sk, d] -> (o [Sq, d], lse [Sq])."""
+def attend_head(q, k, v, scale: float, causal: bool, row_chunk: int = 1024,
+                return_max: bool = False):
+    """Forward for one (sequence, query head): q [Sq, d], k/v [Sk, d] -> (o [Sq, d], lse [Sq]).
+
+    With ``return_max`` also the row maxima m [Sq] of the scaled, masked scores
+    (the m_i of the definition above; -inf for a row with no visible key)."""
     q, k, v = _as64(q), _as64(k), _as64(v)
     nq, nk = q.shape[0], k.shape[0]
     o = np.zeros((nq, v.shape[1]))
     lse = np.full(nq, np.inf)
+    mx = np.full(nq, -np.inf)
     for r0 in range(0, nq, row_chunk):
         r1 = min(nq, r0 + row_chunk)
         s = scale * (q[r0:r1] @ k.T)
@@ -74,7 +79,8 @@ def attend_head(q, k, v, scale: float, causal: bool, row_chunk: int = 1024):
         l = p.sum(axis=1)
         o[r0:r1] = np.where(has[:, None], (p @ v) / np.where(has, l, 1.0)[:, None], 0.0)
         lse[r0:r1] = np.where(has, m_safe + np.log(np.where(has, l, 1.0)), np.inf)
-    return o, lse
+        mx[r0:r1] = m
+    return (o, lse, mx) if return_max else (o, lse)
 
 
 def attend_head_backward(q, k, v, do, scale: float, causal: bool, row_chunk: int = 1024):

@@ -135,11 +135,13 @@ def dequantize_v_transposed(codes, scales, S: int):
 
 
 def forward_fp8(q_codes, q_scales, k_codes, k_scales, vt_codes, v_scales, scale: float,
-                causal: bool, heads=None, seqs=None):
+                causal: bool, heads=None, seqs=None, return_max: bool = False):
     """The FP8 forward's definition: exact fp64 attention over the dequantized
     inputs. Returns (o, lse) like ``attention_fp64.forward`` (dense layout;
-    entries of heads or sequences outside the subset are NaN). Dequantizes one
-    (sequence, head) at a time, so a subset of a large problem stays small."""
+    entries of heads or sequences outside the subset are NaN), and with
+    ``return_max`` also the row maxima of the scaled scores [B, Hq, Sq].
+    Dequantizes one (sequence, head) at a time, so a subset of a large problem
+    stays small."""
     qc, kc, vc = np.asarray(q_codes), np.asarray(k_codes), np.asarray(vt_codes)
     qs, ks, vs = (np.asarray(x, dtype=np.float64) for x in (q_scales, k_scales, v_scales))
     B, Sq, Hq, d = qc.shape
@@ -147,6 +149,7 @@ def forward_fp8(q_codes, q_scales, k_codes, k_scales, vt_codes, v_scales, scale:
     group = Hq // Hkv
     o = np.full((B, Sq, Hq, d), np.nan)
     lse = np.full((B, Hq, Sq), np.nan)
+    mx = np.full((B, Hq, Sq), np.nan)
     for b in range(B):
         if seqs is not None and b not in seqs:
             continue
@@ -155,5 +158,6 @@ def forward_fp8(q_codes, q_scales, k_codes, k_scales, vt_codes, v_scales, scale:
             qh = e4m3_decode(qc[b, :, h]) * np.repeat(qs[b, h], BLOCK)[:Sq, None]
             kh = e4m3_decode(kc[b, :, g]) * np.repeat(ks[b, g], BLOCK)[:Sk, None]
             vh = e4m3_decode(vc[b, g, :, :Sk]).T * vs[b, g]
-            o[b, :, h], lse[b, h] = _attend_head(qh, kh, vh, scale, causal)
-    return o, lse
+            o[b, :, h], lse[b, h], mx[b, h] = _attend_head(qh, kh, vh, scale, causal,
+                                                           return_max=True)
+    return (o, lse, mx) if return_max else (o, lse)

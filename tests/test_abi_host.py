@@ -16,9 +16,17 @@ def lib():
     return _lib.load()
 
 
-def _declared():
-    src = open(os.path.join(ROOT, "include", "fa.h")).read()
-    return re.findall(r"FA_API[^;]*?\b(fa_\w+)\s*\(", src)
+def _declared(header="fa.h", macro="FA_API"):
+    src = open(os.path.join(ROOT, "include", header)).read()
+    return re.findall(macro + r"[^;]*?\b(fa_\w+)\s*\(", src)
+
+
+def _dynamic_symbols(path):
+    """Names in the library's dynamic symbol table that start with fa_."""
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True,
+                         check=True).stdout
+    return {line.split()[-1] for line in out.splitlines() if line.split()[-1].startswith("fa_")}
 
 
 def test_exports_every_declared_symbol(lib):
@@ -28,6 +36,20 @@ def test_exports_every_declared_symbol(lib):
         assert hasattr(lib, n), n
     from exact_attention_smem_gb300 import _lib
     assert set(_lib.exported_symbols()) == set(names)
+    # the attention library exports exactly the contract: no test hooks
+    assert _dynamic_symbols(_lib.LIB_PATH) == set(names)
+
+
+def test_test_library_exports_its_header(lib):
+    import fa_testing_lib as ft
+    tlib = ft.load()
+    names = _declared("fa_testing.h", "FA_TEST_API")
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(tlib, n), n
+    assert set(ft.SIGS) == set(names)
+    assert _dynamic_symbols(ft.TEST_LIB_PATH) == set(names)
+    assert not set(names) & set(_declared())
 
 
 def test_status_strings(lib):

@@ -6,7 +6,7 @@ import numpy as np
 import pytest
 
 import oracle
-from exact_attention_smem_gb300 import fa_exp2_poly_host
+from fa_testing_lib import fa_exp2_poly_host
 
 
 def test_every_negative_bf16_input():

@@ -14,6 +14,18 @@
     5e-2 leaves headroom for bf16 output rounding. A structural error (a
     wrong block scale, a dropped key block, a transposed operand) is off by
     tens of percent or more;
+  - O element by element (so that one badly wrong row cannot hide under the
+    per-head norm): a weight in e4m3's normal range is off by at most 2^-4 of
+    itself; the kernel stores 2^7 times the weight, so one below the normal
+    range is off by at most half the smallest subnormal step, 2^-10, i.e.
+    2^-17 of the row's largest weight; the row sum is taken over the unrounded
+    weights. Hence
+        |O - O*|_ic <= (2^-4 + 2^-8) sum_j P_ij |V_jc|
+                       + 2^-17 max_j P_ij sum_{j visible} |V_jc| + ulp_bf16 / 2,
+    with P the exact softmax weights; 2^-8 covers the fp32 accumulation of
+    the scores and of P V. Both sums come from the oracle (attention over |V|,
+    and with Q = 0 the mean of the visible |V| rows), max_j P_ij from its row
+    maxima, exp(m_i - LSE_i);
   - Q = 0 makes every weight exactly 1 (2^7 in the kernel, exact in e4m3), so
     O is the plain mean of the visible V rows: checked to 4e-3 max-abs (bf16
     output rounding).
@@ -69,6 +81,38 @@ def test_quantize_v_bit_exact(S, d):
     assert np.array_equal(scales.cpu().numpy(), rs)
 
 
+def _bf16_half_ulp(x):
+    a = np.maximum(np.abs(x), 2.0 ** -126)
+    return np.exp2(np.floor(np.log2(a)) - 8)
+
+
+def _check_elementwise(o, codes, scale, causal, heads=None, seqs=None):
+    """Element-wise bound on the FP8 forward's O (module docstring); o is the
+    kernel's O as float [B, Sq, Hq, d], codes = (q8, qs, k8, ks, v8, vs) as
+    numpy arrays. Returns the largest error / bound ratio (must be <= 1)."""
+    q8, qs, k8, ks, v8, vs = codes
+    ro, rl, rm = f8.forward_fp8(q8, qs, k8, ks, v8, vs, scale, causal, heads=heads, seqs=seqs,
+                                return_max=True)
+    v_abs = v8 & np.uint8(0x7F)                       # e4m3 sign bit cleared: |V|
+    a, _ = f8.forward_fp8(q8, qs, k8, ks, v_abs, vs, scale, causal, heads=heads, seqs=seqs)
+    mean_abs, _ = f8.forward_fp8(np.zeros_like(q8), qs, k8, ks, v_abs, vs, scale, causal,
+                                 heads=heads, seqs=seqs)
+    B, Sq, Hq, d = ro.shape
+    Sk = k8.shape[1]
+    i = np.arange(Sq)
+    n_vis = np.clip(i + 1 + Sk - Sq, 0, Sk) if causal else np.full(Sq, Sk)
+    sum_abs = mean_abs * n_vis[None, :, None, None]
+    with np.errstate(invalid="ignore"):
+        p_max = np.where(np.isfinite(rl), np.exp(rm - rl), 0.0)       # [B, Hq, Sq]
+    p_max = p_max.transpose(0, 2, 1)[..., None]
+    bound = ((2.0 ** -4 + 2.0 ** -8) * a + 2.0 ** -17 * p_max * sum_abs +
+             _bf16_half_ulp(np.maximum(np.abs(o), np.abs(ro))) + 1e-6)
+    sel = ~np.isnan(ro)
+    ratio = np.abs(o - ro)[sel] / bound[sel]
+    assert np.all(np.isfinite(o[sel]))
+    return float(ratio.max()) if ratio.size else 0.0
+
+
 def _fp8_case(B, Hq, Hkv, Sq, Sk, causal, seed, zero_q=False):
     x = random_inputs(B=B, Hq=Hq, Hkv=Hkv, Sq=Sq, Sk=Sk, d=128, seed=seed, device="cuda")
     q = torch.zeros_like(x.q) if zero_q else x.q
@@ -78,9 +122,11 @@ def _fp8_case(B, Hq, Hkv, Sq, Sk, causal, seed, zero_q=False):
     scale = 128 ** -0.5
     o, lse = fa.forward_fp8(q8, qs, k8, ks, v8, vs, causal=causal, scale=scale)
     torch.cuda.synchronize()
-    ro, rl = f8.forward_fp8(q8.cpu().numpy(), qs.cpu().numpy(), k8.cpu().numpy(),
-                            ks.cpu().numpy(), v8.cpu().numpy(), vs.cpu().numpy(), scale, causal)
-    return o.float().cpu().numpy(), lse.cpu(), ro, rl
+    codes = tuple(t.cpu().numpy() for t in (q8, qs, k8, ks, v8, vs))
+    ro, rl = f8.forward_fp8(*codes, scale, causal)
+    o = o.float().cpu().numpy()
+    assert _check_elementwise(o, codes, scale, causal) <= 1.0
+    return o, lse.cpu(), ro, rl
 
 
 def _rel_l2_per_head(o, ro):
@@ -162,17 +208,20 @@ def test_fp8_full_size_parity(name):
         heads, seqs = list(range(w.Hq // w.Hkv)), [0, w.B - 1]
     else:
         heads, seqs = [0, w.Hq - 1], None
-    ro, rl = f8.forward_fp8(q8.cpu().numpy(), qs.cpu().numpy(), k8.cpu().numpy(),
-                            ks.cpu().numpy(), v8.cpu().numpy(), vs.cpu().numpy(), w.scale, True,
-                            heads=heads, seqs=seqs)
+    codes = tuple(t.cpu().numpy() for t in (q8, qs, k8, ks, v8, vs))
+    ro, rl = f8.forward_fp8(*codes, w.scale, True, heads=heads, seqs=seqs)
     bsel = list(range(w.B)) if seqs is None else seqs
     lse_c = lse.cpu()
     e_lse = max_abs(lse_c[bsel][:, heads], rl[bsel][:, heads])
-    o_c = o[bsel][:, :, heads].float().cpu().numpy()
+    o_all = o.float().cpu().numpy()
+    o_c = o_all[bsel][:, :, heads]
     e_o = _rel_l2_per_head(o_c, ro[bsel][:, :, heads])
-    print(f"\nfp8 {name}: LSE max-abs {e_lse:.2e}, O rel-L2 (worst head) {e_o:.2e}")
+    ratio = _check_elementwise(o_all, codes, w.scale, True, heads=heads, seqs=seqs)
+    print(f"\nfp8 {name}: LSE max-abs {e_lse:.2e}, O rel-L2 (worst head) {e_o:.2e}, "
+          f"element-wise error / bound {ratio:.3f}")
     assert e_lse <= LSE_TOL
     assert e_o <= O_REL_L2_FP8
+    assert ratio <= 1.0
 
 
 @pytest.mark.parametrize("tau", [0.0, 1.0])

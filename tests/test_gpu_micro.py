@@ -10,6 +10,7 @@ import pytest
 import torch
 
 import exact_attention_smem_gb300 as fa
+import fa_testing_lib as ft
 
 pytestmark = pytest.mark.gpu
 
@@ -17,7 +18,7 @@ pytestmark = pytest.mark.gpu
 def _rate(kind, iters):
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     out = torch.zeros(2 * sms, dtype=torch.float64, device="cuda")
-    fa.fa_micro(kind, iters, out, sms)
+    ft.fa_micro(kind, iters, out, sms)
     torch.cuda.synchronize()
     v = out.view(sms, 2).cpu()
     rates = v[:, 1] / v[:, 0]
@@ -27,7 +28,7 @@ def _rate(kind, iters):
 def test_microbenchmarks():
     fa.load()
     torch.cuda.set_device(0)
-    fa.fa_get_device_error(clear=True)
+    ft.fa_test_get_device_error(clear=True)
     mufu, sms = _rate(0, 20000)
     poly, _ = _rate(1, 20000)
     mma, _ = _rate(2, 2000)
@@ -48,7 +49,7 @@ def test_microbenchmarks():
             for busy in (0, 1):
                 r, _ = _rate(40 + op * 4 + same * 2 + busy, 2000)
                 lat[f"{oname}_{'same' if same else 'other'}_sub_{'mma' if busy else 'idle'}"] = 1.0 / r
-    assert fa.fa_get_device_error(clear=True) == 0
+    assert ft.fa_test_get_device_error(clear=True) == 0
     res = {"probe_latency_clk": lat, "issue_ss_n128_by_extras": issue,"sms": sms, "mufu_ex2_per_clk_per_sm": mufu, "poly_exp2_per_clk_per_sm": poly,
            "mma_bf16_flop_per_clk_per_sm": mma,
            "mma_flop_per_clk_per_sm_by_shape": dict(ss_n256=mma, **shapes)}

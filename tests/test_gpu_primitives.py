@@ -5,6 +5,7 @@ import pytest
 import torch
 
 import exact_attention_smem_gb300 as fa
+import fa_testing_lib as ft
 import oracle
 
 pytestmark = pytest.mark.gpu
@@ -14,15 +15,15 @@ pytestmark = pytest.mark.gpu
 def _dev():
     fa.load()
     torch.cuda.set_device(0)
-    fa.fa_get_device_error(clear=True)
+    ft.fa_test_get_device_error(clear=True)
     yield
-    assert fa.fa_get_device_error(clear=True) == 0
+    assert ft.fa_test_get_device_error(clear=True) == 0
 
 
 def _exp2_dev(x, mode):
     xd = torch.tensor(x, dtype=torch.float32, device="cuda")
     y = torch.empty_like(xd)
-    fa.fa_test_exp2(xd, y, mode)
+    ft.fa_test_exp2(xd, y, mode)
     torch.cuda.synchronize()
     return y.cpu().numpy()
 
@@ -32,7 +33,7 @@ def test_poly_exp2_device_matches_host_twin_bitwise():
                          (np.arange(0x8000, 0x10000, dtype=np.uint32) << 16).view(np.float32)])
     xs = xs[~np.isnan(xs)]
     dev = _exp2_dev(xs, 0)
-    host = np.array([fa.fa_exp2_poly_host(float(x)) for x in xs], dtype=np.float32)
+    host = np.array([ft.fa_exp2_poly_host(float(x)) for x in xs], dtype=np.float32)
     assert np.array_equal(dev.view(np.uint32), host.view(np.uint32))
     sel = xs >= -125
     rel = np.abs(dev[sel] / oracle.exp2_exact(xs[sel].astype(np.float64)) - 1)
@@ -53,7 +54,7 @@ def test_mma_probe(mode, N):
     A = torch.randn(128, 128, generator=g).to(torch.bfloat16)
     B = torch.randn(*((N, 128) if mode == 0 else (128, N)), generator=g).to(torch.bfloat16)
     C = torch.full((128, N), float("nan"), device="cuda")
-    fa.fa_test_mma(A.cuda(), B.cuda(), C, mode, N)
+    ft.fa_test_mma(A.cuda(), B.cuda(), C, mode, N)
     torch.cuda.synchronize()
     a, b = A.double().numpy(), B.double().numpy()
     want = a @ b.T if mode == 0 else (a @ b if mode == 1 else a.T @ b)
@@ -72,7 +73,7 @@ def test_mma_fp8_probe(mode, N):
     A = rng.choice(codes, (128, 128))
     B = rng.choice(codes, (N, 128))
     C = torch.full((128, N), float("nan"), device="cuda")
-    fa.fa_test_mma_fp8(torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda(), C, mode, N)
+    ft.fa_test_mma_fp8(torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda(), C, mode, N)
     torch.cuda.synchronize()
     a, b = oracle.fp8_e4m3.e4m3_decode(A), oracle.fp8_e4m3.e4m3_decode(B)
     want = a @ b.T
@@ -87,9 +88,9 @@ def test_tma_and_tmem_round_trips():
     src = torch.randn(128, 64, generator=torch.Generator().manual_seed(5)).to(torch.bfloat16).cuda()
     dst = torch.zeros_like(src)
     out = torch.zeros(128, 32, dtype=torch.int32, device="cuda")
-    fa.fa_test_roundtrip(src, dst, out)
+    ft.fa_test_roundtrip(src, dst, out)
     torch.cuda.synchronize()
-    assert fa.fa_get_device_error(clear=True) == 0
+    assert ft.fa_test_get_device_error(clear=True) == 0
     assert torch.equal(dst.view(torch.int16), src.view(torch.int16))
     want = torch.arange(128).view(128, 1) * 1000 + torch.arange(32).view(1, 32)
     assert torch.equal(out.cpu(), want.to(torch.int32))
@@ -104,9 +105,9 @@ def test_mma_pair_probe(mode, N):
     B = torch.randn(*((N, 128) if mode == 0 else (128, N)), generator=g).to(torch.bfloat16)
     C = torch.full((256, N), float("nan"), device="cuda")
     flags = torch.zeros(4, dtype=torch.int32, device="cuda")
-    fa.fa_test_mma_pair(A.cuda(), B.cuda(), C, flags, mode, N)
+    ft.fa_test_mma_pair(A.cuda(), B.cuda(), C, flags, mode, N)
     torch.cuda.synchronize()
-    assert fa.fa_get_device_error(clear=True) == 0
+    assert ft.fa_test_get_device_error(clear=True) == 0
     f = flags.cpu().tolist()
     assert f[0] == 1 and f[1] == 1 and f[2] == f[3], f
     a, b = A.double().numpy(), B.double().numpy()
@@ -117,7 +118,7 @@ def test_mma_pair_probe(mode, N):
 
 def test_bounded_wait_times_out_instead_of_hanging():
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    fa.fa_test_wait_timeout(status, 50.0)
+    ft.fa_test_wait_timeout(status, 50.0)
     torch.cuda.synchronize()
     assert status.item() == 1
-    assert fa.fa_get_device_error(clear=True) == 901
+    assert ft.fa_test_get_device_error(clear=True) == 901

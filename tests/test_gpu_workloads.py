@@ -5,7 +5,10 @@ The whole problem runs on the GPU; the fp64 oracle then checks a subset it can
 finish in seconds to a minute: all heads for the two S=2048 workloads, query
 heads {0, last} for the long and packed ones, and KV group 0 of the first and
 last batch for the GQA one. Tolerances: O max-abs 1e-2, LSE max-abs 1e-3, dQ /
-dK / dV relative L2 2e-2 (over the checked subset).
+dK / dV relative L2 2e-2 (over the checked subset). The default backward form
+is checked on every workload; the two other forms (the dK/dV pass on CTA
+pairs, and the one-pass form with fp32 dQ atomics) on the long and the packed
+workload, against the same oracle result.
 """
 import numpy as np
 import pytest
@@ -25,6 +28,21 @@ def _dev():
     torch.cuda.set_device(0)
     fa.fa_get_device_error(clear=True)
     yield
+    fa.fa_debug_set("bwd_mode", 1)
+
+
+_ORACLE = {}
+
+
+def _oracle_grads(name, w, x):
+    """The oracle's dQ/dK/dV on the checked subset (computed once per workload)."""
+    if name not in _ORACLE:
+        _, kv_heads, seqs = _subset(name, w, x)
+        q, k, v, do = (t.cpu() for t in (x.q, x.k, x.v, x.do))
+        cu_h = None if x.cu_seqlens is None else x.cu_seqlens.cpu()
+        _ORACLE[name] = oracle.backward(q, k, v, do, w.scale, w.causal, cu_seqlens=cu_h,
+                                        kv_heads=kv_heads, seqs=seqs)
+    return _ORACLE[name]
 
 
 def _subset(name, w, x):
@@ -58,27 +76,59 @@ def test_workload_parity(name):
     assert eo <= O_TOL, f"{name}: O max-abs {eo}"
     assert el <= LSE_TOL, f"{name}: LSE max-abs {el}"
     if grads is not None:
-        ref = oracle.backward(q, k, v, do, w.scale, w.causal, cu_seqlens=cu_h, kv_heads=kv_heads,
-                              seqs=seqs)
+        ref = _oracle_grads(name, w, x)
         errs = {n: rel_l2(g, r) for n, g, r in zip(("dq", "dk", "dv"), grads, ref)}
         assert all(e <= GRAD_TOL for e in errs.values()), f"{name}: {errs}"
     print(f"{name}: O {eo:.2e} LSE {el:.2e}" + ("" if grads is None else f" grads {errs}"))
 
 
+@pytest.mark.parametrize("mode", [2, 0], ids=["two_pass_pairs", "one_pass"])
+@pytest.mark.parametrize("name", ["long_s32768_causal", "varlen16_causal"])
+def test_workload_backward_forms(name, mode):
+    """The non-default backward forms at full size, in the bench's launch
+    configuration: the pair kernel's many units per CTA pair, its cluster
+    occupancy and its head groups, and the one-pass form's L2-sized dQ
+    accumulator groups."""
+    w = WORKLOADS[name]
+    x = make_inputs(w, "cuda")
+    cu = x.cu_seqlens
+    o, lse = fa.forward(x.q, x.k, x.v, causal=w.causal, scale=w.scale, cu_seqlens=cu)
+    fa.fa_debug_set("bwd_mode", mode)
+    try:
+        grads = fa.backward(x.q, x.k, x.v, o, lse, x.do, causal=w.causal, scale=w.scale,
+                            cu_seqlens=cu)
+        torch.cuda.synchronize()
+    finally:
+        fa.fa_debug_set("bwd_mode", 1)
+    assert fa.fa_get_device_error(clear=True) == 0
+    ref = _oracle_grads(name, w, x)
+    errs = {n: rel_l2(g, r) for n, g, r in zip(("dq", "dk", "dv"), grads, ref)}
+    assert all(e <= GRAD_TOL for e in errs.values()), f"{name} mode {mode}: {errs}"
+    print(f"{name} bwd_mode {mode}: grads {errs}")
+
+
 def test_gqa_literal_kv_scaling_reading():
     """The literal reading of the GQA workload (factor on K and V rows): O is
     checked against 1e-2 plus half a bf16 ulp of the exact value, since bf16
-    rounding of |O| >= 4 alone can exceed 1e-2; LSE and gradients as usual."""
+    rounding of |O| >= 4 alone can exceed 1e-2; LSE max-abs 1e-3 and dQ / dK /
+    dV relative L2 2e-2 as in every other workload (KV group 0 of the first
+    and last batch)."""
     import dataclasses
     w = dataclasses.replace(WORKLOADS["gqa_s8192_causal"], scale_v=True)
     x = make_inputs(w, "cuda")
     o, lse = fa.forward(x.q, x.k, x.v, causal=True, scale=w.scale)
+    grads = fa.backward(x.q, x.k, x.v, o, lse, x.do, causal=True, scale=w.scale)
     torch.cuda.synchronize()
+    assert fa.fa_get_device_error(clear=True) == 0
     heads = list(range(w.Hq // w.Hkv))
-    ro, rl = oracle.forward(x.q.cpu(), x.k.cpu(), x.v.cpu(), w.scale, True, heads=heads,
-                            seqs=[0, w.B - 1])
+    q, k, v, do = (t.cpu() for t in (x.q, x.k, x.v, x.do))
+    ro, rl = oracle.forward(q, k, v, w.scale, True, heads=heads, seqs=[0, w.B - 1])
     g = o.float().cpu().numpy().astype(np.float64)
     sel = ~np.isnan(ro)
     ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(ro[sel]), 1e-30))) - 7)
     assert np.all(np.abs(g[sel] - ro[sel]) <= O_TOL + 0.5 * ulp)
     assert max_abs(lse, rl) <= LSE_TOL
+    ref = oracle.backward(q, k, v, do, w.scale, True, kv_heads=[0], seqs=[0, w.B - 1])
+    errs = {n: rel_l2(gr, r) for n, gr, r in zip(("dq", "dk", "dv"), grads, ref)}
+    assert all(e <= GRAD_TOL for e in errs.values()), errs
+    print(f"gqa literal K/V scaling: grads {errs}")

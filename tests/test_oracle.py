@@ -99,7 +99,7 @@ def test_zero_queries_closed_form(causal, nq, nk):
 def _brute_force(q, k, v, scale, causal):
     """Pure-Python loops with math.exp: one row at a time, no numpy arithmetic."""
     nq, nk, dv = len(q), len(k), len(v[0])
-    out, lses = [], []
+    out, lses, maxes = [], [], []
     for i in range(nq):
         scores = []
         for j in range(nk):
@@ -111,17 +111,21 @@ def _brute_force(q, k, v, scale, causal):
         tot = sum(x for _, x in w)
         out.append([sum(x * v[j][c] for j, x in w) / tot for c in range(dv)])
         lses.append(mx + math.log(tot))
-    return np.array(out), np.array(lses)
+        maxes.append(mx)
+    return np.array(out), np.array(lses), np.array(maxes)
 
 
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("nq,nk,d", [(5, 5, 3), (3, 6, 2), (4, 4, 1)])
 def test_brute_force_tiny(causal, nq, nk, d):
     q, k, v = _rand((nq, d), 11, 2), _rand((nk, d), 12, 2), _rand((nk, d + 1), 13)
-    o, lse = oracle.attend_head(q, k, v, 0.7, causal)
-    ob, lb = _brute_force(q.tolist(), k.tolist(), v.tolist(), 0.7, causal)
+    o, lse, m = oracle.attend_head(q, k, v, 0.7, causal, return_max=True)
+    ob, lb, mb = _brute_force(q.tolist(), k.tolist(), v.tolist(), 0.7, causal)
     np.testing.assert_allclose(o, ob, atol=1e-13)
     np.testing.assert_allclose(lse, lb, atol=1e-13)
+    np.testing.assert_allclose(m, mb, atol=1e-13)
+    o2, lse2 = oracle.attend_head(q, k, v, 0.7, causal)      # the flag changes nothing else
+    assert np.array_equal(o, o2) and np.array_equal(lse, lse2)
 
 
 @pytest.mark.parametrize("causal", [False, True])
@@ -344,7 +348,7 @@ def _pins_pass(ns):
         for causal in (False, True):
             q, k, v = _rand((5, 3), 11, 2), _rand((6, 3), 12, 2), _rand((6, 4), 13)
             o, lse = attend(q, k, v, 0.7, causal)
-            ob, lb = _brute_force(q.tolist(), k.tolist(), v.tolist(), 0.7, causal)
+            ob, lb, _ = _brute_force(q.tolist(), k.tolist(), v.tolist(), 0.7, causal)
             if not (np.allclose(o, ob, atol=1e-12) and np.allclose(lse, lb, atol=1e-12)):
                 return False
     except Exception:

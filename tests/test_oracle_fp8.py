@@ -5,6 +5,7 @@ invariants, and the fp64 attention oracle's own pins)."""
 import numpy as np
 import pytest
 
+from oracle import attention_fp64 as A
 from oracle import fp8_e4m3 as f8
 from oracle import forward as fwd64
 
@@ -132,6 +133,12 @@ def test_fp8_forward_is_attention_of_dequantized_inputs(causal):
     o8, l8 = f8.forward_fp8(qc, qs, qc, qs, vc, vs, 0.125, causal)
     o, l = fwd64(x, x, x, 0.125, causal)
     assert np.allclose(o8, o, atol=1e-12) and np.allclose(l8, l, atol=1e-12)
+    # the row maxima it returns on request are the fp64 oracle's
+    _, _, m8 = f8.forward_fp8(qc, qs, qc, qs, vc, vs, 0.125, causal, return_max=True)
+    for h in range(H):
+        xh = x[0, :, h]
+        _, _, mh = A.attend_head(xh, xh, xh, 0.125, causal, return_max=True)
+        assert np.allclose(m8[0, h], mh, atol=1e-12)
 
 
 @pytest.mark.parametrize("Sk", [128, 2048])
@@ -152,6 +159,18 @@ def test_weight_rounding_error_matches_the_tolerance_derivation(Sk):
     rel = np.linalg.norm(o8 - o) / np.linalg.norm(o)
     assert 0.005 < rel < 0.05
     assert np.abs(p8 / np.where(p > 0, p, 1) - 1)[p >= 2.0 ** -6].max() <= 2.0 ** -4
+    # Element-wise: a weight in e4m3's normal range is off by at most 2^-4 of
+    # itself, one below it (stored value < 2^-6) by at most half the smallest
+    # subnormal step, 2^-10; divided by the row sum l >= 2^7 (the row maximum
+    # is stored as 2^7), each output element is off by at most
+    # 2^-4 * sum_j p_j |v_jc| / l + 2^-10 * sum_j |v_jc| / l.
+    l = p.sum(axis=1, keepdims=True)
+    bound = 2.0 ** -4 * (p @ np.abs(v)) / l + 2.0 ** -10 * np.abs(v).sum(axis=0) / l
+    err = np.abs(o8 - o)
+    assert np.all(err <= bound)
+    # not vacuous: independent rounding errors partly cancel over many keys,
+    # so the worst case is approached less closely as Sk grows
+    assert (err / bound).max() > 0.05
 
 
 # ---------------------------------------------------------------------------

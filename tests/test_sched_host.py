@@ -8,7 +8,7 @@ import itertools
 
 import pytest
 
-from exact_attention_smem_gb300 import fa_sched_list
+from fa_testing_lib import fa_sched_list
 
 
 def _seqs(B, cu, Sq, Sk):
@@ -128,3 +128,40 @@ def test_causal_balance_near_lpt_bound():
                  for b in range(g)]
         mean = sum(loads) / g
         assert max(loads) <= 1.03 * mean, (kind, max(loads) / mean)
+
+
+def _graham(costs, G):
+    """Graham's list scheduling of the costs in LPT order: each next unit goes
+    to the least-loaded of G workers; returns the largest load."""
+    import heapq
+    loads = [0] * G
+    for c in sorted(costs, reverse=True):
+        heapq.heapreplace(loads, loads[0] + c)
+    return max(loads)
+
+
+def test_varlen_balance_near_lpt_bound():
+    """The packed causal workload (16 sequences, lengths log-uniform on
+    [128, 16384] drawn from seed 4, 32 heads) on 152 CTAs: the static snake
+    deal of the LPT list keeps every CTA's total cost within 5% of the mean,
+    and within 1% of what Graham's greedy list scheduling reaches, for the
+    forward, the dK/dV pass, the dQ pass and the pair dK/dV pass, each with
+    the head grouping its kernel uses for packed layouts (one group)."""
+    import torch
+    from attn_inputs import WORKLOADS, varlen_lengths
+    w = WORKLOADS["varlen16_causal"]
+    gen = torch.Generator(device="cpu").manual_seed(w.seed)
+    lengths = varlen_lengths(gen, w.varlen_nseq, w.varlen_lo, w.varlen_hi)
+    cu = [0]
+    for n in lengths:
+        cu.append(cu[-1] + n)
+    T = cu[-1]
+    for kind in (0, 2, 3, 4):
+        G = 76 if kind == 4 else 152               # the pair kernel's grid counts CTA pairs
+        per = [fa_sched_list(kind, len(lengths), cu, T, T, w.Hq, True, G, b, w.Hq)
+               for b in range(G)]
+        loads = [sum(u[3] for u in units) for units in per]
+        mean = sum(loads) / G
+        assert max(loads) <= 1.05 * mean, (kind, max(loads) / mean)
+        greedy = _graham([u[3] for units in per for u in units], G)
+        assert max(loads) <= 1.01 * greedy, (kind, max(loads) / greedy)
