@@ -8,6 +8,8 @@ causal; backward 2.5x forward.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
   python bench.py --fp8 [--workload W]     # FP8 (e4m3) forward only, one GPU
+  python bench.py --once [--workload W] [--bwd-mode M] [--fp8]
+                                           # one step, no timing (profiler captures)
 
 Prints one JSON line (rank 0). N > 1 (torchrun) runs one independent replica
 per GPU (the path has no exchange step) and reports the whole-job aggregate.
@@ -289,6 +291,33 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def run_once(args):
+    """One forward and one backward (or one FP8 forward) of the workload, no
+    timing and no output line: the launch sequence a profiler capture selects
+    kernels from (forward, preprocess, pad, dK/dV pass, dQ pass)."""
+    import torch
+
+    import exact_attention_smem_gb300 as fa
+    from attn_inputs import WORKLOADS, make_inputs
+
+    torch.cuda.set_device(0)
+    fa.load()
+    w = WORKLOADS[WORKLOAD]
+    x = make_inputs(w, "cuda")
+    if args.fp8:
+        q8, qs = fa.quantize_fp8(x.q, 0)
+        k8, ks = fa.quantize_fp8(x.k, 0)
+        v8, vs = fa.quantize_fp8(x.v, 1)
+        fa.forward_fp8(q8, qs, k8, ks, v8, vs, causal=w.causal, scale=w.scale)
+    else:
+        o, lse = fa.forward(x.q, x.k, x.v, causal=w.causal, scale=w.scale,
+                            cu_seqlens=x.cu_seqlens)
+        fa.backward(x.q, x.k, x.v, o, lse, x.do, causal=w.causal, scale=w.scale,
+                    cu_seqlens=x.cu_seqlens)
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_error() == 0
+
+
 def run_fp8(args):
     """The FP8 (e4m3) forward on one GPU: Q, K, V quantized once before the
     timed region (codes resident in HBM), then K timed forward launches."""
@@ -514,15 +543,27 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline leg")
     ap.add_argument("--fp8", action="store_true", help="time the FP8 (e4m3) forward instead")
     ap.add_argument("--workload", default=WORKLOAD,
-                    choices=["long_s32768_causal", "mha_s2048_causal", "gqa_s8192_causal"],
-                    help="dense causal workload to run (the bench line is long_s32768_causal; "
-                         "the others serve small profiling captures)")
+                    choices=["long_s32768_causal", "mha_s2048_causal", "gqa_s8192_causal",
+                             "varlen16_causal"],
+                    help="causal workload to run (the bench line is long_s32768_causal; the "
+                         "others serve profiling captures and measurements)")
+    ap.add_argument("--once", action="store_true",
+                    help="run one forward + backward and exit (for profiler captures)")
+    ap.add_argument("--bwd-mode", type=int, default=None, choices=[0, 1, 2],
+                    help="backward form (fa_debug_set bwd_mode; default: the library's)")
     args = ap.parse_args()
+    if args.workload == "varlen16_causal" and not args.once:
+        ap.error("the packed workload runs with --once only")
+    if args.bwd_mode is not None:
+        import exact_attention_smem_gb300 as fa
+        fa.fa_debug_set("bwd_mode", args.bwd_mode)
     if args.steps is None:
         args.steps = 50 if args.fp8 else 10
     globals()["WORKLOAD"] = args.workload
     if args.impl == "reference":
         run_reference(args)
+    elif args.once:
+        run_once(args)
     elif args.fp8:
         run_fp8(args)
     else:
