@@ -288,7 +288,8 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const f
   Shape sh;
   int st = validate_common(ptrs, 9, B, Hq, Hkv, Sq, Sk, d, scale, cu_seqlens, &sh, cu_seqlens_k);
   if (st != FA_OK) return st;
-  if (d > 128) return fail(FA_ERR_UNSUPPORTED, "backward head dim %d (supported: 64, 128)", d);
+  if (d > 192)
+    return fail(FA_ERR_UNSUPPORTED, "backward head dim %d (supported: 64, 128, 192)", d);
   if (B == 0 || (sh.Tq == 0 && sh.Tk == 0)) return FA_OK;
   const size_t need = fa_bwd_workspace_bytes(B, Hq, Sq, d, sh.packed ? (int)sh.Tq : 0);
   if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
@@ -316,12 +317,20 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const f
   if ((st = encode_rows(&p.tm_v, sh.Tk > 0 ? v : q, sh.Tk > 0 ? Tk : Tq, sh.Tk > 0 ? Hkv : Hq,
                         d)) != FA_OK)
     return st;
-  if (mode == 2) {
+  if (mode == 2 || d == 192) {
     if ((st = encode_rows(&p.tm_q2, sh.Tq > 0 ? q : k, sh.Tq > 0 ? Tq : Tk, sh.Tq > 0 ? Hq : Hkv,
                           d, 64)) != FA_OK)
       return st;
     if ((st = encode_rows(&p.tm_do2, sh.Tq > 0 ? dout : k, sh.Tq > 0 ? Tq : Tk,
                           sh.Tq > 0 ? Hq : Hkv, d, 64)) != FA_OK)
+      return st;
+  }
+  if (d == 192) {
+    if ((st = encode_rows(&p.tm_k2, sh.Tk > 0 ? k : q, sh.Tk > 0 ? Tk : Tq, sh.Tk > 0 ? Hkv : Hq,
+                          d, 64)) != FA_OK)
+      return st;
+    if ((st = encode_rows(&p.tm_v2, sh.Tk > 0 ? v : q, sh.Tk > 0 ? Tk : Tq, sh.Tk > 0 ? Hkv : Hq,
+                          d, 64)) != FA_OK)
       return st;
   }
   auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };

@@ -57,12 +57,19 @@ constexpr int REGS_CONTROL = 104;
 constexpr int SMEM_LIMIT = 232448;
 constexpr int MAX_SEQ_SMEM = 200;  // packed boundaries kept in shared memory up to this
 
-template <int D>
+template <int D, int ROWS = 128>
 struct Tile {
   static constexpr int CHUNKS = D / 64;        // 128-byte column chunks per row
-  static constexpr int CHUNK = 128 * 128;      // 128 rows x 128 bytes, 128B swizzle
-  static constexpr int BYTES = CHUNKS * CHUNK; // one 128-row tile
+  static constexpr int CHUNK = ROWS * 128;     // ROWS rows x 128 bytes, 128B swizzle
+  static constexpr int BYTES = CHUNKS * CHUNK; // one tile of ROWS rows
 };
+
+// Head dims up to 128 step over 128 query rows (dK/dV pass) and 128 keys (dQ
+// pass). Head dim 192 steps over 64: the dK/dV pass then holds dV 192 + dK 192
+// + S^T 64 + dP^T 64 = 512 TMEM columns and ~216 KB of tiles, the dQ pass
+// S 2 x 64 + dP 64 + dQ 192 = 384 columns and ~216 KB.
+template <int D>
+constexpr int step_rows() { return D > 128 ? 64 : 128; }
 
 // dK/dV pass layout. Q slots are held from S^T(i) to dK(i), the longest span,
 // so Q gets three slots and dO two. The -LSE*log2(e) and -D values of a
@@ -73,10 +80,12 @@ struct Tile {
 template <int D>
 struct CfgKV {
   using T = Tile<D>;
+  static constexpr int BMS = step_rows<D>();          // query rows per step
+  using QT = Tile<D, BMS>;                             // a Q or dO step tile
   static constexpr int NQ = 3, NDO = 2, NLD = 2;
-  static constexpr int LD_BYTES = 2 * BM * 4;          // [-LSE*log2e x128][-D x128]
+  static constexpr int LD_BYTES = 2 * BMS * 4;        // [-LSE*log2e x BMS][-D x BMS]
   static constexpr int K_OFF = 0, V_OFF = T::BYTES, Q_OFF = 2 * T::BYTES,
-                       DO_OFF = Q_OFF + NQ * T::BYTES, LD_OFF = DO_OFF + NDO * T::BYTES,
+                       DO_OFF = Q_OFF + NQ * QT::BYTES, LD_OFF = DO_OFF + NDO * QT::BYTES,
                        BAR_OFF = LD_OFF + NLD * LD_BYTES;
   static constexpr int B_KVFULL = 0, B_KVEMPTY = 1, B_QFULL = 2, B_QEMPTY = B_QFULL + NQ,
                        B_DOFULL = B_QEMPTY + NQ, B_DOEMPTY = B_DOFULL + NDO,
@@ -88,10 +97,10 @@ struct CfgKV {
   static constexpr int CU_OFF = MISC_OFF + 16;
   static constexpr int SMEM_BYTES = CU_OFF + (MAX_SEQ_SMEM + 1) * 4;
   static_assert(SMEM_BYTES <= SMEM_LIMIT, "dK/dV pass shared memory");
-  // TMEM: dV [0,D), dK [D,2D), S^T/P^T [2D,2D+128), dP^T/dS^T [2D+128,2D+256)
-  static constexpr uint32_t TM_DV = 0, TM_DK = D, TM_SB = 2 * D, TM_DB = 2 * D + 128;
-  static_assert(2 * D + 256 <= 512, "TMEM columns");
-  static constexpr uint32_t IDESC_S = idesc_bf16(128, 128, false, false);  // S^T, dP^T
+  // TMEM: dV [0,D), dK [D,2D), S^T/P^T [2D,2D+BMS), dP^T/dS^T [2D+BMS,2D+2BMS)
+  static constexpr uint32_t TM_DV = 0, TM_DK = D, TM_SB = 2 * D, TM_DB = 2 * D + BMS;
+  static_assert(2 * D + 2 * BMS <= 512, "TMEM columns");
+  static constexpr uint32_t IDESC_S = idesc_bf16(128, BMS, false, false);  // S^T, dP^T
   static constexpr uint32_t IDESC_ACC = idesc_bf16(128, D, false, true);   // dV, dK
 };
 
@@ -101,9 +110,11 @@ struct CfgKV {
 template <int D>
 struct CfgQ {
   using T = Tile<D>;
+  static constexpr int BNS = step_rows<D>();          // keys per block
+  using KT = Tile<D, BNS>;                             // a K or V block tile
   static constexpr int NKV = 5;
   static constexpr int Q_OFF = 0, DO_OFF = T::BYTES, KV_OFF = 2 * T::BYTES,
-                       BAR_OFF = KV_OFF + NKV * T::BYTES;
+                       BAR_OFF = KV_OFF + NKV * KT::BYTES;
   static constexpr int B_QFULL = 0, B_QEMPTY = 1, B_KVFULL = 2, B_KVEMPTY = B_KVFULL + NKV,
                        B_SFULL = B_KVEMPTY + NKV,   // [2]
                        B_DPFULL = B_SFULL + 2, B_DSREADY = B_DPFULL + 1,
@@ -112,9 +123,10 @@ struct CfgQ {
   static constexpr int CU_OFF = MISC_OFF + 16;
   static constexpr int SMEM_BYTES = CU_OFF + (MAX_SEQ_SMEM + 1) * 4 + 1024;
   static_assert(SMEM_BYTES <= SMEM_LIMIT, "dQ pass shared memory");
-  // TMEM: S/dS buffers [0,128) and [128,256), dP [256,384), dQ [384,384+D)
-  static constexpr uint32_t TM_S = 0, TM_DP = 256, TM_DQ = 384;
-  static constexpr uint32_t IDESC_S = idesc_bf16(128, 128, false, false);  // S, dP
+  // TMEM: S/dS buffers [0,BNS) and [BNS,2BNS), dP [2BNS,3BNS), dQ [3BNS,3BNS+D)
+  static constexpr uint32_t TM_S = 0, TM_DP = 2 * BNS, TM_DQ = 3 * BNS;
+  static_assert(3 * BNS + D <= 512, "TMEM columns");
+  static constexpr uint32_t IDESC_S = idesc_bf16(128, BNS, false, false);  // S, dP
   static constexpr uint32_t IDESC_DQ = idesc_bf16(128, D, false, true);    // dQ
 };
 
@@ -129,27 +141,33 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64
   }
 }
 
-// X (TMEM, 128 x 128 fp32) = A (128 rows x D) * B (128 rows x D)^T, both K-major tiles.
-template <int D, uint32_t IDESC>
+// X (TMEM, 128 x BROWS fp32) = A (128 rows x D) * B (BROWS rows x D)^T, both
+// K-major tiles.
+template <int D, uint32_t IDESC, int BROWS = 128>
 __device__ __forceinline__ void mma_abt(uint32_t tm, uint32_t a, uint32_t b) {
-  using T = Tile<D>;
+  using TA = Tile<D>;
+  using TB = Tile<D, BROWS>;
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
-    const uint32_t off = (kk >> 2) * T::CHUNK + (kk & 3) * 32;
-    mma_ss(tm, sdesc_sw128(a + off, T::CHUNK, 1024), sdesc_sw128(b + off, T::CHUNK, 1024), IDESC,
+    const uint32_t k_off = (kk & 3) * 32;
+    mma_ss(tm, sdesc_sw128(a + (kk >> 2) * TA::CHUNK + k_off, TA::CHUNK, 1024),
+           sdesc_sw128(b + (kk >> 2) * TB::CHUNK + k_off, TB::CHUNK, 1024), IDESC,
            kk > 0 ? 1u : 0u);
   }
 }
 
-// Acc (TMEM, 128 x D) (+)= X (TMEM, 128 x 128 bf16 in columns [0,32) and [64,96))
-//                          * Y (128 rows x D tile, MN-major B)
-template <int D, uint32_t IDESC>
+// Acc (TMEM, 128 x D) (+)= X (TMEM, 128 x KROWS bf16; each warpgroup's half of
+//                          the K dimension packed into the first half of its
+//                          KROWS/2 fp32 columns: [0, KROWS/4) and [KROWS/2, 3KROWS/4))
+//                          * Y (KROWS rows x D tile, MN-major B)
+template <int D, uint32_t IDESC, int KROWS = 128>
 __device__ __forceinline__ void mma_acc(uint32_t tm_acc, uint32_t tm_x, uint32_t y, bool acc) {
-  using T = Tile<D>;
+  using TY = Tile<D, KROWS>;
+  constexpr int KS = KROWS / 16;                  // K steps; half of them per warpgroup
 #pragma unroll
-  for (int kk = 0; kk < 8; ++kk) {
-    const uint32_t ta = tm_x + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8);
-    mma_ts(tm_acc, ta, sdesc_sw128(y + kk * 2048, T::CHUNK, 1024), IDESC,
+  for (int kk = 0; kk < KS; ++kk) {
+    const uint32_t ta = tm_x + (kk < KS / 2 ? kk * 8 : KROWS / 2 + (kk - KS / 2) * 8);
+    mma_ts(tm_acc, ta, sdesc_sw128(y + kk * 2048, TY::CHUNK, 1024), IDESC,
            (acc || kk > 0) ? 1u : 0u);
   }
 }
@@ -160,12 +178,32 @@ __device__ __forceinline__ uint32_t pack2(uint64_t v) {
   return pack_bf16x2(lo, hi);
 }
 
-// 64 fp32 values -> 32 bf16 pairs, stored over the first 32 of the 64 columns.
-__device__ __forceinline__ void store_bf16_half(uint32_t taddr, const uint64_t (&v2)[32]) {
-  uint32_t pk[32];
+// COLS fp32 values (COLS/2 pairs) -> bf16 pairs stored over the first COLS/2 columns.
+template <int COLS = 64>
+__device__ __forceinline__ void store_bf16_half(uint32_t taddr, const uint64_t (&v2)[COLS / 2]) {
+  uint32_t pk[COLS / 2];
 #pragma unroll
-  for (int c = 0; c < 32; ++c) pk[c] = pack2(v2[c]);
-  tmem_st32(taddr, pk);
+  for (int c = 0; c < COLS / 2; ++c) pk[c] = pack2(v2[c]);
+  if constexpr (COLS == 64)
+    tmem_st32(taddr, pk);
+  else
+    tmem_st16(taddr, pk);
+}
+
+// TMEM row loads of a warpgroup's COLS columns (64 or 32).
+template <int COLS>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[COLS]) {
+  if constexpr (COLS == 64)
+    tmem_ld64(taddr, r);
+  else
+    tmem_ld32(taddr, r);
+}
+template <int COLS>
+__device__ __forceinline__ void tmem_st_half(uint32_t taddr, const uint32_t* r) {
+  if constexpr (COLS == 64)
+    tmem_st32(taddr, r);
+  else
+    tmem_st16(taddr, r);
 }
 
 struct StepInfo {
@@ -180,11 +218,13 @@ __device__ __forceinline__ StepInfo step_of(int i, int cost, int m_first, int g,
   return s;
 }
 
+// First block of QROWS query rows that sees the unit's keys.
+template <int QROWS = BM>
 __device__ __forceinline__ int first_qblock(const Unit& u, int causal) {
   if (!causal) return 0;
   int r0 = u.m * BN - (u.k_len - u.q_len);
   r0 = r0 > 0 ? r0 : 0;
-  return r0 / BM;
+  return r0 / QROWS;
 }
 
 // Writes one warpgroup's half (D/2 columns) of a TMEM accumulator row to a bf16 row.
@@ -231,6 +271,9 @@ template <int D, int POLY8>
 __global__ void __launch_bounds__(NUM_THREADS, 1) dkdv_kernel(const __grid_constant__ BwdParams p) {
   using C = CfgKV<D>;
   using T = Tile<D>;
+  using QT = typename C::QT;
+  constexpr int BMS = C::BMS;                           // query rows per step
+  constexpr int COLS = BMS / 2;                         // score columns per warpgroup
   extern __shared__ __align__(1024) uint8_t smem_al[];
   uint32_t base;                                        // opaque to the compiler: checked, not assumed
   asm volatile("{\n\t.reg .u64 t;\n\tcvta.to.shared.u64 t, %1;\n\tcvt.u32.u64 %0, t;\n\t}"
@@ -294,8 +337,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dkdv_kernel(const __grid_const
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  const SchedSpec spec{cu_in_smem ? cu_s : p.cu, p.nseq, p.Sq, p.Sk, p.Hkv, p.causal, BN, BM, 1,
-                       p.hblock, nullptr, p.k_off};
+  const SchedSpec spec{cu_in_smem ? cu_s : p.cu, p.nseq, p.Sq, p.Sk, p.Hkv, p.causal, BN, BMS,
+                       1, p.hblock, nullptr, p.k_off};
   const WaitCtl wc{p.err, abort_flag, p.timeout_ns};
   const int G = gridDim.x;
   const int cta = blockIdx.x;
@@ -318,7 +361,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dkdv_kernel(const __grid_const
         if (!w.seek(snake_index(k, G, cta), u)) break;
         if (u.cost == 0) continue;
         const int n = u.cost * group;
-        const int m_first = first_qblock(u, p.causal);
+        const int m_first = first_qblock<BMS>(u, p.causal);
         // The first two steps' Q/dO need only free ring slots: they go out
         // before the wait for the previous unit to release K/V.
         const int lead = n < 2 ? n : 2;
@@ -342,15 +385,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dkdv_kernel(const __grid_const
           // Q(s) goes into slot s % NQ once dK(s - NQ) is done, dO(s) into slot
           // s % NDO once dV(s - NDO) is done.
           const StepInfo st = step_of(i, u.cost, m_first, u.head, group);
-          const int row = u.q_start + st.m * BM;
+          const int row = u.q_start + st.m * BMS;
           const int sq = nq % C::NQ, sd = nd % C::NDO;
           if (nq >= (uint32_t)C::NQ) {
             ok = mbar_wait(BAR(C::B_QEMPTY + sq), ((nq / C::NQ) - 1) & 1, wc, SITE_DKDV_Q_EMPTY);
             if (!ok) break;
           }
-          mbar_arrive_expect_tx(BAR(C::B_QFULL + sq), T::BYTES);
-          for (int c = 0; c < T::CHUNKS; ++c)
-            tma_load_3d(base + C::Q_OFF + sq * T::BYTES + c * T::CHUNK, &p.tm_q,
+          mbar_arrive_expect_tx(BAR(C::B_QFULL + sq), QT::BYTES);
+          for (int c = 0; c < QT::CHUNKS; ++c)
+            tma_load_3d(base + C::Q_OFF + sq * QT::BYTES + c * QT::CHUNK, &p.tm_q,
                         BAR(C::B_QFULL + sq), c * 64, st.h, row);
           ++nq;
           if (nd >= (uint32_t)C::NDO) {
@@ -358,9 +401,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dkdv_kernel(const __grid_const
                            SITE_DKDV_DO_EMPTY);
             if (!ok) break;
           }
-          mbar_arrive_expect_tx(BAR(C::B_DOFULL + sd), T::BYTES);
-          for (int c = 0; c < T::CHUNKS; ++c)
-            tma_load_3d(base + C::DO_OFF + sd * T::BYTES + c * T::CHUNK, &p.tm_do,
+          mbar_arrive_expect_tx(BAR(C::B_DOFULL + sd), QT::BYTES);
+          for (int c = 0; c < QT::CHUNKS; ++c)
+            tma_load_3d(base + C::DO_OFF + sd * QT::BYTES + c * QT::CHUNK, &p.tm_do,
                         BAR(C::B_DOFULL + sd), c * 64, st.h, row);
           ++nd;
           // the step's row values, released by the compute warps after dS
@@ -371,11 +414,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dkdv_kernel(const __grid_const
             if (!ok) break;
           }
           const long long off = (long long)st.h * p.pad_hstride + pad_start(u.seq, u.q_start) +
-                                (long long)st.m * BM;
+                                (long long)st.m * BMS;
           const uint32_t ld = base + C::LD_OFF + sl * C::LD_BYTES;
           mbar_arrive_expect_tx(BAR(C::B_LDFULL + sl), C::LD_BYTES);
-          bulk_load(ld, p.lse2 + off, BM * 4, BAR(C::B_LDFULL + sl));
-          bulk_load(ld + BM * 4, p.delta + off, BM * 4, BAR(C::B_LDFULL + sl));
+          bulk_load(ld, p.lse2 + off, BMS * 4, BAR(C::B_LDFULL + sl));
+          bulk_load(ld + BMS * 4, p.delta + off, BMS * 4, BAR(C::B_LDFULL + sl));
           ++nl;
         }
       }
@@ -400,8 +443,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dkdv_kernel(const __grid_const
       bool ok = true;
       const uint32_t kt = base + C::K_OFF, vt = base + C::V_OFF;
       const uint32_t tSB = tmem + C::TM_SB, tDB = tmem + C::TM_DB;
-      auto qslot = [&](uint32_t s) { return base + C::Q_OFF + (s % C::NQ) * T::BYTES; };
-      auto dslot = [&](uint32_t s) { return base + C::DO_OFF + (s % C::NDO) * T::BYTES; };
+      auto qslot = [&](uint32_t s) { return base + C::Q_OFF + (s % C::NQ) * QT::BYTES; };
+      auto dslot = [&](uint32_t s) { return base + C::DO_OFF + (s % C::NDO) * QT::BYTES; };
       for (int k = 0; ok; ++k) {
         Unit u;
         if (!w.seek(snake_index(k, G, cta), u)) break;
@@ -422,9 +465,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dkdv_kernel(const __grid_const
                         BAR(C::B_DOFULL + it % C::NDO), (it / C::NDO) & 1, SITE_DKDV_DO_FULL, wc);
         if (!ok) break;
         tc_fence_after();
-        mma_abt<D, C::IDESC_S>(tSB, kt, qslot(it));
+        mma_abt<D, C::IDESC_S, BMS>(tSB, kt, qslot(it));
         tc_commit(BAR(C::B_SFULL));
-        mma_abt<D, C::IDESC_S>(tDB, vt, dslot(it));
+        mma_abt<D, C::IDESC_S, BMS>(tDB, vt, dslot(it));
         tc_commit(BAR(C::B_DPFULL));
         // K and V feed only S^T and dP^T: they are released once the unit's
         // last dP^T is issued, so the next unit's copy overlaps this one's tail
@@ -440,10 +483,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dkdv_kernel(const __grid_const
           if (!ok) break;
           FA_TRACE(TR_KV_A, it);
           tc_fence_after();
-          mma_acc<D, C::IDESC_ACC>(tmem + C::TM_DV, tSB, dslot(it), i > 0);
+          mma_acc<D, C::IDESC_ACC, BMS>(tmem + C::TM_DV, tSB, dslot(it), i > 0);
           tc_commit(BAR(C::B_DOEMPTY + it % C::NDO));
           if (more) {
-            mma_abt<D, C::IDESC_S>(tSB, kt, qslot(it1));
+            mma_abt<D, C::IDESC_S, BMS>(tSB, kt, qslot(it1));
             tc_commit(BAR(C::B_SFULL));
           }
           // ---- B(i)
@@ -454,10 +497,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dkdv_kernel(const __grid_const
           if (!ok) break;
           FA_TRACE(TR_KV_B, it);
           tc_fence_after();
-          mma_acc<D, C::IDESC_ACC>(tmem + C::TM_DK, tDB, qslot(it), i > 0);
+          mma_acc<D, C::IDESC_ACC, BMS>(tmem + C::TM_DK, tDB, qslot(it), i > 0);
           tc_commit(BAR(C::B_QEMPTY + it % C::NQ));
           if (more) {
-            mma_abt<D, C::IDESC_S>(tDB, vt, dslot(it1));
+            mma_abt<D, C::IDESC_S, BMS>(tDB, vt, dslot(it1));
             tc_commit(BAR(C::B_DPFULL));
             if (i + 2 == n) tc_commit(BAR(C::B_KVEMPTY));
           } else {
@@ -479,7 +522,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dkdv_kernel(const __grid_const
     const int lg = warp & 3;
     const int j = lg * 32 + lane;                         // key row within the block
     const uint32_t lane_off = (uint32_t)(lg * 32) << 16;
-    const int c0 = wg * 64;
+    const int c0 = wg * COLS;
     const uint32_t t_s = tmem + lane_off + C::TM_SB + c0;
     const uint32_t t_dp = tmem + lane_off + C::TM_DB + c0;
     const float sl2 = p.scale_log2;
@@ -505,7 +548,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dkdv_kernel(const __grid_const
         continue;
       }
       const int n = u.cost * group;
-      const int m_first = first_qblock(u, p.causal);
+      const int m_first = first_qblock<BMS>(u, p.causal);
       // query q (within the sequence) sees this key iff q >= qmin
       const int qmin = p.causal ? key - (u.k_len - u.q_len) : -(1 << 30);
       for (int i = 0; i < n; ++i, ++it) {
@@ -515,27 +558,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dkdv_kernel(const __grid_const
         const uint32_t sl = it % C::NLD;
         const float4* nl4 =
             reinterpret_cast<const float4*>(smem + C::LD_OFF + sl * C::LD_BYTES) + c0 / 4;
-        const float4* nd4 = nl4 + BM / 4;
+        const float4* nd4 = nl4 + BMS / 4;
         ok = mbar_wait(BAR(C::B_LDFULL + sl), (it / C::NLD) & 1, wc, SITE_DKDV_LD_FULL);
         if (!ok) break;
         // -LSE*log2(e) into registers while S^T is still on its way
-        float4 l4r[16];
+        float4 l4r[COLS / 4];
 #pragma unroll
-        for (int c = 0; c < 16; ++c) l4r[c] = nl4[c];
+        for (int c = 0; c < COLS / 4; ++c) l4r[c] = nl4[c];
         ok = mbar_wait(BAR(C::B_SFULL), it & 1, wc, SITE_DKDV_S_FULL);
         if (!ok) break;
         if (threadIdx.x == 0) FA_TRACE(TR_KV_S, it);
         tc_fence_after();
-        uint32_t sa[64];
-        tmem_ld64(t_s, sa);
+        uint32_t sa[COLS];
+        tmem_ld_cols<COLS>(t_s, sa);
         // columns c with q0 + c < qmin are masked; a key past the sequence masks all
-        const int cmin = key_ok ? qmin - (st.m * BM + c0) : 64;
+        const int cmin = key_ok ? qmin - (st.m * BMS + c0) : COLS;
         const bool mask = __any_sync(0xffffffffu, cmin > 0);
-        uint64_t p2[32];
+        uint64_t p2[COLS / 2];
         {
           const uint64_t sl2x2 = f2pack(sl2, sl2);
 #pragma unroll
-          for (int c = 0; c < 64; c += 4) {
+          for (int c = 0; c < COLS; c += 4) {
             const float4 l4 = l4r[c / 4];
             float x[4];
             f2unpack(ffma2(f2pack(u2f(sa[c]), u2f(sa[c + 1])), sl2x2, f2pack(l4.x, l4.y)), x[0],
@@ -552,7 +595,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dkdv_kernel(const __grid_const
             p2[c / 2 + 1] = f2pack(pe[2], pe[3]);
           }
         }
-        store_bf16_half(t_s, p2);
+        store_bf16_half<COLS>(t_s, p2);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(BAR(C::B_PREADY));
@@ -561,11 +604,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dkdv_kernel(const __grid_const
         if (!ok) break;
         if (threadIdx.x == 0) FA_TRACE(TR_KV_DP, it);
         tc_fence_after();
-        uint32_t dpa[64];
-        tmem_ld64(t_dp, dpa);
-        uint32_t pk[32];
+        uint32_t dpa[COLS];
+        tmem_ld_cols<COLS>(t_dp, dpa);
+        uint32_t pk[COLS / 2];
 #pragma unroll
-        for (int c = 0; c < 64; c += 4) {
+        for (int c = 0; c < COLS; c += 4) {
           const float4 d4 = nd4[c / 4];
           pk[c / 2] = pack2(fmul2(p2[c / 2], fadd2(f2pack(u2f(dpa[c]), u2f(dpa[c + 1])),
                                                    f2pack(d4.x, d4.y))));
@@ -574,7 +617,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dkdv_kernel(const __grid_const
                                             f2pack(d4.z, d4.w))));
         }
         mbar_arrive(BAR(C::B_LDEMPTY + sl));
-        tmem_st32(t_dp, pk);
+        tmem_st_half<COLS>(t_dp, pk);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(BAR(C::B_DSREADY));
@@ -1065,6 +1108,9 @@ template <int D, int POLY8>
 __global__ void __launch_bounds__(NUM_THREADS, 1) dq_kernel(const __grid_constant__ BwdParams p) {
   using C = CfgQ<D>;
   using T = Tile<D>;
+  using KT = typename C::KT;
+  constexpr int BNS = C::BNS;                           // keys per block
+  constexpr int COLS = BNS / 2;                         // score columns per warpgroup
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -1114,7 +1160,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dq_kernel(const __grid_constan
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  const SchedSpec spec{cu_in_smem ? cu_s : p.cu, p.nseq, p.Sq, p.Sk, p.Hq, p.causal, BM, BN, 0,
+  const SchedSpec spec{cu_in_smem ? cu_s : p.cu, p.nseq, p.Sq, p.Sk, p.Hq, p.causal, BM, BNS, 0,
                        p.hblock_q, nullptr, p.k_off};
   const WaitCtl wc{p.err, abort_flag, p.timeout_ns};
   const int G = gridDim.x;
@@ -1161,12 +1207,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dq_kernel(const __grid_constan
               if (!ok) break;
             }
             if (which == 0) FA_TRACE(TR_Q_KLOAD, pj);
-            mbar_arrive_expect_tx(BAR(C::B_KVFULL + s), T::BYTES);
+            mbar_arrive_expect_tx(BAR(C::B_KVFULL + s), KT::BYTES);
             const void* tm = which ? static_cast<const void*>(&p.tm_v)
                                    : static_cast<const void*>(&p.tm_k);
-            for (int c = 0; c < T::CHUNKS; ++c)
-              tma_load_3d(base + C::KV_OFF + s * T::BYTES + c * T::CHUNK, tm,
-                          BAR(C::B_KVFULL + s), c * 64, kvh, u.k_start + jb * BN);
+            for (int c = 0; c < KT::CHUNKS; ++c)
+              tma_load_3d(base + C::KV_OFF + s * KT::BYTES + c * KT::CHUNK, tm,
+                          BAR(C::B_KVFULL + s), c * 64, kvh, u.k_start + jb * BNS);
           }
           ++pj;
         }
@@ -1186,7 +1232,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dq_kernel(const __grid_constan
       int u_it = 0;
       bool ok = true;
       const uint32_t qt = base + C::Q_OFF, dot = base + C::DO_OFF;
-      auto kv = [&](uint32_t x) { return base + C::KV_OFF + (x % C::NKV) * T::BYTES; };
+      auto kv = [&](uint32_t x) { return base + C::KV_OFF + (x % C::NKV) * KT::BYTES; };
       auto full = [&](uint32_t x) { return BAR(C::B_KVFULL + x % C::NKV); };
       auto empty = [&](uint32_t x) { return BAR(C::B_KVEMPTY + x % C::NKV); };
       auto ph = [&](uint32_t x) { return (x / C::NKV) & 1; };
@@ -1205,9 +1251,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dq_kernel(const __grid_constan
                         SITE_DQ_KV_FULL, full(r + 1), ph(r + 1), SITE_DQ_KV_FULL, wc);
         if (!ok) break;
         tc_fence_after();
-        mma_abt<D, C::IDESC_S>(tmem + C::TM_S + 128 * (sj & 1), qt, kv(r));
+        mma_abt<D, C::IDESC_S, BNS>(tmem + C::TM_S + BNS * (sj & 1), qt, kv(r));
         tc_commit(BAR(C::B_SFULL + (sj & 1)));
-        mma_abt<D, C::IDESC_S>(tmem + C::TM_DP, dot, kv(r + 1));
+        mma_abt<D, C::IDESC_S, BNS>(tmem + C::TM_DP, dot, kv(r + 1));
         tc_commit(BAR(C::B_DPFULL));
         tc_commit(empty(r + 1));
         if (n == 1) tc_commit(BAR(C::B_QEMPTY));
@@ -1215,7 +1261,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dq_kernel(const __grid_constan
           ok = mbar_wait(full(r + 2), ph(r + 2), wc, SITE_DQ_KV_FULL);
           if (!ok) break;
           tc_fence_after();
-          mma_abt<D, C::IDESC_S>(tmem + C::TM_S + 128 * ((sj + 1) & 1), qt, kv(r + 2));
+          mma_abt<D, C::IDESC_S, BNS>(tmem + C::TM_S + BNS * ((sj + 1) & 1), qt, kv(r + 2));
           tc_commit(BAR(C::B_SFULL + ((sj + 1) & 1)));
         }
         for (int jb = 0; jb < n && ok; ++jb, ++sj) {
@@ -1229,10 +1275,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dq_kernel(const __grid_constan
           if (!ok) break;
           FA_TRACE(TR_Q_SYNC, sj);
           tc_fence_after();
-          mma_acc<D, C::IDESC_DQ>(tmem + C::TM_DQ, tmem + C::TM_S + 128 * b, kv(rk), jb > 0);
+          mma_acc<D, C::IDESC_DQ, BNS>(tmem + C::TM_DQ, tmem + C::TM_S + BNS * b, kv(rk), jb > 0);
           tc_commit(empty(rk));
           if (more) {
-            mma_abt<D, C::IDESC_S>(tmem + C::TM_DP, dot, kv(rv1));
+            mma_abt<D, C::IDESC_S, BNS>(tmem + C::TM_DP, dot, kv(rv1));
             tc_commit(BAR(C::B_DPFULL));
             tc_commit(empty(rv1));
             if (jb + 2 == n) tc_commit(BAR(C::B_QEMPTY));
@@ -1240,7 +1286,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dq_kernel(const __grid_constan
             tc_commit(BAR(C::B_DQFULL));
           }
           if (more2) {
-            mma_abt<D, C::IDESC_S>(tmem + C::TM_S + 128 * b, qt, kv(rk2));
+            mma_abt<D, C::IDESC_S, BNS>(tmem + C::TM_S + BNS * b, qt, kv(rk2));
             tc_commit(BAR(C::B_SFULL + b));
           }
         }
@@ -1260,7 +1306,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dq_kernel(const __grid_constan
     const int lg = warp & 3;
     const int rr = lg * 32 + lane;                        // query row within the block
     const uint32_t lane_off = (uint32_t)(lg * 32) << 16;
-    const int c0 = wg * 64;
+    const int c0 = wg * COLS;
     const uint32_t t_s = tmem + lane_off + C::TM_S + c0;
     const uint32_t t_dp = tmem + lane_off + C::TM_DP + c0;
     const float sl2 = p.scale_log2;
@@ -1296,13 +1342,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dq_kernel(const __grid_constan
         if (!ok) break;
         if (threadIdx.x == 0) FA_TRACE(TR_Q_S, sj);
         tc_fence_after();
-        uint32_t sa[64];
-        tmem_ld64(t_s + 128 * b, sa);
-        const int lim = kv_lim - (jb * BN + c0);          // columns c >= lim are masked
-        const bool mask = __any_sync(0xffffffffu, lim < 64);
-        uint64_t p2[32];
+        uint32_t sa[COLS];
+        tmem_ld_cols<COLS>(t_s + BNS * b, sa);
+        const int lim = kv_lim - (jb * BNS + c0);         // columns c >= lim are masked
+        const bool mask = __any_sync(0xffffffffu, lim < COLS);
+        uint64_t p2[COLS / 2];
 #pragma unroll
-        for (int c = 0; c < 64; c += 2) {
+        for (int c = 0; c < COLS; c += 2) {
           float x0, x1;
           f2unpack(ffma2(f2pack(u2f(sa[c]), u2f(sa[c + 1])), sl2x2, nl2), x0, x1);
           float e0 = (c & 7) < POLY8 ? exp2_poly(x0) : ex2_mufu(x0);
@@ -1318,13 +1364,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dq_kernel(const __grid_constan
         if (!ok) break;
         if (threadIdx.x == 0) FA_TRACE(TR_Q_DP, sj);
         tc_fence_after();
-        uint32_t dpa[64];
-        tmem_ld64(t_dp, dpa);
-        uint32_t pk[32];
+        uint32_t dpa[COLS];
+        tmem_ld_cols<COLS>(t_dp, dpa);
+        uint32_t pk[COLS / 2];
 #pragma unroll
-        for (int c = 0; c < 64; c += 2)
+        for (int c = 0; c < COLS; c += 2)
           pk[c / 2] = pack2(fmul2(p2[c / 2], fadd2(f2pack(u2f(dpa[c]), u2f(dpa[c + 1])), nd2)));
-        tmem_st32(t_s + 128 * b, pk);
+        tmem_st_half<COLS>(t_s + BNS * b, pk);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(BAR(C::B_DSREADY));
@@ -1352,9 +1398,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dq_kernel(const __grid_constan
 
 }  // namespace bsplit
 
+// The dK/dV pass runs with p_kv, the dQ pass with p_q (for head dim 192 the two
+// passes read Q/dO and K/V through tensor maps with different box heights).
 template <int D, int POLY8>
-static cudaError_t launch_split_pair(const BwdParams& p, int grid_kv, int grid_q,
-                                     cudaStream_t stream) {
+static cudaError_t launch_split_pair(const BwdParams& p_kv, const BwdParams& p_q, int grid_kv,
+                                     int grid_q, cudaStream_t stream) {
   auto kkv = bsplit::dkdv_kernel<D, POLY8>;
   auto kq = bsplit::dq_kernel<D, POLY8>;
   const int s_kv = bsplit::CfgKV<D>::SMEM_BYTES, s_q = bsplit::CfgQ<D>::SMEM_BYTES;
@@ -1364,11 +1412,11 @@ static cudaError_t launch_split_pair(const BwdParams& p, int grid_kv, int grid_q
       cudaSuccess)
     return e;
   if (grid_kv > 0) {
-    kkv<<<grid_kv, bsplit::NUM_THREADS, s_kv, stream>>>(p);
+    kkv<<<grid_kv, bsplit::NUM_THREADS, s_kv, stream>>>(p_kv);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (grid_q > 0) {
-    kq<<<grid_q, bsplit::NUM_THREADS, s_q, stream>>>(p);
+    kq<<<grid_q, bsplit::NUM_THREADS, s_q, stream>>>(p_q);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   return cudaSuccess;
@@ -1428,17 +1476,31 @@ cudaError_t launch_bwd_split(const BwdParams& p, int d, int grid_kv, int grid_q,
                              cudaStream_t stream, int poly8) {
   if (d == 128) {
     switch (poly8) {
-      case 0: return launch_split_pair<128, 0>(p, grid_kv, grid_q, stream);
-      case 2: return launch_split_pair<128, 2>(p, grid_kv, grid_q, stream);
-      case 4: return launch_split_pair<128, 4>(p, grid_kv, grid_q, stream);
+      case 0: return launch_split_pair<128, 0>(p, p, grid_kv, grid_q, stream);
+      case 2: return launch_split_pair<128, 2>(p, p, grid_kv, grid_q, stream);
+      case 4: return launch_split_pair<128, 4>(p, p, grid_kv, grid_q, stream);
       default: return cudaErrorInvalidValue;
     }
   }
   if (d == 64) {
     switch (poly8) {
-      case 0: return launch_split_pair<64, 0>(p, grid_kv, grid_q, stream);
-      case 2: return launch_split_pair<64, 2>(p, grid_kv, grid_q, stream);
-      case 4: return launch_split_pair<64, 4>(p, grid_kv, grid_q, stream);
+      case 0: return launch_split_pair<64, 0>(p, p, grid_kv, grid_q, stream);
+      case 2: return launch_split_pair<64, 2>(p, p, grid_kv, grid_q, stream);
+      case 4: return launch_split_pair<64, 4>(p, p, grid_kv, grid_q, stream);
+      default: return cudaErrorInvalidValue;
+    }
+  }
+  if (d == 192) {
+    // dK/dV pass: 64-row Q/dO steps; dQ pass: 64-key K/V blocks
+    BwdParams p_kv = p, p_q = p;
+    p_kv.tm_q = p.tm_q2;
+    p_kv.tm_do = p.tm_do2;
+    p_q.tm_k = p.tm_k2;
+    p_q.tm_v = p.tm_v2;
+    switch (poly8) {
+      case 0: return launch_split_pair<192, 0>(p_kv, p_q, grid_kv, grid_q, stream);
+      case 2: return launch_split_pair<192, 2>(p_kv, p_q, grid_kv, grid_q, stream);
+      case 4: return launch_split_pair<192, 4>(p_kv, p_q, grid_kv, grid_q, stream);
       default: return cudaErrorInvalidValue;
     }
   }

@@ -88,7 +88,10 @@ struct BwdParams {
   CUtensorMap tm_q, tm_do;       // [T, Hq, d] views, 64-column boxes of 64 rows (one-pass
                                  // kernel) or 128 rows (two-pass kernels), 128B swizzle
   CUtensorMap tm_k, tm_v;        // [T, Hkv, d] views, 64-column x 128-row boxes
-  CUtensorMap tm_q2, tm_do2;     // 64-column x 64-row boxes (CTA-pair dK/dV pass only)
+  CUtensorMap tm_q2, tm_do2;     // 64-column x 64-row boxes (CTA-pair dK/dV pass; head dim
+                                 // 192: the dK/dV pass's 64-row steps)
+  CUtensorMap tm_k2, tm_v2;      // 64-column x 64-row boxes (head dim 192: the dQ pass's
+                                 // 64-key blocks)
   __nv_bfloat16 *dk, *dv;
   __nv_bfloat16* dq;             // bf16 [Tq, Hq, d] (written directly by the dQ pass)
   float* dq_acc;                 // fp32 [Tq, Hq, d] (one-pass kernel only; else nullptr)

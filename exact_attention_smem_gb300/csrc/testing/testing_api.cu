@@ -123,12 +123,12 @@ extern "C" int fa_test_wait_timeout(int* status_dev, double timeout_ms, void* st
 extern "C" int fa_sched_list(int kind, int B, const int* cu_seqlens_host, int Sq, int Sk,
                              int heads, int causal, int grid, int cta, int heads_per_group,
                              int* out, int max_units) {
-  if (kind < 0 || kind > 4 || B < 0 || Sq < 0 || Sk < 0 || heads <= 0 || grid <= 0 ||
+  if (kind < 0 || kind > 5 || B < 0 || Sq < 0 || Sk < 0 || heads <= 0 || grid <= 0 ||
       cta < 0 || cta >= grid || heads_per_group < 0 || max_units < 0 || (max_units > 0 && !out))
     return -1;
   // kind: 0 forward, 1 one-pass backward, 2 dK/dV pass, 3 dQ pass, 4 dK/dV pass on CTA pairs
-  static const int kUnit[5] = {256, 128, 128, 128, 256}, kInner[5] = {128, 64, 128, 128, 128},
-                   kList[5] = {0, 1, 1, 0, 1};
+  static const int kUnit[6] = {256, 128, 128, 128, 256, 128},
+                   kInner[6] = {128, 64, 128, 128, 128, 64}, kList[6] = {0, 1, 1, 0, 1, 0};
   SchedSpec s{cu_seqlens_host, B, Sq, Sk, heads, causal ? 1 : 0, kUnit[kind], kInner[kind],
               kList[kind], heads_per_group};
   if (heads_per_group == 0) {

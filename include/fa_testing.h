@@ -123,7 +123,9 @@ FA_TEST_API int fa_test_wait_timeout(int* status_dev, double timeout_ms, void* s
  * dK/dV pass of the two-pass backward (units of 128 keys, cost = query blocks
  * of 128), kind 3 = its dQ pass (units of 128 query rows, cost = KV blocks of
  * 128), kind 4 = the dK/dV pass on CTA pairs (units of 256 keys, cost =
- * query blocks of 128). cu_seqlens_host
+ * query blocks of 128), kind 5 = the dQ pass for head dim 192 (units of 128
+ * query rows, cost = KV blocks of 64; the dK/dV pass for head dim 192 is
+ * kind 1). cu_seqlens_host
  * is a HOST array (or NULL for dense B x Sq/Sk). Returns the number of units
  * (may exceed max_units; only max_units are written), or -1 on bad arguments.
  */

@@ -96,7 +96,7 @@ def test_backward_validation_and_workspace(lib):
     assert lib.fa_bwd(*args, FAKE, need - 1, None) == 5
     assert lib.fa_bwd(*args, FAKE + 16, need, None) == 5      # workspace must be 256-aligned
     assert lib.fa_bwd(*args, None, need, None) == 5
-    # head dims 192 and 256 have a forward only
+    # head dim 256 has a forward only
     big = [FAKE] * 9 + [2, 4, 4, 100, 100, 256, 1, 0.1, None]
     assert lib.fa_bwd(*big, FAKE, 1 << 30, None) == 2
     bad = [FAKE] * 8 + [None] + [2, 4, 4, 100, 100, 128, 1, 0.1, None]

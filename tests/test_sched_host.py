@@ -23,7 +23,7 @@ def _visible(i, j, ql, kl, causal):
 
 # kind -> (query-unit rows or key-unit rows, inner block rows, units over queries?)
 _KINDS = {0: (256, 128, True), 1: (128, 64, False), 2: (128, 128, False), 3: (128, 128, True),
-          4: (256, 128, False)}
+          4: (256, 128, False), 5: (128, 64, True)}
 
 
 def _brute_units(kind, B, cu, Sq, Sk, heads, causal):
@@ -67,6 +67,8 @@ CASES = [
     (3, 1, None, 1000, 300, 2, True), (3, 3, [0, 129, 385, 1000], 1000, 1000, 4, True),
     (4, 2, None, 600, 600, 3, True), (4, 1, None, 300, 1000, 2, True), (4, 1, None, 1000, 300, 2, True),
     (4, 4, [0, 1, 1, 700, 3000], 3000, 3000, 2, True),
+    (5, 2, None, 600, 600, 3, True), (5, 2, None, 600, 600, 3, False), (5, 1, None, 300, 1000, 2, True),
+    (5, 1, None, 1000, 300, 2, True), (5, 3, [0, 129, 385, 1000], 1000, 1000, 4, True),
 ]
 
 
