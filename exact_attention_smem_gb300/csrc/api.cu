@@ -288,8 +288,6 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const f
   Shape sh;
   int st = validate_common(ptrs, 9, B, Hq, Hkv, Sq, Sk, d, scale, cu_seqlens, &sh, cu_seqlens_k);
   if (st != FA_OK) return st;
-  if (d > 192)
-    return fail(FA_ERR_UNSUPPORTED, "backward head dim %d (supported: 64, 128, 192)", d);
   if (B == 0 || (sh.Tq == 0 && sh.Tk == 0)) return FA_OK;
   const size_t need = fa_bwd_workspace_bytes(B, Hq, Sq, d, sh.packed ? (int)sh.Tq : 0);
   if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
@@ -317,7 +315,7 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const f
   if ((st = encode_rows(&p.tm_v, sh.Tk > 0 ? v : q, sh.Tk > 0 ? Tk : Tq, sh.Tk > 0 ? Hkv : Hq,
                         d)) != FA_OK)
     return st;
-  if (mode == 2 || d == 192) {
+  if (mode == 2 || d > 128) {
     if ((st = encode_rows(&p.tm_q2, sh.Tq > 0 ? q : k, sh.Tq > 0 ? Tq : Tk, sh.Tq > 0 ? Hq : Hkv,
                           d, 64)) != FA_OK)
       return st;
@@ -325,12 +323,14 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const f
                           sh.Tq > 0 ? Hq : Hkv, d, 64)) != FA_OK)
       return st;
   }
-  if (d == 192) {
+  if (d > 128) {
+    // the dQ pass's K/V blocks: 64 keys at head dim 192, 32 at 256
+    const int kbox = d > 192 ? 32 : 64;
     if ((st = encode_rows(&p.tm_k2, sh.Tk > 0 ? k : q, sh.Tk > 0 ? Tk : Tq, sh.Tk > 0 ? Hkv : Hq,
-                          d, 64)) != FA_OK)
+                          d, kbox)) != FA_OK)
       return st;
     if ((st = encode_rows(&p.tm_v2, sh.Tk > 0 ? v : q, sh.Tk > 0 ? Tk : Tq, sh.Tk > 0 ? Hkv : Hq,
-                          d, 64)) != FA_OK)
+                          d, kbox)) != FA_OK)
       return st;
   }
   auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
@@ -381,8 +381,10 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const f
   aux.lse_seqstride = sh.packed ? 0 : (long long)Hq * Sq;
   aux.dq = static_cast<__nv_bfloat16*>(dq);
   int grid = kn.grid_override > 0 ? kn.grid_override : di->sms;
+  // dK/dV units per KV head: one per 128-key block (two at head dim 256, one
+  // per 128-column half of dV and dK)
   const long long kv_units_per_head =
-      sh.packed ? (sh.Tk + 127) / 128 + B : (long long)B * ((Sk + 127) / 128);
+      (sh.packed ? (sh.Tk + 127) / 128 + B : (long long)B * ((Sk + 127) / 128)) * (d > 192 ? 2 : 1);
   // Head groups keep the data concurrently running units share in L2. Packed
   // layouts use one group in the two-pass form: their scheduler walks the
   // list one (cost level, sequence) group at a time, so head groups of one

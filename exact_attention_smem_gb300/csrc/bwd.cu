@@ -701,7 +701,7 @@ static cudaError_t launch_main(const BwdParams& p, int grid, cudaStream_t stream
 cudaError_t launch_bwd(const BwdParams& p, const BwdAux& aux, int d, int grid, int grid_q,
                        cudaStream_t stream, int poly8, int mode) {
   if (mode == 0 && d != 128) return cudaErrorNotSupported;
-  if (d != 64 && d != 128 && d != 192) return cudaErrorNotSupported;
+  if (d != 64 && d != 128 && d != 192 && d != 256) return cudaErrorNotSupported;
   const long long rows = (long long)p.total_q * p.Hq;
   if (rows > 0) {
     const int blocks = (int)((rows + 7) / 8 < 65535 * 8 ? (rows + 7) / 8 : 65535 * 8);
@@ -709,6 +709,8 @@ cudaError_t launch_bwd(const BwdParams& p, const BwdAux& aux, int d, int grid, i
       bwdk::bwd_pre_kernel<128><<<blocks, 256, 0, stream>>>(p, aux);
     else if (d == 192)
       bwdk::bwd_pre_kernel<192><<<blocks, 256, 0, stream>>>(p, aux);
+    else if (d == 256)
+      bwdk::bwd_pre_kernel<256><<<blocks, 256, 0, stream>>>(p, aux);
     else
       bwdk::bwd_pre_kernel<64><<<blocks, 256, 0, stream>>>(p, aux);
     cudaError_t e = cudaGetLastError();

@@ -64,12 +64,20 @@ struct Tile {
   static constexpr int BYTES = CHUNKS * CHUNK; // one tile of ROWS rows
 };
 
-// Head dims up to 128 step over 128 query rows (dK/dV pass) and 128 keys (dQ
-// pass). Head dim 192 steps over 64: the dK/dV pass then holds dV 192 + dK 192
-// + S^T 64 + dP^T 64 = 512 TMEM columns and ~216 KB of tiles, the dQ pass
-// S 2 x 64 + dP 64 + dQ 192 = 384 columns and ~216 KB.
+// Step sizes by head dim. Up to 128: 128 query rows per dK/dV step, 128 keys
+// per dQ block. 192: 64 and 64 (dK/dV pass: dV 192 + dK 192 + S^T 64 + dP^T 64
+// = 512 TMEM columns, ~216 KB of tiles; dQ pass: S 2 x 64 + dP 64 + dQ 192
+// columns, ~216 KB). 256: dV and dK alone would fill TMEM, so a dK/dV unit
+// accumulates one 128-column half of them (S^T and dP^T are recomputed for
+// each half) over 64-row steps, with 64 KB K and V tiles, two Q slots and one
+// dO slot (~226 KB); the dQ pass takes 32-key blocks (S 2 x 32 + dP 32 + dQ
+// 256 columns; Q and dO 64 KB each, five 16 KB K/V slots).
 template <int D>
-constexpr int step_rows() { return D > 128 ? 64 : 128; }
+constexpr int kv_step_rows() { return D > 128 ? 64 : 128; }
+template <int D>
+constexpr int q_block_keys() { return D > 192 ? 32 : D > 128 ? 64 : 128; }
+template <int D>
+constexpr int acc_cols() { return D > 192 ? 128 : D; }   // dV/dK columns per dK/dV unit
 
 // dK/dV pass layout. Q slots are held from S^T(i) to dK(i), the longest span,
 // so Q gets three slots and dO two. The -LSE*log2(e) and -D values of a
@@ -80,9 +88,11 @@ constexpr int step_rows() { return D > 128 ? 64 : 128; }
 template <int D>
 struct CfgKV {
   using T = Tile<D>;
-  static constexpr int BMS = step_rows<D>();          // query rows per step
+  static constexpr int BMS = kv_step_rows<D>();       // query rows per step
+  static constexpr int DA = acc_cols<D>();             // accumulator columns (dV, dK)
+  static constexpr int HALVES = D / DA;                // units per key block and KV head
   using QT = Tile<D, BMS>;                             // a Q or dO step tile
-  static constexpr int NQ = 3, NDO = 2, NLD = 2;
+  static constexpr int NQ = D > 192 ? 2 : 3, NDO = D > 192 ? 1 : 2, NLD = 2;
   static constexpr int LD_BYTES = 2 * BMS * 4;        // [-LSE*log2e x BMS][-D x BMS]
   static constexpr int K_OFF = 0, V_OFF = T::BYTES, Q_OFF = 2 * T::BYTES,
                        DO_OFF = Q_OFF + NQ * QT::BYTES, LD_OFF = DO_OFF + NDO * QT::BYTES,
@@ -97,11 +107,11 @@ struct CfgKV {
   static constexpr int CU_OFF = MISC_OFF + 16;
   static constexpr int SMEM_BYTES = CU_OFF + (MAX_SEQ_SMEM + 1) * 4;
   static_assert(SMEM_BYTES <= SMEM_LIMIT, "dK/dV pass shared memory");
-  // TMEM: dV [0,D), dK [D,2D), S^T/P^T [2D,2D+BMS), dP^T/dS^T [2D+BMS,2D+2BMS)
-  static constexpr uint32_t TM_DV = 0, TM_DK = D, TM_SB = 2 * D, TM_DB = 2 * D + BMS;
-  static_assert(2 * D + 2 * BMS <= 512, "TMEM columns");
+  // TMEM: dV [0,DA), dK [DA,2DA), S^T/P^T [2DA,2DA+BMS), dP^T/dS^T [2DA+BMS,2DA+2BMS)
+  static constexpr uint32_t TM_DV = 0, TM_DK = DA, TM_SB = 2 * DA, TM_DB = 2 * DA + BMS;
+  static_assert(2 * DA + 2 * BMS <= 512, "TMEM columns");
   static constexpr uint32_t IDESC_S = idesc_bf16(128, BMS, false, false);  // S^T, dP^T
-  static constexpr uint32_t IDESC_ACC = idesc_bf16(128, D, false, true);   // dV, dK
+  static constexpr uint32_t IDESC_ACC = idesc_bf16(128, DA, false, true);  // dV, dK
 };
 
 // dQ pass layout: Q and dO of the unit, and a ring of K/V tiles in the order
@@ -110,7 +120,7 @@ struct CfgKV {
 template <int D>
 struct CfgQ {
   using T = Tile<D>;
-  static constexpr int BNS = step_rows<D>();          // keys per block
+  static constexpr int BNS = q_block_keys<D>();       // keys per block
   using KT = Tile<D, BNS>;                             // a K or V block tile
   static constexpr int NKV = 5;
   static constexpr int Q_OFF = 0, DO_OFF = T::BYTES, KV_OFF = 2 * T::BYTES,
@@ -179,31 +189,33 @@ __device__ __forceinline__ uint32_t pack2(uint64_t v) {
 }
 
 // COLS fp32 values (COLS/2 pairs) -> bf16 pairs stored over the first COLS/2 columns.
-template <int COLS = 64>
-__device__ __forceinline__ void store_bf16_half(uint32_t taddr, const uint64_t (&v2)[COLS / 2]) {
-  uint32_t pk[COLS / 2];
-#pragma unroll
-  for (int c = 0; c < COLS / 2; ++c) pk[c] = pack2(v2[c]);
-  if constexpr (COLS == 64)
-    tmem_st32(taddr, pk);
-  else
-    tmem_st16(taddr, pk);
-}
-
-// TMEM row loads of a warpgroup's COLS columns (64 or 32).
+// TMEM row loads of a warpgroup's COLS columns (64, 32 or 16), and stores of
+// COLS/2 columns (bf16 pairs over the first half of those columns).
 template <int COLS>
 __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[COLS]) {
   if constexpr (COLS == 64)
     tmem_ld64(taddr, r);
-  else
+  else if constexpr (COLS == 32)
     tmem_ld32(taddr, r);
+  else
+    tmem_ld16(taddr, r);
 }
 template <int COLS>
 __device__ __forceinline__ void tmem_st_half(uint32_t taddr, const uint32_t* r) {
   if constexpr (COLS == 64)
     tmem_st32(taddr, r);
-  else
+  else if constexpr (COLS == 32)
     tmem_st16(taddr, r);
+  else
+    tmem_st8(taddr, r);
+}
+
+template <int COLS = 64>
+__device__ __forceinline__ void store_bf16_half(uint32_t taddr, const uint64_t (&v2)[COLS / 2]) {
+  uint32_t pk[COLS / 2];
+#pragma unroll
+  for (int c = 0; c < COLS / 2; ++c) pk[c] = pack2(v2[c]);
+  tmem_st_half<COLS>(taddr, pk);
 }
 
 struct StepInfo {
@@ -274,6 +286,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dkdv_kernel(const __grid_const
   using QT = typename C::QT;
   constexpr int BMS = C::BMS;                           // query rows per step
   constexpr int COLS = BMS / 2;                         // score columns per warpgroup
+  constexpr int DA = C::DA, HALVES = C::HALVES;         // unit head = KV head * HALVES + half
   extern __shared__ __align__(1024) uint8_t smem_al[];
   uint32_t base;                                        // opaque to the compiler: checked, not assumed
   asm volatile("{\n\t.reg .u64 t;\n\tcvta.to.shared.u64 t, %1;\n\tcvt.u32.u64 %0, t;\n\t}"
@@ -337,8 +350,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dkdv_kernel(const __grid_const
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  const SchedSpec spec{cu_in_smem ? cu_s : p.cu, p.nseq, p.Sq, p.Sk, p.Hkv, p.causal, BN, BMS,
-                       1, p.hblock, nullptr, p.k_off};
+  const SchedSpec spec{cu_in_smem ? cu_s : p.cu, p.nseq, p.Sq, p.Sk, p.Hkv * HALVES, p.causal,
+                       BN, BMS, 1, p.hblock * HALVES, nullptr, p.k_off};
   const WaitCtl wc{p.err, abort_flag, p.timeout_ns};
   const int G = gridDim.x;
   const int cta = blockIdx.x;
@@ -362,9 +375,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dkdv_kernel(const __grid_const
         if (u.cost == 0) continue;
         const int n = u.cost * group;
         const int m_first = first_qblock<BMS>(u, p.causal);
-        // The first two steps' Q/dO need only free ring slots: they go out
-        // before the wait for the previous unit to release K/V.
-        const int lead = n < 2 ? n : 2;
+        // The first steps' Q/dO (as many as both rings hold) need only free
+        // ring slots: they go out before the wait for the previous unit to
+        // release K/V. More would wait for this unit's own dV/dK, which need
+        // its K/V.
+        constexpr int LEAD = C::NQ < C::NDO ? C::NQ : C::NDO;
+        const int lead = n < LEAD ? n : LEAD;
         for (int i = 0; i <= n; ++i) {
           if (i == lead) {
             if (u_it > 0) {
@@ -375,16 +391,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dkdv_kernel(const __grid_const
             const int krow = u.k_start + u.m * BN;
             for (int c = 0; c < T::CHUNKS; ++c) {
               tma_load_3d(base + C::K_OFF + c * T::CHUNK, &p.tm_k, BAR(C::B_KVFULL), c * 64,
-                          u.head, krow);
+                          u.head / HALVES, krow);
               tma_load_3d(base + C::V_OFF + c * T::CHUNK, &p.tm_v, BAR(C::B_KVFULL), c * 64,
-                          u.head, krow);
+                          u.head / HALVES, krow);
             }
             ++u_it;
           }
           if (i == n) break;
           // Q(s) goes into slot s % NQ once dK(s - NQ) is done, dO(s) into slot
           // s % NDO once dV(s - NDO) is done.
-          const StepInfo st = step_of(i, u.cost, m_first, u.head, group);
+          const StepInfo st = step_of(i, u.cost, m_first, u.head / HALVES, group);
           const int row = u.q_start + st.m * BMS;
           const int sq = nq % C::NQ, sd = nd % C::NDO;
           if (nq >= (uint32_t)C::NQ) {
@@ -445,11 +461,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dkdv_kernel(const __grid_const
       const uint32_t tSB = tmem + C::TM_SB, tDB = tmem + C::TM_DB;
       auto qslot = [&](uint32_t s) { return base + C::Q_OFF + (s % C::NQ) * QT::BYTES; };
       auto dslot = [&](uint32_t s) { return base + C::DO_OFF + (s % C::NDO) * QT::BYTES; };
+      uint32_t half_off = 0;                              // this unit's dV/dK columns in Q, dO
       for (int k = 0; ok; ++k) {
         Unit u;
         if (!w.seek(snake_index(k, G, cta), u)) break;
         if (u.cost == 0) continue;
         const int n = u.cost * group;
+        half_off = (uint32_t)(u.head % HALVES) * (DA / 64) * QT::CHUNK;
         // Per step two sync points, each probing everything it needs at once
         // (every memory access of this thread waits for the MMAs it has
         // queued, so the probes of a sync point go out together):
@@ -483,7 +501,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dkdv_kernel(const __grid_const
           if (!ok) break;
           FA_TRACE(TR_KV_A, it);
           tc_fence_after();
-          mma_acc<D, C::IDESC_ACC, BMS>(tmem + C::TM_DV, tSB, dslot(it), i > 0);
+          mma_acc<D, C::IDESC_ACC, BMS>(tmem + C::TM_DV, tSB, dslot(it) + half_off, i > 0);
           tc_commit(BAR(C::B_DOEMPTY + it % C::NDO));
           if (more) {
             mma_abt<D, C::IDESC_S, BMS>(tSB, kt, qslot(it1));
@@ -497,7 +515,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dkdv_kernel(const __grid_const
           if (!ok) break;
           FA_TRACE(TR_KV_B, it);
           tc_fence_after();
-          mma_acc<D, C::IDESC_ACC, BMS>(tmem + C::TM_DK, tDB, qslot(it), i > 0);
+          mma_acc<D, C::IDESC_ACC, BMS>(tmem + C::TM_DK, tDB, qslot(it) + half_off, i > 0);
           tc_commit(BAR(C::B_QEMPTY + it % C::NQ));
           if (more) {
             mma_abt<D, C::IDESC_S, BMS>(tDB, vt, dslot(it1));
@@ -534,16 +552,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dkdv_kernel(const __grid_const
     for (int k = 0; ok; ++k) {
       Unit u;
       if (!w.seek(snake_index(k, G, cta), u)) break;
-      const int g = u.head;
+      const int g = u.head / HALVES;
       const int key = u.m * BN + j;                       // key index within the sequence
       const bool key_ok = key < u.k_len;
       const long long krow = ((long long)u.k_start + key) * p.Hkv + g;
-      __nv_bfloat16* dk_row = p.dk + krow * D + wg * (D / 2);
-      __nv_bfloat16* dv_row = p.dv + krow * D + wg * (D / 2);
+      const int col0 = (u.head % HALVES) * DA + wg * (DA / 2);
+      __nv_bfloat16* dk_row = p.dk + krow * D + col0;
+      __nv_bfloat16* dv_row = p.dv + krow * D + col0;
       if (u.cost == 0) {                                   // keys no query sees
         if (key_ok) {
-          zero_half<D>(dk_row);
-          zero_half<D>(dv_row);
+          zero_half<DA>(dk_row);
+          zero_half<DA>(dv_row);
         }
         continue;
       }
@@ -629,8 +648,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dkdv_kernel(const __grid_const
       if (!ok) break;
       tc_fence_after();
       ++u_it;
-      store_acc_half<D>(tmem + lane_off + C::TM_DV + wg * (D / 2), dv_row, 1.0f, key_ok);
-      store_acc_half<D>(tmem + lane_off + C::TM_DK + wg * (D / 2), dk_row, p.scale, key_ok);
+      store_acc_half<DA>(tmem + lane_off + C::TM_DV + wg * (DA / 2), dv_row, 1.0f, key_ok);
+      store_acc_half<DA>(tmem + lane_off + C::TM_DK + wg * (DA / 2), dk_row, p.scale, key_ok);
       tc_fence_before();
     }
   }
@@ -1490,13 +1509,21 @@ cudaError_t launch_bwd_split(const BwdParams& p, int d, int grid_kv, int grid_q,
       default: return cudaErrorInvalidValue;
     }
   }
-  if (d == 192) {
-    // dK/dV pass: 64-row Q/dO steps; dQ pass: 64-key K/V blocks
+  if (d == 192 || d == 256) {
+    // dK/dV pass: 64-row Q/dO steps; dQ pass: 64-key (192) or 32-key (256) K/V blocks
     BwdParams p_kv = p, p_q = p;
     p_kv.tm_q = p.tm_q2;
     p_kv.tm_do = p.tm_do2;
     p_q.tm_k = p.tm_k2;
     p_q.tm_v = p.tm_v2;
+    if (d == 256) {
+      switch (poly8) {
+        case 0: return launch_split_pair<256, 0>(p_kv, p_q, grid_kv, grid_q, stream);
+        case 2: return launch_split_pair<256, 2>(p_kv, p_q, grid_kv, grid_q, stream);
+        case 4: return launch_split_pair<256, 4>(p_kv, p_q, grid_kv, grid_q, stream);
+        default: return cudaErrorInvalidValue;
+      }
+    }
     switch (poly8) {
       case 0: return launch_split_pair<192, 0>(p_kv, p_q, grid_kv, grid_q, stream);
       case 2: return launch_split_pair<192, 2>(p_kv, p_q, grid_kv, grid_q, stream);

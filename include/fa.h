@@ -26,8 +26,7 @@
  *     [T][Hkv][d]; lse is fp32 [Hq][T]. Sequence i owns rows
  *     [cu_seqlens[i], cu_seqlens[i+1]) of every tensor (self-attention: one
  *     boundary list for queries and keys).
- *   - d (head dimension) is 64, 128 or 192 (the forward and fa_merge also take
- *     256); scale must be finite and > 0.
+ *   - d (head dimension) is 64, 128, 192 or 256; scale must be finite and > 0.
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
  *     stream). FA_OK means "validated and enqueued". The library allocates no
  *     memory on any call and keeps no per-call state; the caller owns all
@@ -121,8 +120,10 @@ FA_API size_t fa_bwd_workspace_bytes(int B, int Hq, int Sq, int d, int total_q);
 /*
  * Backward: dq, dk, dv (bf16) from q, k, v, o, lse (as written by fa_fwd) and
  * dout. dk/dv of a KV head are summed over the query heads of its group.
- * Head dim 64, 128 or 192 (FA_ERR_UNSUPPORTED for 256); with 192 the passes
- * step over 64 query rows / 64 keys instead of 128.
+ * Head dim 64, 128, 192 or 256. With 192 the passes step over 64 query rows /
+ * 64 keys instead of 128; with 256 each dK/dV unit accumulates one 128-column
+ * half of dV and dK (S^T and dP^T recomputed per half) and the dQ pass steps
+ * over 32 keys.
  * Runs three kernels on `stream`: a preprocess (the row terms -D and
  * -LSE*log2e), a dK/dV pass over key blocks and a dQ pass over query blocks.
  * Every output element is written by one CTA with a fixed summation order (no

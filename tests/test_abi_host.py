@@ -96,8 +96,8 @@ def test_backward_validation_and_workspace(lib):
     assert lib.fa_bwd(*args, FAKE, need - 1, None) == 5
     assert lib.fa_bwd(*args, FAKE + 16, need, None) == 5      # workspace must be 256-aligned
     assert lib.fa_bwd(*args, None, need, None) == 5
-    # head dim 256 has a forward only
-    big = [FAKE] * 9 + [2, 4, 4, 100, 100, 256, 1, 0.1, None]
+    # head dims outside {64, 128, 192, 256} are rejected before any device work
+    big = [FAKE] * 9 + [2, 4, 4, 100, 100, 320, 1, 0.1, None]
     assert lib.fa_bwd(*big, FAKE, 1 << 30, None) == 2
     bad = [FAKE] * 8 + [None] + [2, 4, 4, 100, 100, 128, 1, 0.1, None]
     assert lib.fa_bwd(*bad, FAKE, need, None) == 1

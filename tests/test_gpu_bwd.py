@@ -163,36 +163,40 @@ def test_head_dim_64_varlen(bwd_mode):
     _check(x, True, 0.125, cu=x.cu_seqlens)
 
 
+@pytest.mark.parametrize("d", [192, 256])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("S", [1, 63, 64, 65, 129, 300, 700])
-def test_head_dim_192(S, causal, bwd_mode):
-    """Head dim 192: the dK/dV pass steps over 64 query rows and the dQ pass
-    over 64-key blocks (TMEM: dV 192 + dK 192 + S^T 64 + dP^T 64 columns). The
-    CTA-pair form is head dim 128 only (mode 2 runs the two-pass form), the
-    one-pass form too (mode 0 is rejected)."""
-    x = random_inputs(B=2, Hq=2, Hkv=2, Sq=S, Sk=S, d=192, seed=600 + S, device="cuda")
+def test_head_dims_192_256(S, causal, d, bwd_mode):
+    """Head dims 192 and 256: the dK/dV pass steps over 64 query rows (at 256
+    each unit accumulates one 128-column half of dV and dK, recomputing S^T and
+    dP^T per half) and the dQ pass over 64-key (192) or 32-key (256) blocks.
+    The CTA-pair form is head dim 128 only (mode 2 runs the two-pass form),
+    the one-pass form too (mode 0 is rejected)."""
+    x = random_inputs(B=2, Hq=2, Hkv=2, Sq=S, Sk=S, d=d, seed=600 + S + d, device="cuda")
     if bwd_mode == 0:
         with pytest.raises(fa.FAError) as e:
-            _run(x, causal, 192 ** -0.5)
+            _run(x, causal, d ** -0.5)
         assert e.value.status == 2
     else:
-        _check(x, causal, 192 ** -0.5)
+        _check(x, causal, d ** -0.5)
 
 
+@pytest.mark.parametrize("d", [192, 256])
 @pytest.mark.parametrize("Sq,Sk", [(100, 300), (300, 100)])
-def test_head_dim_192_sq_ne_sk(Sq, Sk, bwd_mode):
+def test_head_dims_192_256_sq_ne_sk(Sq, Sk, d, bwd_mode):
     if bwd_mode == 0:
         pytest.skip("the one-pass form supports d=128 only")
-    x = random_inputs(B=1, Hq=2, Hkv=2, Sq=Sq, Sk=Sk, d=192, seed=610 + Sq, device="cuda")
-    _check(x, True, 192 ** -0.5)
+    x = random_inputs(B=1, Hq=2, Hkv=2, Sq=Sq, Sk=Sk, d=d, seed=610 + Sq + d, device="cuda")
+    _check(x, True, d ** -0.5)
 
 
-def test_head_dim_192_gqa_and_packed(bwd_mode):
+@pytest.mark.parametrize("d", [192, 256])
+def test_head_dims_192_256_gqa_and_packed(d, bwd_mode):
     if bwd_mode == 0:
         pytest.skip("the one-pass form supports d=128 only")
-    x = random_inputs(B=2, Hq=6, Hkv=2, Sq=333, Sk=333, d=192, seed=620, device="cuda")
-    _check(x, True, 192 ** -0.5)
-    x = random_inputs(B=None, Hq=4, Hkv=2, Sq=None, Sk=None, d=192, seed=621,
+    x = random_inputs(B=2, Hq=6, Hkv=2, Sq=333, Sk=333, d=d, seed=620 + d, device="cuda")
+    _check(x, True, d ** -0.5)
+    x = random_inputs(B=None, Hq=4, Hkv=2, Sq=None, Sk=None, d=d, seed=621 + d,
                       lengths=[1, 63, 0, 200, 129, 64], device="cuda")
-    _check(x, True, 192 ** -0.5, cu=x.cu_seqlens)
-    _check(x, False, 192 ** -0.5, cu=x.cu_seqlens)
+    _check(x, True, d ** -0.5, cu=x.cu_seqlens)
+    _check(x, False, d ** -0.5, cu=x.cu_seqlens)
