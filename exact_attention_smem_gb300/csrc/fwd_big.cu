@@ -395,7 +395,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) fwd_big_kernel(const __grid_co
         const float msub = m_ref == -INFINITY ? 0.f : m_ref;
         const uint64_t sl2x2 = f2pack(sl2, sl2), negm2 = f2pack(-msub, -msub);
         uint64_t la2[2] = {f2pack(0.f, 0.f), f2pack(0.f, 0.f)};
-        uint64_t lb2[2] = {f2pack(0.f, 0.f), f2pack(0.f, 0.f)};
+        float lb4[4] = {0.f, 0.f, 0.f, 0.f};
         uint32_t pk[32];
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
@@ -405,14 +405,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) fwd_big_kernel(const __grid_co
           const float p1 = ((2 * c + 1) & 7) < POLY8 ? exp2_poly(x1) : ex2_mufu(x1);
           const uint32_t pb = pack_bf16x2(p0, p1);
           la2[c & 1] = fadd2(la2[c & 1], f2pack(p0, p1));
-          lb2[c & 1] = fadd2(lb2[c & 1], f2pack(__uint_as_float(pb << 16),
-                                                __uint_as_float(pb & 0xffff0000u)));
+          add_bf16x2_f32(lb4[2 * (c & 1)], lb4[2 * (c & 1) + 1], pb);
           pk[c] = pb;
         }
         {
           float a0, a1, b0, b1;
           f2unpack(fadd2(la2[0], la2[1]), a0, a1);
-          f2unpack(fadd2(lb2[0], lb2[1]), b0, b1);
+          b0 = lb4[0] + lb4[2];
+          b1 = lb4[1] + lb4[3];
           l += a0 + a1;
           lp += b0 + b1;
         }

@@ -525,6 +525,16 @@ __device__ __forceinline__ void tmem_st_wait() {
 #undef FA_Q8
 #undef FA_S8
 
+// a0 += (float)lo(pb), a1 += (float)hi(pb) for a pair of bf16 values packed
+// in pb (mixed-precision adds: the bf16 -> f32 conversion is exact and folded
+// into the add, no unpacking).
+__device__ __forceinline__ void add_bf16x2_f32(float& a0, float& a1, uint32_t pb) {
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+      "add.rn.f32.bf16 %0, lo, %0;\n\tadd.rn.f32.bf16 %1, hi, %1;\n\t}"
+      : "+f"(a0), "+f"(a1)
+      : "r"(pb));
+}
+
 // Named-barrier rendezvous of `count` threads (whole warps) that also ANDs a
 // predicate across them. Unlike any memory access, it does not wait behind the
 // tcgen05 instructions an MMA-issuing warp has queued, so the MMA warp learns
