@@ -390,7 +390,14 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const f
   // list one (cost level, sequence) group at a time, so head groups of one
   // head would multiply that walk by the head count (dense layouts seek
   // directly and keep the L2-sized groups).
-  p.hblock = (mode != 0 && sh.packed) ? Hkv : pick_hblock(kv_units_per_head, Hkv, grid);
+  // When Q and dO of all heads fit in L2 a dense layout also takes one group:
+  // the L2-sized groups buy nothing there and deal the LPT list in lumps (mha
+  // S=2048: per-CTA cost max/mean 1.24 against 1.01 with one group).
+  const double qdo_bytes = (double)sh.Tq * Hq * d * 4.0;
+  p.hblock = (mode != 0 && (sh.packed || qdo_bytes <= 96e6))
+                 ? Hkv
+                 : pick_hblock(kv_units_per_head, Hkv, grid);
+  if (kn.bwd_hblock > 0) p.hblock = kn.bwd_hblock < Hkv ? kn.bwd_hblock : Hkv;
   // dQ units (128 query rows of one head) stream the K/V of their head. When
   // the K/V of all heads would not stay in L2 (GB300: 129 MB) a dense layout
   // takes the fewest heads whose units cover the grid twice (one group over
@@ -516,6 +523,9 @@ extern "C" int fa_debug_set(const char* key, double value) {
   } else if (!strcmp(key, "fwd_hblock")) {
     if (!(value >= 0.0 && value <= 65536.0)) return fail(FA_ERR_INVALID_ARG, "fwd_hblock");
     g_knobs.fwd_hblock = (int)value;
+  } else if (!strcmp(key, "bwd_hblock")) {
+    if (!(value >= 0.0 && value <= 65536.0)) return fail(FA_ERR_INVALID_ARG, "bwd_hblock");
+    g_knobs.bwd_hblock = (int)value;
   } else if (!strcmp(key, "timeout_ms")) {
     if (!(value >= 1.0 && value <= 60000.0)) return fail(FA_ERR_INVALID_ARG, "timeout_ms");
     g_knobs.timeout_ns = (long long)(value * 1e6);

@@ -237,6 +237,7 @@ FA_API int fa_get_device_error(int* code, int clear);
  *                dK/dV pass on CTA pairs (cta_group::2, head dim 128), 0 one
  *                pass with fp32 dQ atomics and a convert pass (head dim 128)
  *   "fwd_hblock" forward heads per scheduler group (0 = all heads, default)
+ *   "bwd_hblock" dK/dV pass: KV heads per scheduler group (0 = automatic)
  * Returns FA_OK or FA_ERR_INVALID_ARG. Process-wide; not thread-safe with
  * concurrent launches.
  */
