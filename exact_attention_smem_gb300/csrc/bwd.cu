@@ -597,50 +597,65 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_kernel(const __grid_consta
 }
 
 // -D and -LSE*log2e into the padded row arrays; zero the dQ accumulator when
-// there is one (one-pass kernel). One warp per (row, head).
+// there is one (one-pass kernel). Each (row, head) of O and dO is read by a
+// group of lanes, 16 bytes (8 values) per lane: D/8 lanes, rounded up to a
+// power of two, so a warp covers 4, 2, 1 or 1 rows (D = 64, 128, 192, 256).
+template <int D>
+struct PreGroup {
+  static constexpr int LANES = D / 8;                       // lanes with data
+  static constexpr int G = LANES <= 8 ? 8 : LANES <= 16 ? 16 : 32;
+  static constexpr int RPW = 32 / G;                        // rows per warp
+};
+
 template <int D>
 __global__ void bwd_pre_kernel(BwdParams p, BwdAux aux) {
+  using PG = PreGroup<D>;
   const long long nrows = (long long)p.total_q * p.Hq;
   const int lane = threadIdx.x & 31;
+  const int gl = lane & (PG::G - 1);                         // lane within the row's group
+  const int c = gl * 8;                                      // this lane's 8 columns
   const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
-  for (long long r = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < nrows;
-       r += warps) {
-    const int t = (int)(r / p.Hq), h = (int)(r % p.Hq);
-    int seq, q_start;
-    if (p.cu) {
-      int lo = 0, hi = p.nseq;                 // last seq with cu[seq] <= t (non-empty)
-      while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (p.cu[mid] <= t) lo = mid; else hi = mid;
-      }
-      seq = lo;
-      q_start = p.cu[lo];
-    } else {
-      seq = t / p.Sq;
-      q_start = seq * p.Sq;
-    }
-    const __nv_bfloat16* orow = aux.o + ((long long)t * p.Hq + h) * D;
-    const __nv_bfloat16* grow = aux.dout + ((long long)t * p.Hq + h) * D;
+  for (long long r0 = ((long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * PG::RPW;
+       r0 < nrows; r0 += warps * PG::RPW) {
+    const long long r = r0 + lane / PG::G;
+    const bool row_ok = r < nrows;
     float acc = 0.f;
-    for (int c = lane * 4; c < D; c += 128) {
-      const uint2 ov = *reinterpret_cast<const uint2*>(orow + c);
-      const uint2 gv = *reinterpret_cast<const uint2*>(grow + c);
+    if (row_ok && c < D) {
+      const uint4 ov = *reinterpret_cast<const uint4*>(aux.o + r * D + c);
+      const uint4 gv = *reinterpret_cast<const uint4*>(aux.dout + r * D + c);
       const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
       const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&gv);
-      for (int e = 0; e < 2; ++e) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
         const float2 of = __bfloat1622float2(o2[e]);
         const float2 gf = __bfloat1622float2(g2[e]);
         acc = fmaf(of.x, gf.x, acc);
         acc = fmaf(of.y, gf.y, acc);
       }
     }
-    for (int sh = 16; sh > 0; sh >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, sh);
-    if (p.dq_acc) {
-      float* zr = p.dq_acc + ((long long)t * p.Hq + h) * D;
-      for (int c = lane * 4; c < D; c += 128)
-        *reinterpret_cast<float4*>(zr + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int sh = PG::G / 2; sh > 0; sh >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, sh);
+    if (!row_ok) continue;
+    if (p.dq_acc && c < D) {
+      float4* zr = reinterpret_cast<float4*>(p.dq_acc + r * D + c);
+      zr[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+      zr[1] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    if (lane == 0) {
+    if (gl == 0) {
+      const int t = (int)(r / p.Hq), h = (int)(r % p.Hq);
+      int seq, q_start;
+      if (p.cu) {
+        int lo = 0, hi = p.nseq;               // last seq with cu[seq] <= t (non-empty)
+        while (hi - lo > 1) {
+          const int mid = (lo + hi) >> 1;
+          if (p.cu[mid] <= t) lo = mid; else hi = mid;
+        }
+        seq = lo;
+        q_start = p.cu[lo];
+      } else {
+        seq = t / p.Sq;
+        q_start = seq * p.Sq;
+      }
       const int row = t - q_start;
       const float lse = aux.lse[(p.cu ? 0ll : (long long)seq * aux.lse_seqstride) +
                                 (long long)h * aux.lse_hstride + (p.cu ? t : row)];
@@ -704,15 +719,19 @@ cudaError_t launch_bwd(const BwdParams& p, const BwdAux& aux, int d, int grid, i
   if (d != 64 && d != 128 && d != 192 && d != 256) return cudaErrorNotSupported;
   const long long rows = (long long)p.total_q * p.Hq;
   if (rows > 0) {
-    const int blocks = (int)((rows + 7) / 8 < 65535 * 8 ? (rows + 7) / 8 : 65535 * 8);
+    // 8 warps per block, RPW rows per warp
+    auto blocks_for = [&](int rpw) {
+      const long long b = (rows + 8ll * rpw - 1) / (8ll * rpw);
+      return (int)(b < 65535ll * 8 ? b : 65535ll * 8);
+    };
     if (d == 128)
-      bwdk::bwd_pre_kernel<128><<<blocks, 256, 0, stream>>>(p, aux);
+      bwdk::bwd_pre_kernel<128><<<blocks_for(bwdk::PreGroup<128>::RPW), 256, 0, stream>>>(p, aux);
     else if (d == 192)
-      bwdk::bwd_pre_kernel<192><<<blocks, 256, 0, stream>>>(p, aux);
+      bwdk::bwd_pre_kernel<192><<<blocks_for(bwdk::PreGroup<192>::RPW), 256, 0, stream>>>(p, aux);
     else if (d == 256)
-      bwdk::bwd_pre_kernel<256><<<blocks, 256, 0, stream>>>(p, aux);
+      bwdk::bwd_pre_kernel<256><<<blocks_for(bwdk::PreGroup<256>::RPW), 256, 0, stream>>>(p, aux);
     else
-      bwdk::bwd_pre_kernel<64><<<blocks, 256, 0, stream>>>(p, aux);
+      bwdk::bwd_pre_kernel<64><<<blocks_for(bwdk::PreGroup<64>::RPW), 256, 0, stream>>>(p, aux);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if (p.nseq > 0) {
