@@ -393,10 +393,13 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const f
   // When Q and dO of all heads fit in L2 a dense layout also takes one group:
   // the L2-sized groups buy nothing there and deal the LPT list in lumps (mha
   // S=2048: per-CTA cost max/mean 1.24 against 1.01 with one group).
+  // Otherwise at least two KV heads per group: one-head groups deal the GQA
+  // workload (B=8, Hkv=8, S=8192) 1.10 max/mean and run its backward in 25.9
+  // ms, two-head groups 25.3 ms (long causal S=32768: 23.7 ms either way).
   const double qdo_bytes = (double)sh.Tq * Hq * d * 4.0;
-  p.hblock = (mode != 0 && (sh.packed || qdo_bytes <= 96e6))
-                 ? Hkv
-                 : pick_hblock(kv_units_per_head, Hkv, grid);
+  int hb_auto = pick_hblock(kv_units_per_head, Hkv, grid);
+  if (mode != 0 && hb_auto < 2) hb_auto = Hkv < 2 ? Hkv : 2;
+  p.hblock = (mode != 0 && (sh.packed || qdo_bytes <= 96e6)) ? Hkv : hb_auto;
   if (kn.bwd_hblock > 0) p.hblock = kn.bwd_hblock < Hkv ? kn.bwd_hblock : Hkv;
   // dQ units (128 query rows of one head) stream the K/V of their head. When
   // the K/V of all heads would not stay in L2 (GB300: 129 MB) a dense layout
