@@ -410,6 +410,7 @@ int bwd_impl(const void* q, const void* k, const void* v, const void* o, const f
       sh.packed ? (sh.Tq + 127) / 128 + B : (long long)B * ((Sq + 127) / 128);
   const double kv_bytes = (double)sh.Tk * Hkv * d * 4.0;
   p.hblock_q = (sh.packed || kv_bytes <= 96e6) ? Hq : pick_hblock(q_units_per_head, Hq, 2 * grid);
+  if (kn.bwd_hblock_q > 0) p.hblock_q = kn.bwd_hblock_q < Hq ? kn.bwd_hblock_q : Hq;
   int grid_q = kn.grid_override > 0 ? kn.grid_override : di->sms;
   if (mode != 0) {
     const long long kv_units = kv_units_per_head * Hkv, q_units = q_units_per_head * Hq;
@@ -529,6 +530,9 @@ extern "C" int fa_debug_set(const char* key, double value) {
   } else if (!strcmp(key, "bwd_hblock")) {
     if (!(value >= 0.0 && value <= 65536.0)) return fail(FA_ERR_INVALID_ARG, "bwd_hblock");
     g_knobs.bwd_hblock = (int)value;
+  } else if (!strcmp(key, "bwd_hblock_q")) {
+    if (!(value >= 0.0 && value <= 65536.0)) return fail(FA_ERR_INVALID_ARG, "bwd_hblock_q");
+    g_knobs.bwd_hblock_q = (int)value;
   } else if (!strcmp(key, "timeout_ms")) {
     if (!(value >= 1.0 && value <= 60000.0)) return fail(FA_ERR_INVALID_ARG, "timeout_ms");
     g_knobs.timeout_ns = (long long)(value * 1e6);

@@ -41,6 +41,7 @@ struct Knobs {
   int grid_override = 0;         // >0: persistent grid size (schedule permutation tests)
   int fwd_hblock = 0;            // >0: forward heads per scheduler group (0: one group)
   int bwd_hblock = 0;            // >0: dK/dV-pass KV heads per scheduler group (0: automatic)
+  int bwd_hblock_q = 0;          // >0: dQ-pass query heads per scheduler group (0: automatic)
   cudaEvent_t ev[2][2] = {{nullptr, nullptr}, {nullptr, nullptr}};  // [fwd|bwd][start|stop]
   long long* trace = nullptr;    // device buffer for the backward role timeline
 };

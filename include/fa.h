@@ -238,6 +238,7 @@ FA_API int fa_get_device_error(int* code, int clear);
  *                pass with fp32 dQ atomics and a convert pass (head dim 128)
  *   "fwd_hblock" forward heads per scheduler group (0 = all heads, default)
  *   "bwd_hblock" dK/dV pass: KV heads per scheduler group (0 = automatic)
+ *   "bwd_hblock_q" dQ pass: query heads per scheduler group (0 = automatic)
  * Returns FA_OK or FA_ERR_INVALID_ARG. Process-wide; not thread-safe with
  * concurrent launches.
  */
