@@ -1,8 +1,8 @@
 """Packed sequences with separate query and key boundaries (fa_fwd_varlen,
 fa_bwd_varlen): prefill over cached keys (more keys than queries), fewer keys
 than queries (bottom-right causal leaves early rows without keys), equal
-counts, and sequences with no keys. Parity against the fp64 oracle with the
-tolerances of the other tests."""
+counts, and sequences with no keys, at head dims 64, 128, 192 and 256.
+Parity against the fp64 oracle with the tolerances of the other tests."""
 import pytest
 import torch
 
@@ -30,7 +30,7 @@ def _dev():
 
 
 @pytest.mark.parametrize("bwd_mode", [1, 0])
-@pytest.mark.parametrize("d,hq,hkv", [(128, 4, 2), (64, 2, 2)])
+@pytest.mark.parametrize("d,hq,hkv", [(128, 4, 2), (64, 2, 2), (192, 4, 2), (256, 2, 1)])
 @pytest.mark.parametrize("causal", [True, False])
 @pytest.mark.parametrize("case", range(len(CASES)))
 def test_separate_boundaries(case, causal, d, hq, hkv, bwd_mode):
