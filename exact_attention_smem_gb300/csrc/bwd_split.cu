@@ -27,12 +27,15 @@
 // deterministic.
 //
 // Both kernels: 12 warps. Warps 0-3 and 4-7 are two compute warpgroups that
-// split the 128 columns of each score tile (64 each, one thread per TMEM lane =
+// split the columns of each score tile (half each, one thread per TMEM lane =
 // tile row); warp 8 allocates TMEM and one of its threads issues the MMAs;
 // warp 9 is the TMA producer; warps 10-11 only complete the register split.
-// A warpgroup writes its bf16 half of P^T/dS^T/dS over the first 32 of its own
-// 64 fp32 columns, so the A operand of the accumulating MMA sits in columns
-// [0,32) and [64,96) of its buffer.
+// A warpgroup writes its bf16 half of P^T/dS^T/dS over the first half of its
+// own fp32 columns, so with 128-column tiles the A operand of the accumulating
+// MMA sits in columns [0,32) and [64,96) of its buffer (64-column tiles:
+// [0,16) and [32,48); 32-column tiles: [0,8) and [16,24)). Head dims 64 and
+// 128 step over 128 query rows / 128 keys; 192 and 256 over smaller steps
+// (kv_step_rows, q_block_keys below).
 #include "exp2_poly.cuh"
 #include "internal.h"
 #include "ptx.cuh"
