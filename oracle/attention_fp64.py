@@ -42,7 +42,7 @@ import numpy as np
 def _as64(x):
     """Accept numpy arrays or torch tensors (any float dtype); return float64 numpy."""
     if hasattr(x, "detach"):
-        x = x.detach().cpu().float().numpy()
+        x = x.detach().cpu().double().numpy()     # exact for bf16, fp16, fp32 and fp64
     return np.asarray(x, dtype=np.float64)
 
 
