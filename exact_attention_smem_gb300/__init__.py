@@ -9,10 +9,10 @@ from __future__ import annotations
 
 import math
 
-from ._lib import (FAError, fa_bwd, fa_bwd_noalloc, fa_bwd_varlen,  # noqa: F401
-                   fa_bwd_workspace_bytes, fa_debug_set, fa_debug_set_events, fa_debug_set_trace,
-                   fa_fwd, fa_fwd_fp8, fa_fwd_varlen, fa_get_device_error, fa_merge,
-                   fa_quantize_fp8, load)
+from ._lib import (FAError, fa_accumulate, fa_bwd, fa_bwd_noalloc,  # noqa: F401
+                   fa_bwd_varlen, fa_bwd_workspace_bytes, fa_debug_set, fa_debug_set_events,
+                   fa_debug_set_trace, fa_fwd, fa_fwd_fp8, fa_fwd_varlen, fa_get_device_error,
+                   fa_merge, fa_quantize_fp8, fa_to_bf16, load)
 
 
 def _dims(q, k, cu_seqlens):

@@ -45,6 +45,8 @@ _SIGS = {
     "fa_debug_set_events": (_I, [_I, _P, _P]),
     "fa_debug_set_trace": (_I, [_P, ctypes.c_size_t]),
     "fa_merge": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P]),
+    "fa_accumulate": (_I, [_P, _P, ctypes.c_longlong, _P]),
+    "fa_to_bf16": (_I, [_P, _P, ctypes.c_longlong, _P]),
     "fa_quantize_fp8": (_I, [_P, _I, _I, _I, _I, _I, _P, _P, _P]),
     "fa_fwd_fp8": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, ctypes.c_float,
                         _P]),
@@ -183,3 +185,15 @@ def fa_fwd_fp8(q8, k8, vt8, q_scale, k_scale, v_scale, o, lse, B, Hq, Hkv, Sq, S
     _check(load().fa_fwd_fp8(_ptr(q8), _ptr(k8), _ptr(vt8), _ptr(q_scale), _ptr(k_scale),
                              _ptr(v_scale), _ptr(o), _ptr(lse), B, Hq, Hkv, Sq, Sk, d,
                              int(causal), float(scale), _stream(stream)), "fa_fwd_fp8")
+
+
+def fa_accumulate(acc, x, n=None, stream=None):
+    """acc (fp32) += x (bf16), element-wise over n elements (default: all of x)."""
+    n = x.numel() if n is None else n
+    _check(load().fa_accumulate(_ptr(acc), _ptr(x), int(n), _stream(stream)), "fa_accumulate")
+
+
+def fa_to_bf16(out, x, n=None, stream=None):
+    """out (bf16) = x (fp32) rounded to nearest even, over n elements (default: all of x)."""
+    n = x.numel() if n is None else n
+    _check(load().fa_to_bf16(_ptr(out), _ptr(x), int(n), _stream(stream)), "fa_to_bf16")

@@ -488,6 +488,36 @@ extern "C" int fa_merge(const void* o_parts, const float* lse_parts, int P, int 
   return FA_OK;
 }
 
+extern "C" int fa_accumulate(float* acc, const void* x, long long n, void* stream) {
+  clear_last_error();
+  if (!acc || !x) return fail(FA_ERR_INVALID_ARG, "acc and x must not be NULL");
+  if (!aligned16(acc) || !aligned16(x))
+    return fail(FA_ERR_INVALID_ARG, "acc and x must be 16-byte aligned");
+  if (n < 0 || n % 8) return fail(FA_ERR_INVALID_ARG, "n=%lld must be >= 0 and a multiple of 8", n);
+  if (n == 0) return FA_OK;
+  DevInfo* di = nullptr;
+  int st = device_info(&di);
+  if (st != FA_OK) return st;
+  cudaError_t e = launch_accumulate(acc, static_cast<const __nv_bfloat16*>(x), n,
+                                    static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : fail(FA_ERR_CUDA, "accumulate launch: %s", cudaGetErrorString(e));
+}
+
+extern "C" int fa_to_bf16(void* out, const float* in, long long n, void* stream) {
+  clear_last_error();
+  if (!out || !in) return fail(FA_ERR_INVALID_ARG, "out and in must not be NULL");
+  if (!aligned16(out) || !aligned16(in))
+    return fail(FA_ERR_INVALID_ARG, "out and in must be 16-byte aligned");
+  if (n < 0 || n % 8) return fail(FA_ERR_INVALID_ARG, "n=%lld must be >= 0 and a multiple of 8", n);
+  if (n == 0) return FA_OK;
+  DevInfo* di = nullptr;
+  int st = device_info(&di);
+  if (st != FA_OK) return st;
+  cudaError_t e = launch_to_bf16(static_cast<__nv_bfloat16*>(out), in, n,
+                                 static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : fail(FA_ERR_CUDA, "conversion launch: %s", cudaGetErrorString(e));
+}
+
 extern "C" const char* fa_status_string(int status) {
   switch (status) {
     case FA_OK: return "ok";

@@ -150,6 +150,10 @@ cudaError_t launch_merge(const __nv_bfloat16* o_parts, const float* lse_parts, i
                          long long rows, int Hq, int S, int d, int packed, __nv_bfloat16* o,
                          float* lse, cudaStream_t stream);
 
+cudaError_t launch_accumulate(float* acc, const __nv_bfloat16* x, long long n,
+                              cudaStream_t stream);
+cudaError_t launch_to_bf16(__nv_bfloat16* out, const float* in, long long n, cudaStream_t stream);
+
 int num_sms();
 int* device_error_word();
 

@@ -29,8 +29,24 @@ NCCL backend device tensors move directly; with gloo (CPU ranks, or a test)
 they are staged through host memory. No TMA or kernel ever reads a peer's
 memory.
 
-The forward and merge are the library's kernels (``attend`` / ``merge``
-default to them); they are parameters so that the ring's schedule can be
+Backward (``ring_backward``). With the merged O and LSE of its query rows, a
+(query chunk a, key chunk b) pair's share of the gradients is exactly what
+``fa_bwd`` computes for that pair alone: P = exp(S - LSE) uses the LSE over
+all keys and D = rowsum(dO * O) the merged O, so the pair's dQ_a, dK_b and dV_b
+are the terms of the full sums that involve the pair's keys ("FlashAttention-4:
+Algorithm and Kernel Pipelining Co-Design for Asymmetric Hardware Scaling",
+abstract item 3: the backward recomputes P from the saved LSE and accumulates
+dQ over key blocks). The K/V chunks go around the ring as in the forward, and
+their dK/dV sums (fp32 for bf16 inputs) travel one step behind them: a rank
+adds its pairs' dK/dV into the sums it received, then passes them on, so the
+transfer of a sum overlaps the next step's backwards; after the last step
+each sum has visited every rank and arrives at the rank that owns the chunk.
+dQ sums stay local. The sums are kept in fp32 by two small library kernels
+(``fa_accumulate``: fp32 += bf16, ``fa_to_bf16``).
+
+The forward, backward, merge and accumulation are the library's kernels
+(``attend`` / ``merge`` / ``backward`` / ``accumulate`` / ``finish`` default to
+them); they are parameters so that the ring's schedule and exchange can be
 checked on CPU ranks against a reference.
 """
 from __future__ import annotations
@@ -84,6 +100,45 @@ def _fa_merge(o_parts, lse_parts):
     lse = torch.empty(lse_parts.shape[1:], dtype=lse_parts.dtype, device=lse_parts.device)
     fa_merge(o_parts, lse_parts, P, B, H, S, d, 0, o, lse)
     return o, lse
+
+
+def _fa_backward():
+    """Per-pair backward into the caller's buffers, with one reused workspace."""
+    import torch
+    from ._lib import fa_bwd, fa_bwd_workspace_bytes
+    ws = [None]
+
+    def backward(q, k, v, o, lse, do, causal, scale, dq, dk, dv):
+        B, Sq, Hq, d = q.shape
+        Sk, Hkv = k.shape[1], k.shape[2]
+        nbytes = fa_bwd_workspace_bytes(B, Hq, Sq, d, 0)
+        if ws[0] is None or ws[0].numel() < nbytes:
+            ws[0] = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+        fa_bwd(q, k, v, o, lse, do, dq, dk, dv, B, Hq, Hkv, Sq, Sk, d, causal, scale, None,
+               ws[0], nbytes, None)
+    return backward
+
+
+def _fa_accumulate(acc, x):
+    from ._lib import fa_accumulate
+    fa_accumulate(acc, x)
+
+
+def _fa_finish(acc, out):
+    from ._lib import fa_to_bf16
+    fa_to_bf16(out, acc)
+
+
+_TAG_KV, _TAG_ACC = 1, 2
+
+
+def _exchange(send, recv, nxt, prv, group, tag):
+    """Post sends of `send` to rank `nxt` and receives into `recv` from rank
+    `prv` as one batch (one NCCL group: no ordering deadlock when nxt == prv)."""
+    import torch.distributed as dist
+    ops = [dist.P2POp(dist.isend, t, _global(nxt, group), group, tag) for t in send]
+    ops += [dist.P2POp(dist.irecv, t, _global(prv, group), group, tag) for t in recv]
+    return dist.batch_isend_irecv(ops)
 
 
 def ring_schedule(world: int, rank: int, causal: bool, layout: str = "zigzag"):
@@ -154,10 +209,7 @@ def ring_forward(q_chunks, k_chunks, v_chunks, causal: bool, scale: float | None
         reqs, incoming = [], None
         if step + 1 < world:
             incoming = [torch.empty_like(t) for t in cur]
-            for t in cur:
-                reqs.append(dist.isend(t, dst=_global(nxt_rank, group), group=group))
-            for t in incoming:
-                reqs.append(dist.irecv(t, src=_global(prv_rank, group), group=group))
+            reqs = _exchange(cur, incoming, nxt_rank, prv_rank, group, _TAG_KV)
         kv = [t.to(device, non_blocking=True) for t in cur] if staged else cur
         ks, vs = kv[:nloc], kv[nloc:]
         for qi, ki, m in pairs:
@@ -170,6 +222,93 @@ def ring_forward(q_chunks, k_chunks, v_chunks, causal: bool, scale: float | None
         if incoming is not None:
             cur = incoming
     return [merge(o_parts[qi], lse_parts[qi]) for qi in range(nloc)]
+
+
+def ring_backward(q_chunks, k_chunks, v_chunks, o_chunks, lse_chunks, do_chunks, causal: bool,
+                  scale: float | None = None, group=None, layout: str = "zigzag", backward=None,
+                  accumulate=None, finish=None):
+    """dQ, dK, dV of this rank's chunks for attention over the whole sequence.
+
+    q/k/v_chunks as for ``ring_forward``; o_chunks and lse_chunks are the
+    merged outputs ``ring_forward`` returned for this rank's query chunks
+    ([B, c, Hq, d] and [B, Hq, c]); do_chunks the output gradients of those
+    rows. Returns three lists (dQ per query chunk, dK and dV per key chunk of
+    this rank), in the inputs' dtype. Every rank of `group` calls this with the
+    same layout and chunk length.
+    """
+    import torch
+    import torch.distributed as dist
+
+    backward = backward or _fa_backward()
+    accumulate = accumulate or _fa_accumulate
+    finish = finish or _fa_finish
+    world = dist.get_world_size(group) if dist.is_initialized() else 1
+    rank = dist.get_rank(group) if dist.is_initialized() else 0
+    if scale is None:
+        scale = 1.0 / math.sqrt(q_chunks[0].shape[-1])
+    nloc = len(chunk_ids(world, rank, layout))
+    for t in (q_chunks, k_chunks, v_chunks, o_chunks, lse_chunks, do_chunks):
+        if len(t) != nloc:
+            raise ValueError(f"rank {rank} holds {nloc} chunks in the {layout} layout")
+    schedule = ring_schedule(world, rank, causal, layout)
+    staged = (world > 1 and dist.get_backend(group) == "gloo" and q_chunks[0].is_cuda)
+    device = q_chunks[0].device
+    acc_dtype = torch.float32 if q_chunks[0].dtype in (torch.bfloat16, torch.float16) \
+        else q_chunks[0].dtype
+
+    def wire(t):
+        return t.cpu() if staged else t
+
+    def local(t):
+        return t.to(device, non_blocking=True) if staged else t
+
+    dq_acc = [torch.zeros(q.shape, dtype=acc_dtype, device=device) for q in q_chunks]
+    # one step's per-pair outputs (a step has at most nloc * nloc pairs)
+    dq_part = [torch.empty_like(q) for q in q_chunks]
+    dk_part = [torch.empty_like(k_chunks[0]) for _ in range(nloc * nloc)]
+    dv_part = [torch.empty_like(v_chunks[0]) for _ in range(nloc * nloc)]
+    # dK/dV sums of the K/V chunks held at this step: the rank's own at step 0
+    acc = ([torch.zeros(k.shape, dtype=acc_dtype, device=device) for k in k_chunks]
+           + [torch.zeros(v.shape, dtype=acc_dtype, device=device) for v in v_chunks])
+    acc_reqs, sent = [], None
+    cur = [wire(t) for t in list(k_chunks) + list(v_chunks)]
+    nxt_rank, prv_rank = (rank + 1) % world, (rank - 1) % world
+    for step, (src, pairs) in enumerate(schedule):
+        kv_reqs, incoming = [], None
+        if step + 1 < world:
+            incoming = [torch.empty_like(t) for t in cur]
+            kv_reqs = _exchange(cur, incoming, nxt_rank, prv_rank, group, _TAG_KV)
+        kv = [local(t) for t in cur]
+        ks, vs = kv[:nloc], kv[nloc:]
+        for j, (qi, ki, m) in enumerate(pairs):
+            backward(q_chunks[qi], ks[ki], vs[ki], o_chunks[qi], lse_chunks[qi], do_chunks[qi],
+                     m == "causal", scale, dq_part[qi], dk_part[j], dv_part[j])
+            accumulate(dq_acc[qi], dq_part[qi])
+        # the sums for these K/V chunks, sent by the previous rank after its step
+        for r in acc_reqs:
+            r.wait()
+        acc = [local(t) for t in acc]
+        for j, (qi, ki, m) in enumerate(pairs):
+            accumulate(acc[ki], dk_part[j])
+            accumulate(acc[nloc + ki], dv_part[j])
+        if world > 1:
+            # on to the rank that holds these chunks next (after the last step: their owner)
+            sent = [wire(t) for t in acc]
+            acc = [torch.empty_like(t) for t in sent]
+            acc_reqs = _exchange(sent, acc, nxt_rank, prv_rank, group, _TAG_ACC)
+        for r in kv_reqs:
+            r.wait()
+        if incoming is not None:
+            cur = incoming
+    for r in acc_reqs:
+        r.wait()
+    acc = [local(t) for t in acc]
+    dq = [torch.empty_like(q) for q in q_chunks]
+    dk = [torch.empty_like(k) for k in k_chunks]
+    dv = [torch.empty_like(v) for v in v_chunks]
+    for a, out in zip(dq_acc + acc, dq + dk + dv):
+        finish(a, out)
+    return dq, dk, dv
 
 
 def _global(rank_in_group, group):

@@ -207,6 +207,24 @@ FA_API int fa_bwd_varlen(const void* q, const void* k, const void* v, const void
 FA_API int fa_merge(const void* o_parts, const float* lse_parts, int P, int B, int Hq, int S,
                     int d, int packed, void* o, float* lse, void* stream);
 
+/*
+ * Accumulation of partial gradients in fp32: acc[i] += x[i] for i < n, acc
+ * fp32, x bf16 (e.g. the dQ, dK, dV that fa_bwd returns for each key shard of
+ * a context-parallel backward; the gradient is their sum, the cross-shard
+ * counterpart of the backward's own accumulation over key blocks:
+ * "FlashAttention-4: Algorithm and Kernel Pipelining Co-Design for Asymmetric
+ * Hardware Scaling", abstract item 3). Device pointers, 16-byte aligned; n a
+ * multiple of 8. Asynchronous on `stream`; allocates nothing. Errors:
+ * FA_ERR_INVALID_ARG (NULL or misaligned pointer, bad n), FA_ERR_CUDA.
+ */
+FA_API int fa_accumulate(float* acc, const void* x, long long n, void* stream);
+
+/*
+ * out[i] = bf16(in[i]) (round to nearest even) for i < n: the final step of an
+ * fp32 gradient accumulation. Same conventions and errors as fa_accumulate.
+ */
+FA_API int fa_to_bf16(void* out, const float* in, long long n, void* stream);
+
 /* Static text for a status code. */
 FA_API const char* fa_status_string(int status);
 

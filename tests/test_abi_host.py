@@ -157,6 +157,18 @@ def test_merge_validates_before_any_device_work(lib):
     assert lib.fa_merge(f, f, 2, 0, 1, 16, 128, 0, f, f, None) == 0      # nothing to do
 
 
+def test_accumulate_and_conversion_validate_before_any_device_work(lib):
+    f = FAKE
+    for fn in (lib.fa_accumulate, lib.fa_to_bf16):
+        assert fn(None, f, 64, None) == 1
+        assert fn(f, None, 64, None) == 1
+        assert fn(f + 4, f, 64, None) == 1                 # 16-byte vectors
+        assert fn(f, f + 8, 64, None) == 1
+        assert fn(f, f, 12, None) == 1                     # whole groups of 8 elements
+        assert fn(f, f, -8, None) == 1
+        assert fn(f, f, 0, None) == 0                      # nothing to do
+
+
 def test_every_knob_is_documented_and_accepted(lib):
     """The keys fa_debug_set accepts are exactly the ones fa.h documents."""
     api = open(os.path.join(ROOT, "exact_attention_smem_gb300", "csrc", "api.cu")).read()
