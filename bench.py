@@ -398,7 +398,9 @@ def run_e2e(fa, w, x, args, stream):
     dV) device->host inside the timed region. The copies run on their own
     streams and device buffers are double-buffered, so step k's input copy and
     step k-1's result copy overlap step k-1's / k's kernels (a buffer set is
-    reused only after the step that last used it has finished with it)."""
+    reused only after the step that last used it has finished with it). Within
+    a step the forward starts once Q, K, V are in (dO follows during the
+    forward) and O, LSE go out during the backward."""
     import torch
     hq, hk, hv, hdo = (t.cpu().pin_memory() for t in (x.q, x.k, x.v, x.do))
     B, Hq, Hkv, S, d = w.B, w.Hq, w.Hkv, w.Sq, w.d
@@ -414,7 +416,9 @@ def run_e2e(fa, w, x, args, stream):
                                                                  device="cuda"),
                              torch.empty_like(x.q), torch.empty_like(x.k), torch.empty_like(x.v))})
     comp, h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
-    ev_in = [torch.cuda.Event() for _ in range(2)]      # inputs of the set copied
+    ev_qkv = [torch.cuda.Event() for _ in range(2)]     # Q, K, V of the set copied in
+    ev_in = [torch.cuda.Event() for _ in range(2)]      # all inputs of the set copied in
+    ev_fwd = [torch.cuda.Event() for _ in range(2)]     # forward done (O, LSE final)
     ev_used = [torch.cuda.Event() for _ in range(2)]    # kernels done with the set
     ev_out = [torch.cuda.Event() for _ in range(2)]     # results of the set copied out
     for e in ev_used + ev_out:
@@ -426,18 +430,26 @@ def run_e2e(fa, w, x, args, stream):
         o_, lse_, dq_, dk_, dv_ = st["out"]
         h2d.wait_event(ev_used[i % 2])
         with torch.cuda.stream(h2d):
-            for dst, src in ((q_, hq), (k_, hk), (v_, hv), (do_, hdo)):
+            for dst, src in ((q_, hq), (k_, hk), (v_, hv)):
                 dst.copy_(src, non_blocking=True)
+            ev_qkv[i % 2].record(h2d)
+            do_.copy_(hdo, non_blocking=True)
         ev_in[i % 2].record(h2d)
-        comp.wait_event(ev_in[i % 2])
+        comp.wait_event(ev_qkv[i % 2])
         comp.wait_event(ev_out[i % 2])
         fa.fa_fwd(q_, k_, v_, o_, lse_, B, Hq, Hkv, S, S, d, True, w.scale, None, comp)
+        ev_fwd[i % 2].record(comp)
+        comp.wait_event(ev_in[i % 2])
         fa.fa_bwd(q_, k_, v_, o_, lse_, do_, dq_, dk_, dv_, B, Hq, Hkv, S, S, d, True, w.scale,
                   None, wsbuf, nbytes, comp)
         ev_used[i % 2].record(comp)
+        d2h.wait_event(ev_fwd[i % 2])
+        with torch.cuda.stream(d2h):
+            for dst, src in ((ho, o_), (hlse, lse_)):
+                dst.copy_(src, non_blocking=True)
         d2h.wait_event(ev_used[i % 2])
         with torch.cuda.stream(d2h):
-            for dst, src in ((ho, o_), (hlse, lse_), (hdq, dq_), (hdk, dk_), (hdv, dv_)):
+            for dst, src in ((hdq, dq_), (hdk, dk_), (hdv, dv_)):
                 dst.copy_(src, non_blocking=True)
         ev_out[i % 2].record(d2h)
 
@@ -457,7 +469,9 @@ def run_e2e(fa, w, x, args, stream):
     d2h_b = sum(t.numel() * t.element_size() for t in (ho, hlse, hdq, hdk, hdv))
     return {"value": round((f_fwd + f_bwd) / (ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
             "ms_per_step": round(ms, 3), "h2d_bytes_per_step": h2d_b, "d2h_bytes_per_step": d2h_b,
-            "steps": n, "overlap": "copies on their own streams, device buffers double-buffered"}
+            "steps": n, "overlap": "copies on their own streams, device buffers double-buffered; "
+                                   "the forward starts once Q, K, V are in, O and LSE go out "
+                                   "during the backward"}
 
 
 def _oracle_sample(w, x_cpu, rows=None):
