@@ -391,6 +391,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dkdv_kernel(const __grid_const
               if (!ok) break;
             }
             mbar_arrive_expect_tx(BAR(C::B_KVFULL), 2 * T::BYTES);
+            FA_TRACE(TR_KV_KVLOAD, nq - (uint32_t)lead);
             const int krow = u.k_start + u.m * BN;
             for (int c = 0; c < T::CHUNKS; ++c) {
               tma_load_3d(base + C::K_OFF + c * T::CHUNK, &p.tm_k, BAR(C::B_KVFULL), c * 64,
@@ -485,6 +486,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dkdv_kernel(const __grid_const
                         BAR(C::B_QFULL + it % C::NQ), (it / C::NQ) & 1, SITE_DKDV_Q_FULL,
                         BAR(C::B_DOFULL + it % C::NDO), (it / C::NDO) & 1, SITE_DKDV_DO_FULL, wc);
         if (!ok) break;
+        FA_TRACE(TR_KV_PRO, it);
         tc_fence_after();
         mma_abt<D, C::IDESC_S, BMS>(tSB, kt, qslot(it));
         tc_commit(BAR(C::B_SFULL));
@@ -649,10 +651,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dkdv_kernel(const __grid_const
       // unit epilogue: this warpgroup's half of the dV and dK rows of this key
       ok = mbar_wait(BAR(C::B_ACCFULL), u_it & 1, wc, SITE_DKDV_ACC_FULL);
       if (!ok) break;
+      if (threadIdx.x == 0) FA_TRACE(TR_KV_EPI, it - 1);
       tc_fence_after();
       ++u_it;
       store_acc_half<DA>(tmem + lane_off + C::TM_DV + wg * (DA / 2), dv_row, 1.0f, key_ok);
       store_acc_half<DA>(tmem + lane_off + C::TM_DK + wg * (DA / 2), dk_row, p.scale, key_ok);
+      if (threadIdx.x == 0) FA_TRACE(TR_KV_EPI_END, it - 1);
       tc_fence_before();
     }
   }

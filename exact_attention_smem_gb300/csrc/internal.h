@@ -58,6 +58,11 @@ enum TraceEvent : int {
   TR_Q_SYNC,                                           // MMA thread after its sync
   TR_Q_S, TR_Q_P, TR_Q_DP, TR_Q_DS,                    // compute thread 0
   TR_Q_KLOAD,                                          // producer: K_j load issued
+  // dK/dV pass unit boundaries, at the index of a unit's first step (EPI: of
+  // the unit just finished, i.e. its last step)
+  TR_KV_KVLOAD,                                        // producer: K/V of the unit issued
+  TR_KV_PRO,                                           // MMA thread: S^T(0)/dP^T(0) issued
+  TR_KV_EPI, TR_KV_EPI_END,                            // compute thread 0: dK/dV write-out
   TR_NUM
 };
 Knobs knobs_snapshot();

@@ -274,8 +274,9 @@ FA_API int fa_debug_set_events(int which /* 0 = forward, 1 = backward */, void* 
 
 /*
  * Tuning hook: while armed, each fa_bwd main kernel writes a role timeline of
- * CTA 0 (clock64 after each cross-role wait, for its first 512 steps) into
- * trace_dev (device buffer of at least 22*512 int64). NULL disarms.
+ * CTA 0 (clock64 after each cross-role wait, for its first 512 steps, and at
+ * the dK/dV pass's unit boundaries) into trace_dev (device buffer of at least
+ * 26*512 int64). NULL disarms. Errors: FA_ERR_INVALID_ARG (buffer too small).
  */
 FA_API int fa_debug_set_trace(void* trace_dev, size_t bytes);
 
