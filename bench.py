@@ -282,7 +282,7 @@ def run_ours(args):
                              "traffic": profiled_traffic("fwd.cu",
                                                          f"fwd_kernel_{WORKLOAD}.md")}},
         "e2e": e2e,
-        "gpu_launches": 5 * args.steps,
+        "gpu_launches": 4 * args.steps,        # forward, preprocess, dK/dV pass, dQ pass
         "clocks": clocks,
         "cpu_baseline": cpu,
     }
@@ -294,7 +294,7 @@ def run_ours(args):
 def run_once(args):
     """One forward and one backward (or one FP8 forward) of the workload, no
     timing and no output line: the launch sequence a profiler capture selects
-    kernels from (forward, preprocess, pad, dK/dV pass, dQ pass)."""
+    kernels from (forward, preprocess, dK/dV pass, dQ pass)."""
     import torch
 
     import exact_attention_smem_gb300 as fa

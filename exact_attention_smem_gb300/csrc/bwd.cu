@@ -2,10 +2,10 @@
 //
 // Three kernels on one stream:
 //   1. preprocess: -D_i = -sum_c dO_ic O_ic and -LSE_i * log2(e) into padded
-//      row arrays (each sequence starts on a 64-row boundary so one 64-row
-//      block is one aligned 256-byte bulk copy; stored negated so the main
-//      kernel uses them as FMA addends), padding rows get LSE = +inf and D = 0,
-//      and the fp32 dQ accumulator is zeroed;
+//      row arrays (each sequence starts on a 128-row boundary so one 64- or
+//      128-row block is one aligned bulk copy; stored negated so the main
+//      kernels use them as FMA addends), padding rows get LSE = +inf and D = 0,
+//      and the fp32 dQ accumulator (one-pass form) is zeroed;
 //   2. main: one persistent CTA per SM walks (sequence, 128-key block, KV head)
 //      units longest-first. For each query head of the KV group and each block
 //      of 64 query rows that sees the keys it computes, with tcgen05 MMAs
@@ -596,93 +596,121 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) bwd_kernel(const __grid_consta
 #undef BAR
 }
 
-// -D and -LSE*log2e into the padded row arrays; zero the dQ accumulator when
-// there is one (one-pass kernel). Each (row, head) of O and dO is read by a
-// group of lanes, 16 bytes (8 values) per lane: D/8 lanes, rounded up to a
-// power of two, so a warp covers 4, 2, 1 or 1 rows (D = 64, 128, 192, 256).
+// -D and -LSE*log2e into the padded row arrays, and their padding rows; zero
+// the dQ accumulator when there is one (one-pass kernel). A warp takes 32
+// consecutive query rows of one head. Each row's O and dO are read by a group
+// of lanes, 16 bytes (8 values) per lane: D/8 lanes rounded up to a power of
+// two, so one pass of the warp covers 4, 2, 1 or 1 rows (D = 64, 128, 192,
+// 256); the loads of eight passes go out together. The 32 results then go
+// out as one coalesced store per array (the arrays are head-major). The
+// remaining warps write the padding rows [q_len, round_up(q_len, 128)) of each
+// (sequence, head): LSE = +inf, D = 0, so a block's padded query rows
+// contribute exact zeros.
 template <int D>
 struct PreGroup {
   static constexpr int LANES = D / 8;                       // lanes with data
   static constexpr int G = LANES <= 8 ? 8 : LANES <= 16 ? 16 : 32;
-  static constexpr int RPW = 32 / G;                        // rows per warp
+  static constexpr int RPW = 32 / G;                        // rows per pass of a warp
+  static constexpr int PASSES = 32 / RPW;                   // passes over 32 rows
+  static constexpr int BATCH = PASSES < 8 ? PASSES : 8;     // passes loaded together
 };
 
 template <int D>
 __global__ void bwd_pre_kernel(BwdParams p, BwdAux aux) {
   using PG = PreGroup<D>;
-  const long long nrows = (long long)p.total_q * p.Hq;
+  const int T = p.total_q;
+  const int nchunk = (T + 31) / 32;
+  const long long nrowwarps = (long long)p.Hq * nchunk;
+  const long long nwork = nrowwarps + (long long)p.Hq * p.nseq;
   const int lane = threadIdx.x & 31;
   const int gl = lane & (PG::G - 1);                         // lane within the row's group
   const int c = gl * 8;                                      // this lane's 8 columns
+  const int sub = lane / PG::G;                              // row of the pass
   const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
-  for (long long r0 = ((long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * PG::RPW;
-       r0 < nrows; r0 += warps * PG::RPW) {
-    const long long r = r0 + lane / PG::G;
-    const bool row_ok = r < nrows;
-    float acc = 0.f;
-    if (row_ok && c < D) {
-      const uint4 ov = *reinterpret_cast<const uint4*>(aux.o + r * D + c);
-      const uint4 gv = *reinterpret_cast<const uint4*>(aux.dout + r * D + c);
-      const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
-      const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&gv);
+  for (long long wi = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); wi < nwork;
+       wi += warps) {
+    if (wi < nrowwarps) {
+      const int h = (int)(wi / nchunk), t0 = (int)(wi - (long long)h * nchunk) * 32;
+      float mine = 0.f;                                      // lane L: D of row t0 + L
+#pragma unroll 1
+      for (int i0 = 0; i0 < PG::PASSES; i0 += PG::BATCH) {
+        uint4 ov[PG::BATCH], gv[PG::BATCH];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float2 of = __bfloat1622float2(o2[e]);
-        const float2 gf = __bfloat1622float2(g2[e]);
-        acc = fmaf(of.x, gf.x, acc);
-        acc = fmaf(of.y, gf.y, acc);
-      }
-    }
-#pragma unroll
-    for (int sh = PG::G / 2; sh > 0; sh >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, sh);
-    if (!row_ok) continue;
-    if (p.dq_acc && c < D) {
-      float4* zr = reinterpret_cast<float4*>(p.dq_acc + r * D + c);
-      zr[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-      zr[1] = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    if (gl == 0) {
-      const int t = (int)(r / p.Hq), h = (int)(r % p.Hq);
-      int seq, q_start;
-      if (p.cu) {
-        int lo = 0, hi = p.nseq;               // last seq with cu[seq] <= t (non-empty)
-        while (hi - lo > 1) {
-          const int mid = (lo + hi) >> 1;
-          if (p.cu[mid] <= t) lo = mid; else hi = mid;
+        for (int b = 0; b < PG::BATCH; ++b) {
+          const int t = t0 + (i0 + b) * PG::RPW + sub;
+          ov[b] = gv[b] = make_uint4(0, 0, 0, 0);
+          if (t < T && c < D) {
+            const long long r = (long long)t * p.Hq + h;
+            ov[b] = *reinterpret_cast<const uint4*>(aux.o + r * D + c);
+            gv[b] = *reinterpret_cast<const uint4*>(aux.dout + r * D + c);
+            if (p.dq_acc) {
+              float4* zr = reinterpret_cast<float4*>(p.dq_acc + r * D + c);
+              zr[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+              zr[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+          }
         }
-        seq = lo;
-        q_start = p.cu[lo];
-      } else {
-        seq = t / p.Sq;
-        q_start = seq * p.Sq;
+#pragma unroll
+        for (int b = 0; b < PG::BATCH; ++b) {
+          const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov[b]);
+          const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&gv[b]);
+          float acc = 0.f;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 of = __bfloat1622float2(o2[e]);
+            const float2 gf = __bfloat1622float2(g2[e]);
+            acc = fmaf(of.x, gf.x, acc);
+            acc = fmaf(of.y, gf.y, acc);
+          }
+#pragma unroll
+          for (int sh = PG::G / 2; sh > 0; sh >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, sh);
+#pragma unroll
+          for (int j = 0; j < PG::RPW; ++j) {
+            const float v = __shfl_sync(0xffffffffu, acc, j * PG::G);
+            if (lane == (i0 + b) * PG::RPW + j) mine = v;
+          }
+        }
       }
-      const int row = t - q_start;
-      const float lse = aux.lse[(p.cu ? 0ll : (long long)seq * aux.lse_seqstride) +
-                                (long long)h * aux.lse_hstride + (p.cu ? t : row)];
-      const long long pi = (long long)h * p.pad_hstride + pad_start(seq, q_start) + row;
-      const_cast<float*>(p.lse2)[pi] = -lse * 1.4426950408889634f;
-      const_cast<float*>(p.delta)[pi] = -acc;
+      const int t = t0 + lane;
+      if (t < T) {
+        int seq, q_start;
+        if (p.cu) {
+          int lo = 0, hi = p.nseq;                           // last seq with cu[seq] <= t
+          while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (p.cu[mid] <= t) lo = mid; else hi = mid;
+          }
+          seq = lo;
+          q_start = p.cu[lo];
+        } else {
+          seq = t / p.Sq;
+          q_start = seq * p.Sq;
+        }
+        const int row = t - q_start;
+        const float lse = aux.lse[(p.cu ? 0ll : (long long)seq * aux.lse_seqstride) +
+                                  (long long)h * aux.lse_hstride + (p.cu ? t : row)];
+        const long long pi = (long long)h * p.pad_hstride + pad_start(seq, q_start) + row;
+        const_cast<float*>(p.lse2)[pi] = -lse * 1.4426950408889634f;
+        const_cast<float*>(p.delta)[pi] = -mine;
+      }
+    } else {
+      const long long k = wi - nrowwarps;
+      const int h = (int)(k / p.nseq), seq = (int)(k - (long long)h * p.nseq);
+      int q_start, q_len;
+      if (p.cu) {
+        q_start = p.cu[seq];
+        q_len = p.cu[seq + 1] - q_start;
+      } else {
+        q_start = seq * p.Sq;
+        q_len = p.Sq;
+      }
+      const int end = (q_len + 127) & ~127;
+      const long long base = (long long)h * p.pad_hstride + pad_start(seq, q_start);
+      for (int row = q_len + lane; row < end; row += 32) {
+        const_cast<float*>(p.lse2)[base + row] = -INFINITY;
+        const_cast<float*>(p.delta)[base + row] = 0.f;
+      }
     }
-  }
-}
-
-// Padding rows [q_len, round_up(q_len, 128)) of every sequence: LSE = +inf,
-// D = 0, so the padded query rows of a block contribute exact zeros.
-__global__ void bwd_pad_kernel(BwdParams p) {
-  const int seq = blockIdx.x, h = blockIdx.y, r = threadIdx.x;   // 128 threads
-  int q_start, q_len;
-  if (p.cu) {
-    q_start = p.cu[seq];
-    q_len = p.cu[seq + 1] - q_start;
-  } else {
-    q_start = seq * p.Sq;
-    q_len = p.Sq;
-  }
-  const int row = ((q_len + 127) & ~127) - 128 + r;
-  if (row >= q_len && row >= 0) {
-    const long long pi = (long long)h * p.pad_hstride + pad_start(seq, q_start) + row;
-    const_cast<float*>(p.lse2)[pi] = -INFINITY;
-    const_cast<float*>(p.delta)[pi] = 0.f;
   }
 }
 
@@ -720,24 +748,21 @@ cudaError_t launch_bwd(const BwdParams& p, const BwdAux& aux, int d, int grid, i
   const long long rows = (long long)p.total_q * p.Hq;
   if (rows > 0) {
     // 8 warps per block, RPW rows per warp
-    auto blocks_for = [&](int rpw) {
-      const long long b = (rows + 8ll * rpw - 1) / (8ll * rpw);
-      return (int)(b < 65535ll * 8 ? b : 65535ll * 8);
-    };
+    // one warp per 32 rows of a head plus one per (sequence, head) for the
+    // padding; 8 warps per block
+    const long long work = (long long)p.Hq * ((p.total_q + 31) / 32 + p.nseq);
+    const long long b = (work + 7) / 8;
+    const int blocks = (int)(b < 65535ll * 8 ? b : 65535ll * 8);
     if (d == 128)
-      bwdk::bwd_pre_kernel<128><<<blocks_for(bwdk::PreGroup<128>::RPW), 256, 0, stream>>>(p, aux);
+      bwdk::bwd_pre_kernel<128><<<blocks, 256, 0, stream>>>(p, aux);
     else if (d == 192)
-      bwdk::bwd_pre_kernel<192><<<blocks_for(bwdk::PreGroup<192>::RPW), 256, 0, stream>>>(p, aux);
+      bwdk::bwd_pre_kernel<192><<<blocks, 256, 0, stream>>>(p, aux);
     else if (d == 256)
-      bwdk::bwd_pre_kernel<256><<<blocks_for(bwdk::PreGroup<256>::RPW), 256, 0, stream>>>(p, aux);
+      bwdk::bwd_pre_kernel<256><<<blocks, 256, 0, stream>>>(p, aux);
     else
-      bwdk::bwd_pre_kernel<64><<<blocks_for(bwdk::PreGroup<64>::RPW), 256, 0, stream>>>(p, aux);
+      bwdk::bwd_pre_kernel<64><<<blocks, 256, 0, stream>>>(p, aux);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    if (p.nseq > 0) {
-      bwdk::bwd_pad_kernel<<<dim3(p.nseq, p.Hq), 128, 0, stream>>>(p);
-      if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    }
   }
   if (mode != 0) {
     cudaEvent_t ev0, ev1;
