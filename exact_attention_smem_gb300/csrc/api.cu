@@ -105,6 +105,7 @@ int fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, i
     if ((st = encode_rows(&p.tm_k, q, sh.Tq, Hq, d)) != FA_OK) return st;
     if ((st = encode_rows(&p.tm_v, q, sh.Tq, Hq, d)) != FA_OK) return st;
   }
+  if (d <= 128 && (st = encode_rows(&p.tm_o, o, sh.Tq, Hq, d)) != FA_OK) return st;
   p.o = static_cast<__nv_bfloat16*>(o);
   p.lse = lse;
   p.cu = cu_seqlens;

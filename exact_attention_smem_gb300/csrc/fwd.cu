@@ -44,7 +44,7 @@ constexpr int TMA_WARP = 9;
 // 192: 2*128*192 + 128*112 = 63488 <= 384*168 = 64512 (no spills either side).
 constexpr int REGS_SOFTMAX = 192;
 constexpr int REGS_CONTROL = 112;
-constexpr int MAX_SEQ_SMEM = 1024;
+constexpr int MAX_SEQ_SMEM = 256;   // packed boundaries kept in shared memory up to this
 
 template <int D>
 struct Cfg {
@@ -60,7 +60,10 @@ struct Cfg {
                        B_DRAIN = B_OFULL + 2, NBAR = B_DRAIN + 1;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int CU_OFF = MISC_OFF + 16;
-  static constexpr int SMEM_BYTES = CU_OFF + (MAX_SEQ_SMEM + 1) * 4 + 1024;
+  // O write-out staging: one 128-row x 64-column chunk (128B swizzle) per softmax warpgroup
+  static constexpr int STAGE_OFF = (CU_OFF + (MAX_SEQ_SMEM + 1) * 4 + 1023) & ~1023;
+  static constexpr int SMEM_BYTES = STAGE_OFF + 2 * CHUNK_BYTES + 1024;
+  static_assert(SMEM_BYTES <= 232448, "forward shared memory");
   static constexpr uint32_t IDESC_S = idesc_bf16(128, 128, false, false);
   static constexpr uint32_t IDESC_PV = idesc_bf16(128, D, false, true);
   static constexpr uint32_t TM_S = 0;
@@ -138,6 +141,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) fwd_kernel(const __grid_consta
     tma_prefetch_desc(&p.tm_q);
     tma_prefetch_desc(&p.tm_k);
     tma_prefetch_desc(&p.tm_v);
+    tma_prefetch_desc(&p.tm_o);
   }
   if (warp == MMA_WARP) {
     tmem_alloc(smem_u32(tmem_slot), 512);
@@ -414,25 +418,57 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) fwd_kernel(const __grid_consta
       tc_fence_after();
       ++u_it;
       const float inv = lp > 0.f ? 1.0f / lp : 0.f;
+      const int row0 = u.m * UNIT_ROWS + t * BM;         // the tile's first row in the sequence
+      if (row0 + BM <= u.q_len) {
+        // A whole tile of the sequence: each 64-column chunk goes through this
+        // warpgroup's staging buffer (rows in the 128B-swizzled layout the
+        // tensor map uses) and out as one TMA store of full 128-byte lines.
+        const uint32_t stage = base + C::STAGE_OFF + t * C::CHUNK_BYTES;
+        uint8_t* stage_p = smem + C::STAGE_OFF + t * C::CHUNK_BYTES + r * 128;
 #pragma unroll 1
-      for (int c = 0; c < D; c += 32) {
-        uint32_t o[32];
-        tmem_ld32(tO + c, o);
-        uint32_t q[16];
+        for (int ch = 0; ch < C::CHUNKS; ++ch) {
+          uint32_t o[64];
+          tmem_ld64(tO + ch * 64, o);
+          uint32_t q[32];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) q[i] = pack_bf16x2(u2f(o[2 * i]) * inv, u2f(o[2 * i + 1]) * inv);
-        if (valid) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c);
-          dst[0] = make_uint4(q[0], q[1], q[2], q[3]);
-          dst[1] = make_uint4(q[4], q[5], q[6], q[7]);
-          dst[2] = make_uint4(q[8], q[9], q[10], q[11]);
-          dst[3] = make_uint4(q[12], q[13], q[14], q[15]);
+          for (int i = 0; i < 32; ++i) q[i] = pack_bf16x2(u2f(o[2 * i]) * inv, u2f(o[2 * i + 1]) * inv);
+          // the previous store from this buffer has read it
+          if (r == 0) tma_store_wait_read();
+          named_bar_sync(1 + t, BM);
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            *reinterpret_cast<uint4*>(stage_p + ((j ^ (r & 7)) << 4)) =
+                make_uint4(q[4 * j], q[4 * j + 1], q[4 * j + 2], q[4 * j + 3]);
+          fence_proxy_async_smem();
+          named_bar_sync(1 + t, BM);
+          if (r == 0) {
+            tma_store_3d(&p.tm_o, stage, ch * 64, u.head, u.q_start + row0);
+            tma_store_commit();
+          }
+        }
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < D; c += 32) {
+          uint32_t o[32];
+          tmem_ld32(tO + c, o);
+          uint32_t q[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) q[i] = pack_bf16x2(u2f(o[2 * i]) * inv, u2f(o[2 * i + 1]) * inv);
+          if (valid) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + c);
+            dst[0] = make_uint4(q[0], q[1], q[2], q[3]);
+            dst[1] = make_uint4(q[4], q[5], q[6], q[7]);
+            dst[2] = make_uint4(q[8], q[9], q[10], q[11]);
+            dst[3] = make_uint4(q[12], q[13], q[14], q[15]);
+          }
         }
       }
       if (valid) *lse_ptr = l > 0.f ? (m_ref + log2f(l)) * 0.69314718055994530942f : INFINITY;
     }
   }
 
+  // the O stores complete before the CTA (and its shared memory) goes away
+  if (warp < 8 && (threadIdx.x & (BM - 1)) == 0) tma_store_wait_all();
   tc_fence_before();
   __syncthreads();
   if (warp == MMA_WARP) {

@@ -70,6 +70,7 @@ void take_events(int which, cudaEvent_t* start, cudaEvent_t* stop);  // one-shot
 
 struct FwdParams {
   CUtensorMap tm_q, tm_k, tm_v;  // [T, H, d] views, 64-column x 128-row boxes, 128B swizzle
+  CUtensorMap tm_o;              // the output O, same view (bf16 forward, head dim <= 128)
   __nv_bfloat16* o;
   float* lse;
   const int* cu;                 // packed boundaries or nullptr
