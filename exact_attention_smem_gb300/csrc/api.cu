@@ -235,6 +235,7 @@ extern "C" int fa_fwd_fp8(const void* q8, const void* k8, const void* vt8, const
     p.tm_k = p.tm_q;
     p.tm_v = p.tm_q;
   }
+  if ((st = encode_rows(&p.tm_o, o, Tq, Hq, d)) != FA_OK) return st;
   p.o = static_cast<__nv_bfloat16*>(o);
   p.lse = lse;
   p.nseq = B;

@@ -58,7 +58,13 @@ struct Cfg {
                        B_SFULL = 2 + 2 * NSTAGE, B_PFULL = B_SFULL + 2, B_OFULL = B_PFULL + 2,
                        B_DRAIN = B_OFULL + 2, NBAR = B_DRAIN + 1;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
-  static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;
+  // O write-out staging (bf16, 128B swizzle): per softmax warpgroup its whole
+  // tile, two 128-row x 64-column chunks
+  static constexpr int OCHUNK_BYTES = 128 * 128;
+  static constexpr int OCHUNKS = D / 64;
+  static constexpr int STAGE_OFF = (MISC_OFF + 16 + 1023) & ~1023;
+  static constexpr int SMEM_BYTES = STAGE_OFF + 2 * OCHUNKS * OCHUNK_BYTES + 1024;
+  static_assert(SMEM_BYTES <= 232448, "FP8 forward shared memory");
   static constexpr uint32_t IDESC_S = idesc_e4m3(128, 128);
   static constexpr uint32_t IDESC_PV = idesc_e4m3(128, D);
   static constexpr uint32_t TM_S = 0;
@@ -133,6 +139,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) fwd_fp8_kernel(const __grid_co
     tma_prefetch_desc(&p.tm_q);
     tma_prefetch_desc(&p.tm_k);
     tma_prefetch_desc(&p.tm_v);
+    tma_prefetch_desc(&p.tm_o);
   }
   if (warp == MMA_WARP) {
     tmem_alloc(smem_u32(tmem_slot), 512);
@@ -402,19 +409,53 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) fwd_fp8_kernel(const __grid_co
       tc_fence_after();
       ++u_it;
       const float inv = l > 0.f ? p.v_scale[(long long)u.seq * p.Hkv + kvh] / l : 0.f;
+      const int row0 = u.m * UNIT_ROWS + t * BM;         // the tile's first row in the sequence
+      if (row0 + BM <= u.q_len) {
+        // A whole tile of the sequence: out through this warpgroup's staging
+        // buffer (the tensor map's 128B-swizzled layout) with TMA stores of
+        // full 128-byte lines.
+        const uint32_t stage = base + C::STAGE_OFF + t * C::OCHUNKS * C::OCHUNK_BYTES;
+        uint8_t* stage_p = smem + C::STAGE_OFF + t * C::OCHUNKS * C::OCHUNK_BYTES + r * 128;
+        if (r == 0) tma_store_wait_read();               // the previous tile's stores read it
+        named_bar_sync(1 + t, BM);
 #pragma unroll 1
-      for (int c = 0; c < D; c += 32) {
-        uint32_t o[32];
-        tmem_ld32(tO + c, o);
-        uint32_t q[16];
+        for (int ch = 0; ch < C::OCHUNKS; ++ch) {
+          uint32_t o[64];
+          tmem_ld64(tO + ch * 64, o);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) q[i] = pack_bf16x2(u2f(o[2 * i]) * inv, u2f(o[2 * i + 1]) * inv);
-        if (valid) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c);
-          dst[0] = make_uint4(q[0], q[1], q[2], q[3]);
-          dst[1] = make_uint4(q[4], q[5], q[6], q[7]);
-          dst[2] = make_uint4(q[8], q[9], q[10], q[11]);
-          dst[3] = make_uint4(q[12], q[13], q[14], q[15]);
+          for (int j = 0; j < 8; ++j) {
+            uint4 v;
+            v.x = pack_bf16x2(u2f(o[8 * j]) * inv, u2f(o[8 * j + 1]) * inv);
+            v.y = pack_bf16x2(u2f(o[8 * j + 2]) * inv, u2f(o[8 * j + 3]) * inv);
+            v.z = pack_bf16x2(u2f(o[8 * j + 4]) * inv, u2f(o[8 * j + 5]) * inv);
+            v.w = pack_bf16x2(u2f(o[8 * j + 6]) * inv, u2f(o[8 * j + 7]) * inv);
+            *reinterpret_cast<uint4*>(stage_p + ch * C::OCHUNK_BYTES + ((j ^ (r & 7)) << 4)) = v;
+          }
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(1 + t, BM);
+        if (r == 0) {
+          for (int ch = 0; ch < C::OCHUNKS; ++ch)
+            tma_store_3d(&p.tm_o, stage + ch * C::OCHUNK_BYTES, ch * 64, u.head,
+                         u.q_start + row0);
+          tma_store_commit();
+        }
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < D; c += 32) {
+          uint32_t o[32];
+          tmem_ld32(tO + c, o);
+          uint32_t q[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            q[i] = pack_bf16x2(u2f(o[2 * i]) * inv, u2f(o[2 * i + 1]) * inv);
+          if (valid) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + c);
+            dst[0] = make_uint4(q[0], q[1], q[2], q[3]);
+            dst[1] = make_uint4(q[4], q[5], q[6], q[7]);
+            dst[2] = make_uint4(q[8], q[9], q[10], q[11]);
+            dst[3] = make_uint4(q[12], q[13], q[14], q[15]);
+          }
         }
       }
       if (valid)
@@ -423,6 +464,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) fwd_fp8_kernel(const __grid_co
     }
   }
 
+  // the O stores complete before the CTA (and its shared memory) goes away
+  if (warp < 8 && (threadIdx.x & (BM - 1)) == 0) tma_store_wait_all();
   tc_fence_before();
   __syncthreads();
   if (warp == MMA_WARP) {
