@@ -1,7 +1,8 @@
 """Packed sequences with separate query and key boundaries (fa_fwd_varlen,
 fa_bwd_varlen): prefill over cached keys (more keys than queries), fewer keys
 than queries (bottom-right causal leaves early rows without keys), equal
-counts, and sequences with no keys, at head dims 64, 128, 192 and 256.
+counts, and sequences with no keys, at head dims 64, 128, 192 and 256; and
+300 packed sequences, more boundaries than the kernels keep in shared memory.
 Parity against the fp64 oracle with the tolerances of the other tests."""
 import pytest
 import torch
@@ -65,3 +66,32 @@ def test_rejects_missing_key_list():
     with pytest.raises(fa.FAError) as e:
         fa.fa_fwd_varlen(x.q, x.k, x.v, o, lse, 1, 2, 2, 10, 20, 128, True, 0.1, x.cu_seqlens, None)
     assert e.value.status == 1
+
+
+@pytest.mark.parametrize("separate_keys", [False, True])
+@pytest.mark.parametrize("causal", [True, False])
+def test_many_sequences_read_boundaries_from_global_memory(causal, separate_keys):
+    """300 packed sequences: more boundaries than the kernels keep in shared
+    memory (forward 256 entries, backward 200; separate key lists take two
+    entries per sequence), so every role reads them from global memory."""
+    g = torch.Generator().manual_seed(7)
+    lq = [int(x) for x in torch.randint(0, 40, (300,), generator=g)]
+    lk = [int(x) for x in torch.randint(0, 60, (300,), generator=g)] if separate_keys else None
+    d, hq, hkv = 128, 2, 1
+    x = random_inputs(B=None, Hq=hq, Hkv=hkv, Sq=None, Sk=None, d=d, seed=77, lengths=lq,
+                      lengths_k=lk, device="cuda")
+    scale = d ** -0.5
+    cu, cuk = x.cu_seqlens, x.cu_seqlens_k
+    o, lse = fa.forward(x.q, x.k, x.v, causal=causal, scale=scale, cu_seqlens=cu, cu_seqlens_k=cuk)
+    grads = fa.backward(x.q, x.k, x.v, o, lse, x.do, causal=causal, scale=scale, cu_seqlens=cu,
+                        cu_seqlens_k=cuk)
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_error(clear=True) == 0
+    qc, kc, vc, doc = (t.cpu() for t in (x.q, x.k, x.v, x.do))
+    cuk_c = None if cuk is None else cuk.cpu()
+    ro, rl = oracle.forward(qc, kc, vc, scale, causal, cu_seqlens=cu.cpu(), cu_seqlens_k=cuk_c)
+    assert max_abs(o, ro) <= O_TOL
+    assert max_abs(lse, rl) <= LSE_TOL
+    ref = oracle.backward(qc, kc, vc, doc, scale, causal, cu_seqlens=cu.cpu(), cu_seqlens_k=cuk_c)
+    errs = {n: rel_l2(g_, r) for n, g_, r in zip(("dq", "dk", "dv"), grads, ref)}
+    assert all(e <= GRAD_TOL for e in errs.values()), errs
