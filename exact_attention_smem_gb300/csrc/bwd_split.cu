@@ -246,6 +246,10 @@ __device__ __forceinline__ int first_qblock(const Unit& u, int causal) {
 template <int D>
 __device__ __forceinline__ void store_acc_half(uint32_t t_acc, __nv_bfloat16* dst, float mul,
                                                bool ok) {
+  // 32-byte stores where the row allows (each thread writes its own row piece,
+  // so a warp's store instruction touches 32 different lines: fewer, wider
+  // stores halve those line accesses); 16-byte ones otherwise
+  const bool wide = (reinterpret_cast<uintptr_t>(dst) & 31) == 0;
 #pragma unroll 1
   for (int c = 0; c < D / 2; c += 32) {
     uint32_t a[32];
@@ -254,11 +258,18 @@ __device__ __forceinline__ void store_acc_half(uint32_t t_acc, __nv_bfloat16* ds
 #pragma unroll
     for (int e = 0; e < 16; ++e) q[e] = pack_bf16x2(u2f(a[2 * e]) * mul, u2f(a[2 * e + 1]) * mul);
     if (ok) {
-      uint4* o4 = reinterpret_cast<uint4*>(dst + c);
-      o4[0] = make_uint4(q[0], q[1], q[2], q[3]);
-      o4[1] = make_uint4(q[4], q[5], q[6], q[7]);
-      o4[2] = make_uint4(q[8], q[9], q[10], q[11]);
-      o4[3] = make_uint4(q[12], q[13], q[14], q[15]);
+      if (wide) {
+        const uint32_t q0[8] = {q[0], q[1], q[2], q[3], q[4], q[5], q[6], q[7]};
+        const uint32_t q1[8] = {q[8], q[9], q[10], q[11], q[12], q[13], q[14], q[15]};
+        st_global_v8(dst + c, q0);
+        st_global_v8(dst + c + 16, q1);
+      } else {
+        uint4* o4 = reinterpret_cast<uint4*>(dst + c);
+        o4[0] = make_uint4(q[0], q[1], q[2], q[3]);
+        o4[1] = make_uint4(q[4], q[5], q[6], q[7]);
+        o4[2] = make_uint4(q[8], q[9], q[10], q[11]);
+        o4[3] = make_uint4(q[12], q[13], q[14], q[15]);
+      }
     }
   }
 }

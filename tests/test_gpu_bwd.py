@@ -200,3 +200,30 @@ def test_head_dims_192_256_gqa_and_packed(d, bwd_mode):
                       lengths=[1, 63, 0, 200, 129, 64], device="cuda")
     _check(x, True, d ** -0.5, cu=x.cu_seqlens)
     _check(x, False, d ** -0.5, cu=x.cu_seqlens)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_outputs_16_byte_aligned_only(d, bwd_mode):
+    """dQ, dK, dV at addresses that are 16- but not 32-byte aligned (the C ABI
+    asks for 16): the write-outs take their narrower stores there."""
+    if bwd_mode == 0 and d != 128:
+        pytest.skip("the one-pass form supports d=128 only")
+    x = random_inputs(B=2, Hq=4, Hkv=2, Sq=300, Sk=300, d=d, seed=91 + d, device="cuda")
+    B, Hq, Hkv, Sq, Sk, _ = _dims(x, None)
+    o, lse = fa.forward(x.q, x.k, x.v, causal=True, scale=d ** -0.5)
+    nbytes = fa.fa_bwd_workspace_bytes(B, Hq, Sq, d, 0)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    outs = []
+    for t in (x.q, x.k, x.v):
+        raw = torch.full((t.numel() + 8,), float("nan"), dtype=torch.bfloat16, device="cuda")
+        v = raw[8:].view(t.shape)                       # 16 bytes past a 256-byte boundary
+        assert v.data_ptr() % 32 == 16
+        outs.append(v)
+    dq, dk, dv = outs
+    fa.fa_bwd(x.q, x.k, x.v, o, lse, x.do, dq, dk, dv, B, Hq, Hkv, Sq, Sk, d, True, d ** -0.5,
+              None, ws, nbytes)
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_error(clear=True) == 0
+    ref = oracle.backward(x.q.cpu(), x.k.cpu(), x.v.cpu(), x.do.cpu(), d ** -0.5, True)
+    for g, r in zip((dq, dk, dv), ref):
+        assert rel_l2(g, r) <= GRAD_TOL
