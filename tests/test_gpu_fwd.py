@@ -147,3 +147,22 @@ def test_poly_exp_split_keeps_parity(poly8):
     x = random_inputs(B=2, Hq=2, Hkv=2, Sq=700, Sk=700, d=128, seed=13, device="cuda")
     _check(x, True, 128 ** -0.5)
     fa.fa_debug_set("poly8", 0)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_output_16_byte_aligned_only(d):
+    """O at an address that is 16- but not 32-byte aligned (the C ABI asks for
+    16): whole tiles still leave through TMA stores, the rest per thread."""
+    x = random_inputs(B=2, Hq=3, Hkv=3, Sq=300, Sk=300, d=d, seed=17 + d, device="cuda")
+    B, Sq, Hq, _ = x.q.shape
+    raw = torch.full((x.q.numel() + 8,), float("nan"), dtype=torch.bfloat16, device="cuda")
+    o = raw[8:].view(x.q.shape)
+    assert o.data_ptr() % 32 == 16
+    lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device="cuda")
+    fa.fa_fwd(x.q, x.k, x.v, o, lse, B, Hq, Hq, Sq, Sq, d, True, d ** -0.5, None)
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_error(clear=True) == 0
+    assert torch.isnan(raw[:8].float()).all()                # nothing written before O
+    ro, rl = oracle.forward(x.q.cpu(), x.k.cpu(), x.v.cpu(), d ** -0.5, True)
+    assert max_abs(o, ro) <= O_TOL
+    assert max_abs(lse, rl) <= LSE_TOL
