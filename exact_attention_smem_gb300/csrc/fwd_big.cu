@@ -427,6 +427,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) fwd_big_kernel(const __grid_co
       tc_fence_after();
       ++u_it;
       const float inv = lp > 0.f ? 1.0f / lp : 0.f;
+      // one row per thread: 32-byte stores where the row is 32-byte aligned
+      // (half the store instructions and line accesses), else 16-byte ones
+      const bool wide = (reinterpret_cast<uintptr_t>(orow) & 31) == 0;
 #pragma unroll 1
       for (int c = 0; c < D; c += 32) {
         uint32_t o[32];
@@ -435,11 +438,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) fwd_big_kernel(const __grid_co
 #pragma unroll
         for (int i = 0; i < 16; ++i) q[i] = pack_bf16x2(u2f(o[2 * i]) * inv, u2f(o[2 * i + 1]) * inv);
         if (valid) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c);
-          dst[0] = make_uint4(q[0], q[1], q[2], q[3]);
-          dst[1] = make_uint4(q[4], q[5], q[6], q[7]);
-          dst[2] = make_uint4(q[8], q[9], q[10], q[11]);
-          dst[3] = make_uint4(q[12], q[13], q[14], q[15]);
+          if (wide) {
+            const uint32_t q0[8] = {q[0], q[1], q[2], q[3], q[4], q[5], q[6], q[7]};
+            const uint32_t q1[8] = {q[8], q[9], q[10], q[11], q[12], q[13], q[14], q[15]};
+            st_global_v8(orow + c, q0);
+            st_global_v8(orow + c + 16, q1);
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(orow + c);
+            dst[0] = make_uint4(q[0], q[1], q[2], q[3]);
+            dst[1] = make_uint4(q[4], q[5], q[6], q[7]);
+            dst[2] = make_uint4(q[8], q[9], q[10], q[11]);
+            dst[3] = make_uint4(q[12], q[13], q[14], q[15]);
+          }
         }
       }
       if (valid) *lse_ptr = l > 0.f ? (m_ref + log2f(l)) * 0.69314718055994530942f : INFINITY;
