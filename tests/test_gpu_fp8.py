@@ -238,3 +238,23 @@ def test_fp8_forward_rescale_threshold(tau):
     assert _rel_l2_per_head(o, ro) <= O_REL_L2_FP8
     with pytest.raises(fa.FAError):
         fa.fa_debug_set("fp8_tau", 2.0)
+
+
+def test_fp8_output_16_byte_aligned_only():
+    """O at an address that is 16- but not 32-byte aligned: the same values,
+    bit for bit, as into an aligned buffer (whole tiles leave through TMA
+    stores, the rest per thread)."""
+    x = random_inputs(B=2, Hq=2, Hkv=2, Sq=300, Sk=300, d=128, seed=5, device="cuda")
+    q8, qs = fa.quantize_fp8(x.q, 0)
+    k8, ks = fa.quantize_fp8(x.k, 0)
+    v8, vs = fa.quantize_fp8(x.v, 1)
+    ref, ref_lse = fa.forward_fp8(q8, qs, k8, ks, v8, vs, causal=True, scale=128 ** -0.5)
+    raw = torch.full((x.q.numel() + 8,), float("nan"), dtype=torch.bfloat16, device="cuda")
+    o = raw[8:].view(x.q.shape)
+    assert o.data_ptr() % 32 == 16
+    lse = torch.empty_like(ref_lse)
+    fa.forward_fp8(q8, qs, k8, ks, v8, vs, causal=True, scale=128 ** -0.5, out=o, lse=lse)
+    torch.cuda.synchronize()
+    assert fa.fa_get_device_error(clear=True) == 0
+    assert torch.isnan(raw[:8].float()).all()
+    assert torch.equal(o, ref) and torch.equal(lse, ref_lse)
