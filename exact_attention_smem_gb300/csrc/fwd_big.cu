@@ -355,9 +355,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) fwd_big_kernel(const __grid_co
 #pragma unroll
         for (int i = 0; i < 4; ++i) mx[i] = u2f(sr[i]);
 #pragma unroll
-        for (int c = 4; c < BN; c += 8)
+        for (int c = 4; c < BN - 4; c += 8)          // [4, BN - 4) in pairs of four
 #pragma unroll
           for (int i = 0; i < 4; ++i) mx[i] = fmax3(mx[i], u2f(sr[c + i]), u2f(sr[c + 4 + i]));
+#pragma unroll
+        for (int i = 0; i < 4; ++i) mx[i] = fmaxf(mx[i], u2f(sr[BN - 4 + i]));
         const float m_blk = fmaxf(fmax3(mx[0], mx[1], mx[2]), mx[3]) * sl2;
         if (jb == 0) {
           m_ref = m_blk;
