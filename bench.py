@@ -10,6 +10,7 @@ causal; backward 2.5x forward.
   python bench.py --fp8 [--workload W]     # FP8 (e4m3) forward only, one GPU
   python bench.py --once [--workload W] [--bwd-mode M] [--fp8]
                                            # one step, no timing (profiler captures)
+  python bench.py --once --head-dim D      # the same at B=1, H=16, S=16384, causal, d=D
 
 Prints one JSON line (rank 0). N > 1 (torchrun) runs one independent replica
 per GPU (the path has no exchange step) and reports the whole-job aggregate.
@@ -303,7 +304,16 @@ def run_once(args):
     torch.cuda.set_device(0)
     fa.load()
     w = WORKLOADS[WORKLOAD]
-    x = make_inputs(w, "cuda")
+    if args.head_dim is not None:
+        # the head-dim shape: B=1, H=16, S=16384, causal, seeded N(0,1) bf16
+        import dataclasses
+        from attn_inputs import random_inputs
+        w = dataclasses.replace(w, B=1, Hq=16, Hkv=16, Sq=16384, Sk=16384, d=args.head_dim,
+                                causal=True, scale=args.head_dim ** -0.5)
+        x = random_inputs(B=1, Hq=16, Hkv=16, Sq=16384, Sk=16384, d=args.head_dim, seed=16,
+                          device="cuda")
+    else:
+        x = make_inputs(w, "cuda")
     if args.fp8:
         q8, qs = fa.quantize_fp8(x.q, 0)
         k8, ks = fa.quantize_fp8(x.k, 0)
@@ -563,11 +573,15 @@ def main():
                          "others serve profiling captures and measurements)")
     ap.add_argument("--once", action="store_true",
                     help="run one forward + backward and exit (for profiler captures)")
+    ap.add_argument("--head-dim", type=int, default=None, choices=[64, 128, 192, 256],
+                    help="with --once: run B=1, H=16, S=16384, causal at this head dim instead")
     ap.add_argument("--bwd-mode", type=int, default=None, choices=[0, 1, 2],
                     help="backward form (fa_debug_set bwd_mode; default: the library's)")
     args = ap.parse_args()
     if args.workload == "varlen16_causal" and not args.once:
         ap.error("the packed workload runs with --once only")
+    if args.head_dim is not None and (not args.once or args.fp8):
+        ap.error("--head-dim goes with --once (bf16 forward + backward)")
     if args.bwd_mode is not None:
         import exact_attention_smem_gb300 as fa
         fa.fa_debug_set("bwd_mode", args.bwd_mode)
