@@ -57,7 +57,10 @@ struct Cfg {
   static constexpr int BAR_OFF = KV_OFF + NSTAGE * TILE_BYTES;
   static constexpr int B_QFULL = 0, B_QEMPTY = 1, B_KVFULL = 2, B_KVEMPTY = 2 + NSTAGE,
                        B_SFULL = 2 + 2 * NSTAGE, B_PFULL = B_SFULL + 2, B_OFULL = B_PFULL + 2,
-                       B_DRAIN = B_OFULL + 2, NBAR = B_DRAIN + 1;
+                       B_DRAIN = B_OFULL + 2,
+                       // tile 1's own Q pair when the tiles load separately
+                       // (B_QFULL / B_QEMPTY then serve tile 0 alone)
+                       B_QFULL1 = B_DRAIN + 1, B_QEMPTY1 = B_DRAIN + 2, NBAR = B_DRAIN + 3;
   static constexpr int MISC_OFF = BAR_OFF + NBAR * 8;
   static constexpr int CU_OFF = MISC_OFF + 16;
   // O write-out staging: one 128-row x 64-column chunk (128B swizzle) per softmax warpgroup
@@ -124,6 +127,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) fwd_kernel(const __grid_consta
   if (threadIdx.x == 0) {
     mbar_init(BAR(C::B_QFULL), 1);
     mbar_init(BAR(C::B_QEMPTY), 1);
+    mbar_init(BAR(C::B_QFULL1), 1);
+    mbar_init(BAR(C::B_QEMPTY1), 1);
     for (int s = 0; s < C::NSTAGE; ++s) {
       mbar_init(BAR(C::B_KVFULL + s), 1);
       mbar_init(BAR(C::B_KVEMPTY + s), 1);
@@ -177,6 +182,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) fwd_kernel(const __grid_consta
       w.init(spec);
       uint32_t kv_it = 0;
       int u_it = 0;
+      uint32_t q_cnt[2] = {0, 0};           // Q loads issued on each Q pair
+      const bool split = p.split_q != 0;
       bool ok = true;
       for (int k = 0; ok; ++k) {
         Unit u;
@@ -185,15 +192,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) fwd_kernel(const __grid_consta
         if (n == 0) continue;
         const int kvh = u.head / group;
         const int q_row = u.q_start + u.m * UNIT_ROWS;
-        if (u_it > 0) {
-          ok = mbar_wait(BAR(C::B_QEMPTY), (u_it - 1) & 1, wc, SITE_FWD_Q_EMPTY);
-          if (!ok) break;
+        for (int t = 0; t < (split ? 2 : 1); ++t) {
+          const uint32_t full = BAR(t ? C::B_QFULL1 : C::B_QFULL);
+          if (u_it > 0) {
+            ok = mbar_wait(BAR(t ? C::B_QEMPTY1 : C::B_QEMPTY), (u_it - 1) & 1, wc,
+                           SITE_FWD_Q_EMPTY);
+            if (!ok) break;
+          }
+          mbar_arrive_expect_tx(full, split ? C::TILE_BYTES : 2 * C::TILE_BYTES);
+          for (int tt = t; tt < (split ? t + 1 : 2); ++tt)
+            for (int c = 0; c < C::CHUNKS; ++c)
+              tma_load_3d(base + C::Q_OFF + tt * C::TILE_BYTES + c * C::CHUNK_BYTES, &p.tm_q,
+                          full, c * 64, u.head, q_row + tt * BM);
+          ++q_cnt[t];
         }
-        mbar_arrive_expect_tx(BAR(C::B_QFULL), 2 * C::TILE_BYTES);
-        for (int t = 0; t < 2; ++t)
-          for (int c = 0; c < C::CHUNKS; ++c)
-            tma_load_3d(base + C::Q_OFF + t * C::TILE_BYTES + c * C::CHUNK_BYTES, &p.tm_q,
-                        BAR(C::B_QFULL), c * 64, u.head, q_row + t * BM);
+        if (!ok) break;
         ++u_it;
         for (int j = 0; j < n && ok; ++j) {
           for (int which = 0; which < 2; ++which) {
@@ -217,7 +230,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) fwd_kernel(const __grid_consta
         // let the copies already issued land before the CTA exits
         for (uint32_t i = kv_it > (uint32_t)C::NSTAGE ? kv_it - C::NSTAGE : 0; i < kv_it; ++i)
           drain_wait(BAR(C::B_KVFULL + i % C::NSTAGE), (i / C::NSTAGE) & 1, 100000000ull);
-        if (u_it > 0) drain_wait(BAR(C::B_QFULL), (u_it - 1) & 1, 100000000ull);
+        for (int t = 0; t < 2; ++t)
+          if (q_cnt[t] > 0)
+            drain_wait(BAR(t ? C::B_QFULL1 : C::B_QFULL), (q_cnt[t] - 1) & 1, 100000000ull);
       }
     }
   } else if (warp == MMA_WARP) {
@@ -231,25 +246,36 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) fwd_kernel(const __grid_consta
       const uint32_t q0 = base + C::Q_OFF, q1 = q0 + C::TILE_BYTES, kvb = base + C::KV_OFF;
       const uint32_t tS0 = tmem + C::TM_S, tS1 = tS0 + 128;
       const uint32_t tO0 = tmem + C::TM_O, tO1 = tO0 + D;
+      const bool split = p.split_q != 0;
+      // tile 1's Q empty barrier: its own pair when the tiles load separately
+      const uint32_t q_empty1 = BAR(split ? C::B_QEMPTY1 : C::B_QEMPTY);
       for (int k = 0; ok; ++k) {
         Unit u;
         if (!w.seek(snake_index(k, G, cta), u)) break;
         const int n = u.cost;
         if (n == 0) continue;
-        ok = mbar_wait(BAR(C::B_QFULL), u_it & 1, wc, SITE_FWD_Q_FULL);
-        if (!ok) break;
-        ++u_it;
         int sk = kv_it % C::NSTAGE;
-        ok = mbar_wait(BAR(C::B_KVFULL + sk), (kv_it / C::NSTAGE) & 1, wc, SITE_FWD_KV_FULL);
-        if (!ok) break;
+        if (split) {
+          ok = mbar_wait3(BAR(C::B_QFULL), u_it & 1, SITE_FWD_Q_FULL, BAR(C::B_QFULL1),
+                          u_it & 1, SITE_FWD_Q_FULL, BAR(C::B_KVFULL + sk),
+                          (kv_it / C::NSTAGE) & 1, SITE_FWD_KV_FULL, wc);
+          if (!ok) break;
+        } else {
+          ok = mbar_wait(BAR(C::B_QFULL), u_it & 1, wc, SITE_FWD_Q_FULL);
+          if (!ok) break;
+          ok = mbar_wait(BAR(C::B_KVFULL + sk), (kv_it / C::NSTAGE) & 1, wc, SITE_FWD_KV_FULL);
+          if (!ok) break;
+        }
+        ++u_it;
         tc_fence_after();
         issue_s<D>(tS0, q0, kvb + sk * C::TILE_BYTES);
         tc_commit(BAR(C::B_SFULL + 0));
+        if (split && n == 1) tc_commit(BAR(C::B_QEMPTY));
         issue_s<D>(tS1, q1, kvb + sk * C::TILE_BYTES);
         tc_commit(BAR(C::B_SFULL + 1));
         tc_commit(BAR(C::B_KVEMPTY + sk));
         ++kv_it;
-        if (n == 1) tc_commit(BAR(C::B_QEMPTY));
+        if (n == 1) tc_commit(q_empty1);
         for (int j = 0; j < n; ++j) {
           // sync point 1: V_j, P_0(j) and (if any) K_{j+1}, probed together
           const int sv = kv_it % C::NSTAGE;
@@ -267,6 +293,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) fwd_kernel(const __grid_consta
           if (more) {
             issue_s<D>(tS0, q0, kvb + sk2 * C::TILE_BYTES);
             tc_commit(BAR(C::B_SFULL + 0));
+            if (split && j + 2 == n) tc_commit(BAR(C::B_QEMPTY));
           } else {
             tc_commit(BAR(C::B_OFULL + 0));
           }
@@ -281,7 +308,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) fwd_kernel(const __grid_consta
             tc_commit(BAR(C::B_SFULL + 1));
             tc_commit(BAR(C::B_KVEMPTY + sk2));
             ++kv_it;
-            if (j + 2 == n) tc_commit(BAR(C::B_QEMPTY));
+            if (j + 2 == n) tc_commit(q_empty1);
           } else {
             tc_commit(BAR(C::B_OFULL + 1));
           }

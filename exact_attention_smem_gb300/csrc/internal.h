@@ -40,6 +40,7 @@ struct Knobs {
   long long timeout_ns = 2000000000LL;
   int grid_override = 0;         // >0: persistent grid size (schedule permutation tests)
   int fwd_hblock = 0;            // >0: forward heads per scheduler group (0: one group)
+  int fwd_split_q = -1;          // forward Q barriers per tile: 1 on, 0 off, -1 automatic
   int bwd_hblock = 0;            // >0: dK/dV-pass KV heads per scheduler group (0: automatic)
   int bwd_hblock_q = 0;          // >0: dQ-pass query heads per scheduler group (0: automatic)
   cudaEvent_t ev[2][2] = {{nullptr, nullptr}, {nullptr, nullptr}};  // [fwd|bwd][start|stop]
@@ -83,6 +84,7 @@ struct FwdParams {
   float scale_log2;              // softmax scale * log2(e)
   float tau;                     // rescale threshold (base 2)
   int hblock;                    // heads per scheduler group
+  int split_q;                   // bf16 forward, d <= 128: one Q full/empty pair per tile
   int* err;
   unsigned long long timeout_ns;
   // FP8 forward only (else unused): e4m3 inputs with per-block scales

@@ -255,6 +255,11 @@ FA_API int fa_get_device_error(int* code, int clear);
  *                dK/dV pass on CTA pairs (cta_group::2, head dim 128), 0 one
  *                pass with fp32 dQ atomics and a convert pass (head dim 128)
  *   "fwd_hblock" forward heads per scheduler group (0 = all heads, default)
+ *   "fwd_split_q" bf16 forward (head dim <= 128): 1 loads each of a unit's two
+ *                Q tiles on its own barrier pair (tile 0's next Q as soon as
+ *                tile 0's last S is done), 0 both on one pair, -1 automatic
+ *                (default: 1 for dense layouts with at most 4096 keys). Results
+ *                are bit-identical either way.
  *   "bwd_hblock" dK/dV pass: KV heads per scheduler group (0 = automatic)
  *   "bwd_hblock_q" dQ pass: query heads per scheduler group (0 = automatic)
  * Returns FA_OK or FA_ERR_INVALID_ARG. Process-wide; not thread-safe with

@@ -22,6 +22,7 @@ def _dev():
     fa.fa_debug_set("grid", 0)
     fa.fa_debug_set("tau", 0)
     fa.fa_debug_set("poly8", 0)
+    fa.fa_debug_set("fwd_split_q", -1)
 
 
 def _run(x, causal, scale, cu=None):
@@ -166,3 +167,46 @@ def test_output_16_byte_aligned_only(d):
     ro, rl = oracle.forward(x.q.cpu(), x.k.cpu(), x.v.cpu(), d ** -0.5, True)
     assert max_abs(o, ro) <= O_TOL
     assert max_abs(lse, rl) <= LSE_TOL
+
+
+@pytest.mark.parametrize("case", ["causal", "noncausal_d64", "sq_ne_sk", "gqa", "packed",
+                                  "long_units"])
+def test_split_q_barriers_bitwise_invisible(case):
+    """The two ways of loading a unit's two Q tiles (one barrier pair for both,
+    or one pair per tile so that tile 0's next Q loads early) give the same
+    bits, on dense, GQA and packed layouts (the automatic choice uses the
+    per-tile form only for dense layouts with at most 4096 keys), and the
+    per-tile form matches the oracle."""
+    cu = None
+    if case == "causal":
+        x, causal = random_inputs(B=2, Hq=4, Hkv=4, Sq=700, Sk=700, d=128, seed=95,
+                                  device="cuda"), True
+    elif case == "noncausal_d64":
+        x, causal = random_inputs(B=2, Hq=4, Hkv=4, Sq=300, Sk=300, d=64, seed=96,
+                                  device="cuda"), False
+    elif case == "sq_ne_sk":
+        x, causal = random_inputs(B=2, Hq=2, Hkv=2, Sq=300, Sk=900, d=128, seed=97,
+                                  device="cuda"), True
+    elif case == "gqa":
+        x, causal = random_inputs(B=1, Hq=8, Hkv=2, Sq=513, Sk=513, d=128, seed=98,
+                                  device="cuda"), True
+    elif case == "packed":
+        x = random_inputs(B=None, Hq=4, Hkv=4, Sq=None, Sk=None, d=128, seed=99,
+                          lengths=[1, 127, 128, 129, 300, 700, 256], device="cuda")
+        causal, cu = True, x.cu_seqlens
+    else:   # a few units of many blocks each (S = 4096: the largest automatic case)
+        x, causal = random_inputs(B=1, Hq=2, Hkv=2, Sq=4096, Sk=4096, d=128, seed=100,
+                                  device="cuda"), True
+    scale = 1.0 / math.sqrt(x.q.shape[-1])
+    outs = []
+    try:
+        for mode in (0, 1):
+            fa.fa_debug_set("fwd_split_q", mode)
+            outs.append(_run(x, causal, scale, cu))
+    finally:
+        fa.fa_debug_set("fwd_split_q", -1)
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+    if case != "long_units":
+        ro, rl = oracle.forward(x.q.cpu(), x.k.cpu(), x.v.cpu(), scale, causal,
+                                cu_seqlens=None if cu is None else cu.cpu())
+        assert max_abs(outs[1][0], ro) <= O_TOL and max_abs(outs[1][1], rl) <= LSE_TOL
