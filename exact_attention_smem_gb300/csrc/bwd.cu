@@ -742,7 +742,7 @@ static cudaError_t launch_main(const BwdParams& p, int grid, cudaStream_t stream
 }
 
 cudaError_t launch_bwd(const BwdParams& p, const BwdAux& aux, int d, int grid, int grid_q,
-                       cudaStream_t stream, int poly8, int mode) {
+                       cudaStream_t stream, int poly8, int mode, int pdl) {
   if (mode == 0 && d != 128) return cudaErrorNotSupported;
   if (d != 64 && d != 128 && d != 192 && d != 256) return cudaErrorNotSupported;
   const long long rows = (long long)p.total_q * p.Hq;
@@ -772,7 +772,7 @@ cudaError_t launch_bwd(const BwdParams& p, const BwdAux& aux, int d, int grid, i
         mode == 2 ? launch_bwd_pair(p, p.total_k > 0 ? grid : 0, p.total_q > 0 ? grid_q : 0,
                                     stream, poly8)
                   : launch_bwd_split(p, d, p.total_k > 0 ? grid : 0, p.total_q > 0 ? grid_q : 0,
-                                     stream, poly8);
+                                     stream, poly8, pdl);
     if (ev1) cudaEventRecord(ev1, stream);
     return e;
   }

@@ -301,6 +301,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dkdv_kernel(const __grid_const
   constexpr int BMS = C::BMS;                           // query rows per step
   constexpr int COLS = BMS / 2;                         // score columns per warpgroup
   constexpr int DA = C::DA, HALVES = C::HALVES;         // unit head = KV head * HALVES + half
+  // a dQ pass launched as this grid's programmatic dependent may start
+  // launching now; its CTAs take SMs as this grid's CTAs exit
+  griddep_launch_dependents();
   extern __shared__ __align__(1024) uint8_t smem_al[];
   uint32_t base;                                        // opaque to the compiler: checked, not assumed
   asm volatile("{\n\t.reg .u64 t;\n\tcvta.to.shared.u64 t, %1;\n\tcvt.u32.u64 %0, t;\n\t}"
@@ -1430,6 +1433,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dq_kernel(const __grid_constan
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+  // launched as the dK/dV pass's dependent: this grid completes only after
+  // that one has (no wait at all when launched the ordinary way)
+  if (threadIdx.x == 0) griddep_wait();
 #undef BAR
 }
 
@@ -1439,7 +1445,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) dq_kernel(const __grid_constan
 // passes read Q/dO and K/V through tensor maps with different box heights).
 template <int D, int POLY8>
 static cudaError_t launch_split_pair(const BwdParams& p_kv, const BwdParams& p_q, int grid_kv,
-                                     int grid_q, cudaStream_t stream) {
+                                     int grid_q, cudaStream_t stream, int pdl) {
   auto kkv = bsplit::dkdv_kernel<D, POLY8>;
   auto kq = bsplit::dq_kernel<D, POLY8>;
   const int s_kv = bsplit::CfgKV<D>::SMEM_BYTES, s_q = bsplit::CfgQ<D>::SMEM_BYTES;
@@ -1453,8 +1459,22 @@ static cudaError_t launch_split_pair(const BwdParams& p_kv, const BwdParams& p_q
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (grid_q > 0) {
-    kq<<<grid_q, bsplit::NUM_THREADS, s_q, stream>>>(p_q);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    // After a dK/dV pass, as its programmatic dependent: the dQ pass reads only
+    // what the preprocess wrote (complete before the dK/dV pass began) and
+    // shares nothing with the dK/dV pass, so its CTAs may start on the SMs the
+    // dK/dV CTAs leave; each dQ CTA waits for the dK/dV grid before it exits,
+    // so the backward completes only once both passes have.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid_q, 1, 1);
+    cfg.blockDim = dim3(bsplit::NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = s_q;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl && grid_kv > 0 ? 1 : 0;
+    if ((e = cudaLaunchKernelEx(&cfg, kq, p_q)) != cudaSuccess) return e;
   }
   return cudaSuccess;
 }
@@ -1510,20 +1530,20 @@ cudaError_t launch_bwd_pair(const BwdParams& p, int grid_pair, int grid_q, cudaS
 
 // The two passes of the split backward (after the preprocess pass of bwd.cu).
 cudaError_t launch_bwd_split(const BwdParams& p, int d, int grid_kv, int grid_q,
-                             cudaStream_t stream, int poly8) {
+                             cudaStream_t stream, int poly8, int pdl) {
   if (d == 128) {
     switch (poly8) {
-      case 0: return launch_split_pair<128, 0>(p, p, grid_kv, grid_q, stream);
-      case 2: return launch_split_pair<128, 2>(p, p, grid_kv, grid_q, stream);
-      case 4: return launch_split_pair<128, 4>(p, p, grid_kv, grid_q, stream);
+      case 0: return launch_split_pair<128, 0>(p, p, grid_kv, grid_q, stream, pdl);
+      case 2: return launch_split_pair<128, 2>(p, p, grid_kv, grid_q, stream, pdl);
+      case 4: return launch_split_pair<128, 4>(p, p, grid_kv, grid_q, stream, pdl);
       default: return cudaErrorInvalidValue;
     }
   }
   if (d == 64) {
     switch (poly8) {
-      case 0: return launch_split_pair<64, 0>(p, p, grid_kv, grid_q, stream);
-      case 2: return launch_split_pair<64, 2>(p, p, grid_kv, grid_q, stream);
-      case 4: return launch_split_pair<64, 4>(p, p, grid_kv, grid_q, stream);
+      case 0: return launch_split_pair<64, 0>(p, p, grid_kv, grid_q, stream, pdl);
+      case 2: return launch_split_pair<64, 2>(p, p, grid_kv, grid_q, stream, pdl);
+      case 4: return launch_split_pair<64, 4>(p, p, grid_kv, grid_q, stream, pdl);
       default: return cudaErrorInvalidValue;
     }
   }
@@ -1536,16 +1556,16 @@ cudaError_t launch_bwd_split(const BwdParams& p, int d, int grid_kv, int grid_q,
     p_q.tm_v = p.tm_v2;
     if (d == 256) {
       switch (poly8) {
-        case 0: return launch_split_pair<256, 0>(p_kv, p_q, grid_kv, grid_q, stream);
-        case 2: return launch_split_pair<256, 2>(p_kv, p_q, grid_kv, grid_q, stream);
-        case 4: return launch_split_pair<256, 4>(p_kv, p_q, grid_kv, grid_q, stream);
+        case 0: return launch_split_pair<256, 0>(p_kv, p_q, grid_kv, grid_q, stream, pdl);
+        case 2: return launch_split_pair<256, 2>(p_kv, p_q, grid_kv, grid_q, stream, pdl);
+        case 4: return launch_split_pair<256, 4>(p_kv, p_q, grid_kv, grid_q, stream, pdl);
         default: return cudaErrorInvalidValue;
       }
     }
     switch (poly8) {
-      case 0: return launch_split_pair<192, 0>(p_kv, p_q, grid_kv, grid_q, stream);
-      case 2: return launch_split_pair<192, 2>(p_kv, p_q, grid_kv, grid_q, stream);
-      case 4: return launch_split_pair<192, 4>(p_kv, p_q, grid_kv, grid_q, stream);
+      case 0: return launch_split_pair<192, 0>(p_kv, p_q, grid_kv, grid_q, stream, pdl);
+      case 2: return launch_split_pair<192, 2>(p_kv, p_q, grid_kv, grid_q, stream, pdl);
+      case 4: return launch_split_pair<192, 4>(p_kv, p_q, grid_kv, grid_q, stream, pdl);
       default: return cudaErrorInvalidValue;
     }
   }

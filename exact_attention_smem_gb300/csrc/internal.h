@@ -43,6 +43,7 @@ struct Knobs {
   int fwd_split_q = -1;          // forward Q barriers per tile: 1 on, 0 off, -1 automatic
   int bwd_hblock = 0;            // >0: dK/dV-pass KV heads per scheduler group (0: automatic)
   int bwd_hblock_q = 0;          // >0: dQ-pass query heads per scheduler group (0: automatic)
+  int bwd_pdl = -1;              // dQ pass as the dK/dV pass's dependent: 1 on, 0 off, -1 auto
   cudaEvent_t ev[2][2] = {{nullptr, nullptr}, {nullptr, nullptr}};  // [fwd|bwd][start|stop]
   long long* trace = nullptr;    // device buffer for the backward role timeline
 };
@@ -147,10 +148,13 @@ struct BwdAux {                  // inputs of the preprocess / convert passes
 };
 // mode 1: preprocess, dK/dV pass (grid), dQ pass (grid_q); mode 0: preprocess,
 // one-pass kernel (grid), convert.
+// pdl: the two-pass form launches its dQ pass as a programmatic dependent of
+// the dK/dV pass (the passes share no data), so dQ CTAs take SMs as dK/dV
+// CTAs finish.
 cudaError_t launch_bwd(const BwdParams& p, const BwdAux& aux, int d, int grid, int grid_q,
-                       cudaStream_t stream, int poly8, int mode);
+                       cudaStream_t stream, int poly8, int mode, int pdl);
 cudaError_t launch_bwd_split(const BwdParams& p, int d, int grid_kv, int grid_q,
-                             cudaStream_t stream, int poly8);
+                             cudaStream_t stream, int poly8, int pdl);
 cudaError_t launch_bwd_pair(const BwdParams& p, int grid_pair, int grid_q, cudaStream_t stream,
                             int poly8);
 int dkdv_pair_max_clusters();

@@ -159,6 +159,15 @@ __device__ __forceinline__ void tma_store_commit() {
 __device__ __forceinline__ void tma_store_wait_all() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
+// Programmatic dependent launch. A grid lets the next kernel of its stream
+// (launched with programmatic stream serialization) start launching once all
+// its CTAs have executed launch_dependents or exited; wait blocks until the
+// grids a kernel depends on have completed and their memory is visible (it
+// returns at once in a kernel launched the ordinary way).
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 // 32-byte global store (256-bit vector; the address must be 32-byte aligned).
 __device__ __forceinline__ void st_global_v8(void* ptr, const uint32_t (&v)[8]) {
   asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(ptr), "r"(v[0]),

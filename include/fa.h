@@ -262,6 +262,12 @@ FA_API int fa_get_device_error(int* code, int clear);
  *                are bit-identical either way.
  *   "bwd_hblock" dK/dV pass: KV heads per scheduler group (0 = automatic)
  *   "bwd_hblock_q" dQ pass: query heads per scheduler group (0 = automatic)
+ *   "bwd_pdl"    two-pass backward: 1 launches the dQ pass as a programmatic
+ *                dependent of the dK/dV pass, so that its CTAs start on the
+ *                SMs the dK/dV pass leaves (the passes share no data; the call
+ *                still completes only when both have); 0 launches it the
+ *                ordinary way; -1 automatic (default: 1 for dense layouts with
+ *                at most 4096 keys). Results are bit-identical.
  * Returns FA_OK or FA_ERR_INVALID_ARG. Process-wide; not thread-safe with
  * concurrent launches.
  */

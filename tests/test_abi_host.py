@@ -183,7 +183,8 @@ def test_every_knob_is_documented_and_accepted(lib):
     assert accepted == documented
     defaults = {"tau": 0.0, "poly8": 0.0, "bwd_poly8": 0.0, "fp8_poly8": 0.0, "fp8_tau": 1.5,
                 "timeout_ms": 2000.0, "grid": 0.0, "bwd_mode": 1.0, "fwd_hblock": 0.0,
-                "bwd_hblock": 0.0, "bwd_hblock_q": 0.0, "fwd_split_q": -1.0}
+                "bwd_hblock": 0.0, "bwd_hblock_q": 0.0, "fwd_split_q": -1.0,
+                "bwd_pdl": -1.0}
     assert set(defaults) == accepted
     for k, v in defaults.items():                     # every key takes its default value
         assert lib.fa_debug_set(k.encode(), v) == 0, k
