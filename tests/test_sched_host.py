@@ -167,3 +167,20 @@ def test_varlen_balance_near_lpt_bound():
         assert max(loads) <= 1.05 * mean, (kind, max(loads) / mean)
         greedy = _graham([u[3] for units in per for u in units], G)
         assert max(loads) <= 1.01 * greedy, (kind, max(loads) / greedy)
+
+
+def test_short_causal_balance_matches_greedy():
+    """The short causal workload (B=4, H=16, S=2048) on 152 CTAs, each kernel
+    with the head grouping it uses there (one group: the K/V and Q/dO of all
+    heads fit L2): the static snake deal's largest per-CTA cost equals that of
+    Graham's greedy list scheduling. For the forward that is 32 blocks, the
+    optimum: every unit costs an even number of blocks and the mean is 30.3."""
+    G = 152
+    for kind in (0, 2, 3):
+        per = [fa_sched_list(kind, 4, None, 2048, 2048, 16, True, G, b, 16) for b in range(G)]
+        loads = [sum(u[3] for u in units) for units in per]
+        costs = [u[3] for units in per for u in units]
+        assert len(costs) == (512 if kind == 0 else 1024)
+        assert max(loads) == _graham(costs, G), kind
+        if kind == 0:
+            assert all(c % 2 == 0 for c in costs) and max(loads) == 32
